@@ -1,0 +1,168 @@
+/*
+ * l2decode.h -- C ABI of the B300 (sm_103a) fp32 Llama-2 decode library.
+ *
+ * What it computes. One decode step of the Llama 2 architecture in fp32, as
+ * the llama2.c pages describe the single-file C engine: in
+ * "llama2.c｜Baby LLaMA-openAI维基百科" (openai.wiki), introduction, a
+ * Llama-2 model trained in PyTorch has its weights saved as a raw binary file
+ * and run by a ~500-line C file in fp32 with the architecture hard-coded; the
+ * 新智元 llama2.c article (m.greenbasetech.com) says the same in the paragraph
+ * before "感受魔力" and runs it as `./run out/model.bin` under "使用指南".
+ * Per token: embedding row, then per layer RMSNorm, Q/K/V projections, RoPE,
+ * causal multi-head attention over a KV cache, output projection + residual,
+ * RMSNorm, SwiGLU feed-forward (W1 gate, W3 up, W2 down) + residual; then a
+ * final RMSNorm, the vocabulary classifier and the greedy argmax. The pages
+ * name the architecture without writing its formulas; the readings taken are:
+ *   RMSNorm  out_i = g_i * x_i / sqrt(mean(x^2) + eps)
+ *   RoPE     adjacent pairs (2i, 2i+1) of each head turn by
+ *            pos * theta^(-2i/head_dim) (angles evaluated in double)
+ *   scores   (q . k) / sqrt(head_dim), softmax over positions 0..pos
+ *   SwiGLU   silu(W1 x) * (W3 x), silu(z) = z / (1 + exp(-z))
+ *   greedy   the lowest index wins a tie
+ *
+ * Threading and streams. A handle is not thread-safe. Every call is
+ * synchronous unless it takes a stream (the *_device calls), in which case the
+ * work is queued on that stream and the call returns without waiting.
+ *
+ * Errors. Every int-returning call returns L2_OK (0) or a negative code below;
+ * l2_last_error() gives a one-line description of the last failure on that
+ * handle. No call aborts the process, traps, or hangs: device-side waits are
+ * bounded and report L2_ETIMEOUT.
+ */
+#ifndef L2DECODE_H
+#define L2DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library are exported explicitly; everything else in it
+ * is hidden. */
+#if defined(__GNUC__)
+#define L2_API __attribute__((visibility("default")))
+#else
+#define L2_API
+#endif
+
+#define L2_OK 0
+#define L2_EINVAL (-1)   /* bad config or argument (range, size, batch)          */
+#define L2_ENOMEM (-2)   /* device or pinned-host allocation failed              */
+#define L2_ECUDA (-3)    /* a CUDA runtime call failed (no device, launch error) */
+#define L2_ETIMEOUT (-4) /* a bounded device-side wait gave up                   */
+#define L2_EBLOB (-5)    /* blob size does not match the config                  */
+
+/* Model configuration. Shapes from the pages: dim 288 / 6 layers / 6 heads
+ * (openai.wiki introduction) and dim 512 / 8 layers / 8 heads / context 1024
+ * (openai.wiki "训练示例"); larger shapes follow the same architecture.
+ * Requirements: all sizes > 0; dim % n_heads == 0; head_dim = dim / n_heads
+ * even and <= 256; n_heads % n_kv_heads == 0; dim % 4 == 0;
+ * hidden_dim % 4 == 0; 1 <= max_batch <= 1024. */
+typedef struct {
+    int32_t dim;               /* d, width of the residual stream            */
+    int32_t hidden_dim;        /* F, SwiGLU hidden width                     */
+    int32_t n_layers;          /* L                                          */
+    int32_t n_heads;           /* H query heads                              */
+    int32_t n_kv_heads;        /* KVH key/value heads (H % KVH == 0)         */
+    int32_t vocab_size;        /* V                                          */
+    int32_t seq_len;           /* S, KV-cache length (positions 0..S-1)      */
+    float rope_theta;          /* 10000 in the Llama 2 architecture          */
+    float norm_eps;            /* 1e-5                                       */
+    int32_t max_batch;         /* sequences one handle can decode at once    */
+    int32_t shared_classifier; /* 1: classifier = embedding table (no Wcls)  */
+} l2_config;
+
+typedef struct l2_handle l2_handle;
+
+/* Floats in a weight blob for cfg; 0 for an invalid config.
+ * Blob layout (the pages say only "raw binary file"; this is the documented
+ * order), fp32 little-endian, contiguous, every matrix row-major [out][in]
+ * acting as y = W x, kvd = n_kv_heads * head_dim:
+ *   E[V][d], g_att[L][d], Wq[L][d][d], Wk[L][kvd][d], Wv[L][kvd][d],
+ *   Wo[L][d][d], g_ffn[L][d], W1[L][F][d], W2[L][d][F], W3[L][F][d],
+ *   g_final[d], Wcls[V][d] (absent when shared_classifier = 1). */
+L2_API size_t l2_blob_floats(const l2_config* cfg);
+
+/* Creates a handle on the current CUDA device: validates cfg, allocates the
+ * weights, KV caches and run state, copies blob (host memory, blob_floats
+ * floats, read only during the call; the caller keeps ownership) to the
+ * device and re-tiles it into the streaming layout, and builds the per-step
+ * CUDA graph. *out receives the handle (NULL on failure).
+ * Errors: L2_EINVAL (cfg), L2_EBLOB (size), L2_ENOMEM, L2_ECUDA. */
+L2_API int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_handle** out);
+
+/* One decode step for B sequences; sequence b consumes token tokens[b] at
+ * position pos[b], writes its KV-cache slot pos[b] and attends over slots
+ * 0..pos[b] (slots below pos[b] must hold that sequence's earlier steps;
+ * re-running a lower pos overwrites its slot). Sequence b uses cache b.
+ * tokens, pos: host arrays [B]. logits_out: host [B][V] floats or NULL.
+ * Errors: L2_EINVAL for B < 1, B > max_batch, a token outside [0, V) or a
+ * position outside [0, S). Synchronous. */
+L2_API int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t B,
+               float* logits_out);
+
+/* Same as l2_forward with device buffers owned by the caller (for example
+ * PyTorch tensors): d_tokens, d_pos int32 [B], d_logits fp32 [B][V] or NULL.
+ * Queued on `stream` (a cudaStream_t, NULL = legacy default stream); returns
+ * without waiting. Device values are not range-checked: tokens are clamped to
+ * [0, V) and positions to [0, S) on the device. */
+L2_API int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_pos, int32_t B,
+                      float* d_logits, void* stream);
+
+/* Greedy generation for one sequence (cache 0), the loop of the single-file
+ * engine (新智元 article, "使用指南": `./run out/model.bin` streams token ids):
+ * forwards at positions 0 .. n_prompt+steps-2; position p consumes prompt[p]
+ * while p < n_prompt, afterwards the previous argmax; no stop token.
+ * out_tokens[k] (host, [steps]) is the argmax at position n_prompt-1+k.
+ * The token stays on the device between steps; one copy in, one copy out.
+ * Errors: L2_EINVAL for n_prompt < 1, steps < 1, n_prompt+steps-1 > S, or a
+ * prompt id outside [0, V). Synchronous. */
+L2_API int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
+                int32_t* out_tokens);
+
+/* l2_generate with device buffers: d_prompt int32 [n_prompt], d_out int32
+ * [steps]; queued on `stream`, returns without waiting. Host-side checks as
+ * l2_generate; device prompt ids are not range-checked (clamped). */
+L2_API int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt, int32_t steps,
+                       int32_t* d_out, void* stream);
+
+/* Greedy generation for B independent sequences in lockstep (batched
+ * decode). prompts: host, the B prompts concatenated; lens: host [B], each
+ * >= 1; out_tokens: host [B][steps]. Sequence b runs forwards at positions
+ * 0 .. lens[b]+steps-2 of its own cache; a sequence that has produced its
+ * `steps` tokens idles while the others finish.
+ * Errors: L2_EINVAL for B < 1 or > max_batch, a length < 1,
+ * lens[b]+steps-1 > S, or an id outside [0, V). Synchronous. */
+L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
+                      int32_t steps, int32_t* out_tokens);
+
+/* Clears KV cache `seq` (-1: all caches) to zero. Errors: L2_EINVAL. */
+L2_API int l2_reset(l2_handle* h, int32_t seq);
+
+/* Frees every device and host resource of h. NULL is accepted. */
+L2_API void l2_destroy(l2_handle* h);
+
+/* Text of the last error on h (or of the last failed l2_create when h is
+ * NULL). The pointer stays valid until the next call on h. */
+L2_API const char* l2_last_error(const l2_handle* h);
+
+/* Measurement hook: launches one kernel kind of the step `iters` times on
+ * `stream`, cycling over layers, bracketed by CUDA events, and writes the mean
+ * duration of one launch in milliseconds to *ms. kind: 0 QKV+RoPE,
+ * 1 attention, 2 Wo+residual, 3 W1/W3+SwiGLU, 4 W2+residual,
+ * 5 classifier+argmax. It reads and writes the handle's own run state (the
+ * KV cache contents are left as they were, except slot `pos` of cache 0).
+ * Errors: L2_EINVAL, L2_ECUDA. Synchronous. */
+L2_API int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
+                   float* ms);
+
+/* Algorithmic bytes one launch of `kind` reads and writes at position pos
+ * (weights + activations + KV rows), batch 1. 0 for an invalid kind. */
+L2_API double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* L2DECODE_H */

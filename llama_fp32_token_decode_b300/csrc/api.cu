@@ -1,0 +1,610 @@
+// api.cu -- the C ABI of include/l2decode.h: handle lifetime, validation,
+// weight upload + layout pass, per-forward CUDA graphs, and the decode loops.
+//
+// Decode loop (llama2.c pages: `./run out/model.bin` streams one token per
+// forward in the single-file fp32 engine, 新智元 article "使用指南" and
+// openai.wiki "模型推理"): the token and position of each forward live on the
+// device. The classifier's last CTA writes the next token and advances the
+// position, so a generation is `n_prompt + steps - 1` replays of one captured
+// forward graph with no host round trip in between: one copy in, one copy out.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "l2_internal.cuh"
+
+using namespace l2;
+
+struct l2_handle {
+    l2_config cfg{};
+    int dev = 0, num_sms = 0;
+    int hd = 0, kvd = 0;
+
+    float* weights = nullptr;
+    float *emb = nullptr, *g_att = nullptr, *g_ffn = nullptr, *g_final = nullptr;
+    float *wqkv = nullptr, *wo = nullptr, *w13 = nullptr, *w2 = nullptr, *wcls = nullptr;
+    size_t weight_floats = 0;
+
+    float* kv = nullptr;             // K caches then V caches
+    float *k_cache = nullptr, *v_cache = nullptr;
+    size_t cache_layer = 0;          // floats of one layer of one sequence
+    size_t cache_seq = 0;            // floats of one sequence (all layers)
+
+    float* act = nullptr;            // activations block
+    float *x = nullptr, *q = nullptr, *att = nullptr, *hb = nullptr, *logits = nullptr;
+    float2* rope = nullptr;
+    L2State* st = nullptr;
+    int* ibuf = nullptr;             // prompt [S] + out [S]
+    int *d_prompt = nullptr, *d_out = nullptr;
+
+    MatvecPlan p_qkv{}, p_wo{}, p_w13{}, p_w2{}, p_cls{};
+    int nsplit = 1;
+    uint64_t policy = 0;
+
+    cudaStream_t stream = nullptr;
+    cudaGraphExec_t fwd1 = nullptr;  // one forward
+    cudaGraphExec_t fwdN = nullptr;  // kGraphBatch forwards
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    std::string err;
+};
+
+namespace {
+
+constexpr int kGraphBatch = 8;
+thread_local std::string g_create_error;
+
+int fail(l2_handle* h, int code, const std::string& msg) {
+    if (h)
+        h->err = msg;
+    else
+        g_create_error = msg;
+    return code;
+}
+
+int cuda_fail(l2_handle* h, cudaError_t e, const char* what) {
+    const int code = (e == cudaErrorMemoryAllocation) ? L2_ENOMEM : L2_ECUDA;
+    return fail(h, code, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define L2_CUDA(h, call)                                         \
+    do {                                                         \
+        cudaError_t e_ = (call);                                 \
+        if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
+    } while (0)
+
+size_t align64(size_t n) { return (n + 63) & ~static_cast<size_t>(63); }
+
+bool config_valid(const l2_config* c, std::string* why) {
+    auto bad = [&](const char* m) {
+        if (why) *why = m;
+        return false;
+    };
+    if (!c) return bad("config is NULL");
+    if (c->dim <= 0 || c->hidden_dim <= 0 || c->n_layers <= 0 || c->n_heads <= 0 ||
+        c->n_kv_heads <= 0 || c->vocab_size <= 0 || c->seq_len <= 0 || c->max_batch <= 0)
+        return bad("every size must be positive");
+    if (c->dim % c->n_heads != 0) return bad("dim must be a multiple of n_heads");
+    if (c->n_heads % c->n_kv_heads != 0) return bad("n_heads must be a multiple of n_kv_heads");
+    const int hd = c->dim / c->n_heads;
+    if (hd % 2 != 0) return bad("head_dim must be even (RoPE pairs)");
+    if (hd > 256) return bad("head_dim must be <= 256");
+    if (c->dim % 4 != 0 || c->hidden_dim % 4 != 0) return bad("dim and hidden_dim must be multiples of 4");
+    if (c->dim > 16384 || c->hidden_dim > 32768) return bad("dim <= 16384 and hidden_dim <= 32768");
+    if (c->vocab_size > (1 << 24)) return bad("vocab_size <= 2^24");
+    if (c->seq_len > (1 << 20)) return bad("seq_len <= 2^20");
+    if (c->max_batch > 1024) return bad("max_batch <= 1024");
+    if (!(c->norm_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("norm_eps >= 0 and rope_theta > 0");
+    if (c->shared_classifier != 0 && c->shared_classifier != 1) return bad("shared_classifier is 0 or 1");
+    return true;
+}
+
+__global__ void init_state_kernel(L2State* st, int pos, int token, const int* d_token,
+                                  const int* d_pos, int vocab, int seq_len, int n_prompt, int mode,
+                                  const int* prompt, int* out, int reset_err) {
+    int p = d_pos ? d_pos[0] : pos;
+    int t = d_token ? d_token[0] : (prompt && mode == 1 ? prompt[0] : token);
+    p = min(max(p, 0), seq_len - 1);
+    t = min(max(t, 0), vocab - 1);
+    st->pos = p;
+    st->token = t;
+    st->n_prompt = n_prompt;
+    st->mode = mode;
+    st->prompt = prompt;
+    st->out_tokens = out;
+    st->argmax_key = 0ull;
+    st->cls_done = 0u;
+    if (reset_err) st->err = 0;
+}
+
+MatvecArgs base_args(l2_handle* h) {
+    MatvecArgs a{};
+    a.eps = h->cfg.norm_eps;
+    a.d = h->cfg.dim;
+    a.kvd = h->kvd;
+    a.head_dim = h->hd;
+    a.seq_len = h->cfg.seq_len;
+    a.vocab = h->cfg.vocab_size;
+    a.rope = h->rope;
+    a.st = h->st;
+    a.l2_policy = h->policy;
+    return a;
+}
+
+// Launches kernel `kind` of layer l on stream s (kind as in l2_time_kernel).
+cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, kvd = h->kvd;
+    MatvecArgs a = base_args(h);
+    switch (kind) {
+        case 0:
+            a.W = h->wqkv + static_cast<size_t>(l) * (d + 2 * kvd) * d;
+            a.plan = h->p_qkv;
+            a.src = h->x;
+            a.gain = h->g_att + l * d;
+            a.emb = (l == 0) ? h->emb : nullptr;
+            a.x_init = (l == 0) ? h->x : nullptr;
+            a.q_out = h->q;
+            a.k_cache = h->k_cache + l * h->cache_layer;
+            a.v_cache = h->v_cache + l * h->cache_layer;
+            return launch_matvec(EPI_QKV_ROPE, a, s, true);
+        case 1: {
+            AttnArgs t{};
+            t.q = h->q;
+            t.k_cache = h->k_cache + l * h->cache_layer;
+            t.v_cache = h->v_cache + l * h->cache_layer;
+            t.att = h->att;
+            t.n_heads = c.n_heads;
+            t.n_kv_heads = c.n_kv_heads;
+            t.head_dim = h->hd;
+            t.seq_len = c.seq_len;
+            t.nsplit = h->nsplit;
+            t.st = h->st;
+            return launch_attention(t, s, true);
+        }
+        case 2:
+            a.W = h->wo + static_cast<size_t>(l) * d * d;
+            a.plan = h->p_wo;
+            a.src = h->att;
+            a.out = h->x;
+            return launch_matvec(EPI_RESIDUAL, a, s, true);
+        case 3:
+            a.W = h->w13 + static_cast<size_t>(l) * 2 * F * d;
+            a.plan = h->p_w13;
+            a.src = h->x;
+            a.gain = h->g_ffn + l * d;
+            a.out = h->hb;
+            return launch_matvec(EPI_SWIGLU, a, s, true);
+        case 4:
+            a.W = h->w2 + static_cast<size_t>(l) * d * F;
+            a.plan = h->p_w2;
+            a.src = h->hb;
+            a.out = h->x;
+            return launch_matvec(EPI_RESIDUAL, a, s, true);
+        case 5:
+            a.W = h->wcls;
+            a.plan = h->p_cls;
+            a.src = h->x;
+            a.gain = h->g_final;
+            a.out = h->logits;
+            return launch_matvec(EPI_CLASSIFIER, a, s, true);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t enqueue_forward(l2_handle* h, cudaStream_t s) {
+    for (int l = 0; l < h->cfg.n_layers; ++l)
+        for (int k = 0; k < 5; ++k) {
+            cudaError_t e = launch_kind(h, k, l, s);
+            if (e != cudaSuccess) return e;
+        }
+    return launch_kind(h, 5, 0, s);
+}
+
+int capture(l2_handle* h, int n_forwards, cudaGraphExec_t* out) {
+    cudaGraph_t g = nullptr;
+    L2_CUDA(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_forwards && e == cudaSuccess; ++i) e = enqueue_forward(h, h->stream);
+    cudaError_t e2 = cudaStreamEndCapture(h->stream, &g);
+    if (e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_fail(h, e, "kernel launch during capture");
+    }
+    if (e2 != cudaSuccess) return cuda_fail(h, e2, "cudaStreamEndCapture");
+    e = cudaGraphInstantiate(out, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphInstantiate");
+    return L2_OK;
+}
+
+int check_device_error(l2_handle* h) {
+    int err = 0;
+    L2_CUDA(h, cudaMemcpy(&err, &h->st->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (err & (ERR_TIMEOUT_TMA | ERR_BAD_PLAN))
+        return fail(h, L2_ETIMEOUT, "a bounded device wait gave up (bulk-copy completion)");
+    return L2_OK;
+}
+
+int upload(l2_handle* h, const float* blob) {
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, kvd = h->kvd;
+    const size_t o_gatt = V * d, o_wq = o_gatt + L * d, o_wk = o_wq + L * d * d;
+    const size_t o_wv = o_wk + L * kvd * d, o_wo = o_wv + L * kvd * d, o_gffn = o_wo + L * d * d;
+    const size_t o_w1 = o_gffn + L * d, o_w2 = o_w1 + L * F * d, o_w3 = o_w2 + L * d * F;
+    const size_t o_gfin = o_w3 + L * F * d, o_wcls = o_gfin + d;
+    cudaStream_t s = h->stream;
+    const size_t fs = sizeof(float);
+    auto h2d = [&](float* dst, size_t off, size_t n) {
+        return cudaMemcpyAsync(dst, blob + off, n * fs, cudaMemcpyHostToDevice, s);
+    };
+    L2_CUDA(h, h2d(h->emb, 0, V * d));
+    L2_CUDA(h, h2d(h->g_att, o_gatt, L * d));
+    L2_CUDA(h, h2d(h->g_ffn, o_gffn, L * d));
+    L2_CUDA(h, h2d(h->g_final, o_gfin, d));
+    for (size_t l = 0; l < L; ++l) {
+        float* dst = h->wqkv + l * (d + 2 * kvd) * d;
+        L2_CUDA(h, h2d(dst, o_wq + l * d * d, d * d));
+        L2_CUDA(h, h2d(dst + d * d, o_wk + l * kvd * d, kvd * d));
+        L2_CUDA(h, h2d(dst + (d + kvd) * d, o_wv + l * kvd * d, kvd * d));
+    }
+    L2_CUDA(h, h2d(h->wo, o_wo, L * d * d));
+    L2_CUDA(h, h2d(h->w2, o_w2, L * d * F));
+    if (!c.shared_classifier) L2_CUDA(h, h2d(h->wcls, o_wcls, V * d));
+    // W1/W3 interleave through a per-layer staging buffer
+    float* stage = nullptr;
+    L2_CUDA(h, cudaMalloc(&stage, 2 * F * d * fs));
+    int rc = L2_OK;
+    for (size_t l = 0; l < L && rc == L2_OK; ++l) {
+        cudaError_t e = h2d(stage, o_w1 + l * F * d, F * d);
+        if (e == cudaSuccess) e = h2d(stage + F * d, o_w3 + l * F * d, F * d);
+        if (e == cudaSuccess)
+            e = launch_interleave_rows(h->w13 + l * 2 * F * d, stage, stage + F * d,
+                                       static_cast<long long>(F), static_cast<int>(d), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) rc = cuda_fail(h, e, "weight upload / layout pass");
+    }
+    cudaFree(stage);
+    if (rc != L2_OK) return rc;
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return L2_OK;
+}
+
+void free_all(l2_handle* h) {
+    if (h->fwd1) cudaGraphExecDestroy(h->fwd1);
+    if (h->fwdN) cudaGraphExecDestroy(h->fwdN);
+    if (h->ev0) cudaEventDestroy(h->ev0);
+    if (h->ev1) cudaEventDestroy(h->ev1);
+    if (h->stream) cudaStreamDestroy(h->stream);
+    cudaFree(h->weights);
+    cudaFree(h->kv);
+    cudaFree(h->act);
+    h->fwd1 = h->fwdN = nullptr;
+    h->ev0 = h->ev1 = nullptr;
+    h->stream = nullptr;
+    h->weights = h->kv = h->act = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t l2_blob_floats(const l2_config* c) {
+    if (!config_valid(c, nullptr)) return 0;
+    const size_t d = c->dim, F = c->hidden_dim, L = c->n_layers, V = c->vocab_size;
+    const size_t kvd = static_cast<size_t>(c->n_kv_heads) * (d / c->n_heads);
+    size_t n = V * d + L * d + L * d * d + 2 * L * kvd * d + L * d * d + L * d + 3 * L * F * d + d;
+    if (!c->shared_classifier) n += V * d;
+    return n;
+}
+
+int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_handle** out) {
+    if (out) *out = nullptr;
+    std::string why;
+    if (!out) return fail(nullptr, L2_EINVAL, "out is NULL");
+    if (!config_valid(cfg, &why)) return fail(nullptr, L2_EINVAL, "invalid config: " + why);
+    if (!blob) return fail(nullptr, L2_EINVAL, "blob is NULL");
+    if (blob_floats != l2_blob_floats(cfg))
+        return fail(nullptr, L2_EBLOB, "blob size " + std::to_string(blob_floats) +
+                                           " != expected " + std::to_string(l2_blob_floats(cfg)));
+    l2_handle* h = new l2_handle();
+    h->cfg = *cfg;
+    auto bail = [&](int rc) {
+        g_create_error = h->err;
+        free_all(h);
+        delete h;
+        return rc;
+    };
+    cudaError_t e = cudaGetDevice(&h->dev);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaGetDevice"));
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, h->dev);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaGetDeviceProperties"));
+    if (prop.major < 10) return bail(fail(h, L2_ECUDA, "needs a Blackwell (sm_10x) device"));
+    h->num_sms = prop.multiProcessorCount;
+
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, S = c.seq_len;
+    const size_t B = c.max_batch;
+    h->hd = c.dim / c.n_heads;
+    h->kvd = c.n_kv_heads * h->hd;
+    const size_t kvd = h->kvd;
+
+    // plans
+    h->p_qkv = plan_matvec(static_cast<int>(d + 2 * kvd), static_cast<int>(d), 2, h->num_sms);
+    h->p_wo = plan_matvec(static_cast<int>(d), static_cast<int>(d), 1, h->num_sms);
+    h->p_w13 = plan_matvec(static_cast<int>(2 * F), static_cast<int>(d), 2, h->num_sms);
+    h->p_w2 = plan_matvec(static_cast<int>(d), static_cast<int>(F), 1, h->num_sms);
+    h->p_cls = plan_matvec(static_cast<int>(V), static_cast<int>(d), 1, h->num_sms);
+    size_t smem_max = 0;
+    for (const MatvecPlan* p : {&h->p_qkv, &h->p_wo, &h->p_w13, &h->p_w2, &h->p_cls})
+        smem_max = p->smem_bytes > smem_max ? p->smem_bytes : smem_max;
+    // the opt-in limit covers static + dynamic shared memory; keep 1 KB for the static part
+    if (smem_max + 1024 > prop.sharedMemPerBlockOptin)
+        return bail(fail(h, L2_EINVAL, "shape needs more shared memory than a CTA has"));
+    if ((e = prepare_attention()) != cudaSuccess) return bail(cuda_fail(h, e, "attention setup"));
+    h->nsplit = attn_nsplit(c.n_heads, c.seq_len, h->num_sms);
+    while (h->nsplit > 1 && attn_cluster_ok(h->hd, h->nsplit, c.n_heads) < 1) h->nsplit >>= 1;
+
+    // weights
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off += align64(n);
+        return o;
+    };
+    const size_t o_emb = take(V * d), o_ga = take(L * d), o_gf = take(L * d), o_gfin = take(d);
+    const size_t o_qkv = take(L * (d + 2 * kvd) * d), o_wo = take(L * d * d);
+    const size_t o_w13 = take(L * 2 * F * d), o_w2 = take(L * d * F);
+    const size_t o_cls = c.shared_classifier ? o_emb : take(V * d);
+    h->weight_floats = off;
+    e = cudaMalloc(&h->weights, off * sizeof(float));
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMalloc(weights)"));
+    h->emb = h->weights + o_emb;
+    h->g_att = h->weights + o_ga;
+    h->g_ffn = h->weights + o_gf;
+    h->g_final = h->weights + o_gfin;
+    h->wqkv = h->weights + o_qkv;
+    h->wo = h->weights + o_wo;
+    h->w13 = h->weights + o_w13;
+    h->w2 = h->weights + o_w2;
+    h->wcls = h->weights + o_cls;
+
+    // KV caches: [B][L][KVH][S][hd] for K, then the same for V
+    h->cache_layer = static_cast<size_t>(c.n_kv_heads) * S * h->hd;
+    h->cache_seq = L * h->cache_layer;
+    e = cudaMalloc(&h->kv, 2 * B * h->cache_seq * sizeof(float));
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMalloc(kv cache)"));
+    h->k_cache = h->kv;
+    h->v_cache = h->kv + B * h->cache_seq;
+
+    // activations and state
+    off = 0;
+    const size_t o_x = take(d), o_q = take(d), o_att = take(d), o_hb = take(F);
+    const size_t o_lg = take(B * V);
+    const size_t o_rope = take(S * h->hd);  // float2 [S][hd/2]
+    const size_t o_st = take((sizeof(L2State) + 3) / 4), o_ib = take(2 * S);
+    e = cudaMalloc(&h->act, off * sizeof(float));
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMalloc(activations)"));
+    h->x = h->act + o_x;
+    h->q = h->act + o_q;
+    h->att = h->act + o_att;
+    h->hb = h->act + o_hb;
+    h->logits = h->act + o_lg;
+    h->rope = reinterpret_cast<float2*>(h->act + o_rope);
+    h->st = reinterpret_cast<L2State*>(h->act + o_st);
+    h->ibuf = reinterpret_cast<int*>(h->act + o_ib);
+    h->d_prompt = h->ibuf;
+    h->d_out = h->ibuf + S;
+
+    e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaStreamCreate"));
+    if ((e = cudaEventCreate(&h->ev0)) != cudaSuccess || (e = cudaEventCreate(&h->ev1)) != cudaSuccess)
+        return bail(cuda_fail(h, e, "cudaEventCreate"));
+    if ((e = cudaMemsetAsync(h->act, 0, off * sizeof(float), h->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->kv, 0, 2 * B * h->cache_seq * sizeof(float), h->stream)) != cudaSuccess)
+        return bail(cuda_fail(h, e, "cudaMemset"));
+
+    // RoPE table: angle pos * theta^(-2i/hd) in double, rounded to float
+    {
+        std::vector<float2> tab(S * (h->hd / 2));
+        for (size_t p = 0; p < S; ++p)
+            for (int i = 0; i < h->hd / 2; ++i) {
+                const double freq = pow(static_cast<double>(c.rope_theta), -2.0 * i / h->hd);
+                const double ang = static_cast<double>(p) * freq;
+                tab[p * (h->hd / 2) + i] = make_float2(static_cast<float>(cos(ang)),
+                                                       static_cast<float>(sin(ang)));
+            }
+        e = cudaMemcpyAsync(h->rope, tab.data(), tab.size() * sizeof(float2),
+                            cudaMemcpyHostToDevice, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) return bail(cuda_fail(h, e, "rope table upload"));
+    }
+
+    // L2 policy for the weight stream: keep small models resident in L2
+    const double wbytes = static_cast<double>(h->weight_floats) * 4.0;
+    if (wbytes < 100e6) {
+        const float frac = 1.0f;
+        uint32_t bits;
+        memcpy(&bits, &frac, 4);
+        h->policy = bits;  // evict_last, fraction 1
+    } else {
+        h->policy = 0;     // evict_first
+    }
+
+    if ((e = set_matvec_smem_limits(smem_max)) != cudaSuccess)
+        return bail(cuda_fail(h, e, "cudaFuncSetAttribute"));
+
+    // weights: upload + layout pass (pin the caller's blob when possible)
+    const size_t bytes = blob_floats * sizeof(float);
+    const bool pinned = cudaHostRegister(const_cast<float*>(blob), bytes,
+                                         cudaHostRegisterReadOnly) == cudaSuccess;
+    if (!pinned) cudaGetLastError();
+    int rc = upload(h, blob);
+    if (pinned) cudaHostUnregister(const_cast<float*>(blob));
+    if (rc != L2_OK) return bail(rc);
+
+    if ((rc = capture(h, 1, &h->fwd1)) != L2_OK) return bail(rc);
+    if ((rc = capture(h, kGraphBatch, &h->fwdN)) != L2_OK) return bail(rc);
+    e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "create sync"));
+    *out = h;
+    return L2_OK;
+}
+
+void l2_destroy(l2_handle* h) {
+    if (!h) return;
+    cudaStreamSynchronize(h->stream);
+    free_all(h);
+    delete h;
+}
+
+const char* l2_last_error(const l2_handle* h) {
+    return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int l2_reset(l2_handle* h, int32_t seq) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    const size_t B = h->cfg.max_batch;
+    if (seq < -1 || seq >= static_cast<int32_t>(B)) return fail(h, L2_EINVAL, "seq out of range");
+    if (seq == -1) {
+        L2_CUDA(h, cudaMemsetAsync(h->kv, 0, 2 * B * h->cache_seq * sizeof(float), h->stream));
+    } else {
+        L2_CUDA(h, cudaMemsetAsync(h->k_cache + seq * h->cache_seq, 0, h->cache_seq * sizeof(float), h->stream));
+        L2_CUDA(h, cudaMemsetAsync(h->v_cache + seq * h->cache_seq, 0, h->cache_seq * sizeof(float), h->stream));
+    }
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    return L2_OK;
+}
+
+static int run_forwards(l2_handle* h, int n, cudaStream_t s) {
+    while (n >= kGraphBatch) {
+        L2_CUDA(h, cudaGraphLaunch(h->fwdN, s));
+        n -= kGraphBatch;
+    }
+    for (; n > 0; --n) L2_CUDA(h, cudaGraphLaunch(h->fwd1, s));
+    return L2_OK;
+}
+
+int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_pos, int32_t B,
+                      float* d_logits, void* stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
+    if (!d_tokens || !d_pos) return fail(h, L2_EINVAL, "NULL token or position buffer");
+    if (B != 1) return fail(h, L2_EINVAL, "batched forward is not available in this build");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, d_tokens, d_pos, h->cfg.vocab_size,
+                                      h->cfg.seq_len, 0, 0, nullptr, nullptr, 0);
+    L2_CUDA(h, cudaGetLastError());
+    int rc = run_forwards(h, 1, s);
+    if (rc != L2_OK) return rc;
+    if (d_logits)
+        L2_CUDA(h, cudaMemcpyAsync(d_logits, h->logits, sizeof(float) * h->cfg.vocab_size,
+                                   cudaMemcpyDeviceToDevice, s));
+    return L2_OK;
+}
+
+int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t B,
+               float* logits_out) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!tokens || !pos) return fail(h, L2_EINVAL, "NULL tokens or positions");
+    if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
+    for (int b = 0; b < B; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
+        if (pos[b] < 0 || pos[b] >= h->cfg.seq_len) return fail(h, L2_EINVAL, "position out of range");
+    }
+    if (B != 1) return fail(h, L2_EINVAL, "batched forward is not available in this build");
+    init_state_kernel<<<1, 1, 0, h->stream>>>(h->st, pos[0], tokens[0], nullptr, nullptr,
+                                              h->cfg.vocab_size, h->cfg.seq_len, 0, 0, nullptr,
+                                              nullptr, 1);
+    L2_CUDA(h, cudaGetLastError());
+    int rc = run_forwards(h, 1, h->stream);
+    if (rc != L2_OK) return rc;
+    if (logits_out)
+        L2_CUDA(h, cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * h->cfg.vocab_size,
+                                   cudaMemcpyDeviceToHost, h->stream));
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    return check_device_error(h);
+}
+
+int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt, int32_t steps,
+                       int32_t* d_out, void* stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!d_prompt || !d_out) return fail(h, L2_EINVAL, "NULL prompt or output buffer");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
+                                      h->cfg.seq_len, n_prompt, 1, d_prompt, d_out, 0);
+    L2_CUDA(h, cudaGetLastError());
+    return run_forwards(h, n_prompt + steps - 1, s);
+}
+
+int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
+                int32_t* out_tokens) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!prompt || !out_tokens) return fail(h, L2_EINVAL, "NULL prompt or output");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    for (int i = 0; i < n_prompt; ++i)
+        if (prompt[i] < 0 || prompt[i] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "prompt id out of range");
+    L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, prompt, sizeof(int32_t) * n_prompt,
+                               cudaMemcpyHostToDevice, h->stream));
+    init_state_kernel<<<1, 1, 0, h->stream>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
+                                              h->cfg.seq_len, n_prompt, 1, h->d_prompt, h->d_out, 1);
+    L2_CUDA(h, cudaGetLastError());
+    int rc = run_forwards(h, n_prompt + steps - 1, h->stream);
+    if (rc != L2_OK) return rc;
+    L2_CUDA(h, cudaMemcpyAsync(out_tokens, h->d_out, sizeof(int32_t) * steps,
+                               cudaMemcpyDeviceToHost, h->stream));
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    return check_device_error(h);
+}
+
+int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
+                      int32_t steps, int32_t* out_tokens) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    (void)prompts; (void)lens; (void)B; (void)steps; (void)out_tokens;
+    return fail(h, L2_EINVAL, "batched generation is not available in this build");
+}
+
+int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
+                   float* ms) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (kind < 0 || kind > 5 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "bad kind, iters, pos or output");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    init_state_kernel<<<1, 1, 0, s>>>(h->st, pos, 1, nullptr, nullptr, h->cfg.vocab_size,
+                                      h->cfg.seq_len, 0, 0, nullptr, nullptr, 1);
+    L2_CUDA(h, cudaGetLastError());
+    // warm-up launch, then the timed loop
+    L2_CUDA(h, launch_kind(h, kind, 0, s));
+    L2_CUDA(h, cudaEventRecord(h->ev0, s));
+    for (int i = 0; i < iters; ++i) L2_CUDA(h, launch_kind(h, kind, i % h->cfg.n_layers, s));
+    L2_CUDA(h, cudaEventRecord(h->ev1, s));
+    L2_CUDA(h, cudaEventSynchronize(h->ev1));
+    float t = 0.0f;
+    L2_CUDA(h, cudaEventElapsedTime(&t, h->ev0, h->ev1));
+    *ms = t / iters;
+    return check_device_error(h);
+}
+
+double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
+    if (!h) return 0.0;
+    const double d = h->cfg.dim, F = h->cfg.hidden_dim, V = h->cfg.vocab_size, kvd = h->kvd;
+    switch (kind) {
+        case 0: return 4.0 * ((d + 2 * kvd) * d + 2 * d + d + 2 * kvd);
+        case 1: return 4.0 * (2.0 * (pos + 1) * kvd + 2 * d);
+        case 2: return 4.0 * (d * d + d + 2 * d);
+        case 3: return 4.0 * (2 * F * d + 2 * d + F);
+        case 4: return 4.0 * (d * F + F + 2 * d);
+        case 5: return 4.0 * (V * d + 2 * d + V);
+        default: return 0.0;
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,231 @@
+// attention.cu -- causal multi-head attention of one decode step over the KV
+// cache, split over positions (flash-decoding) inside one thread-block cluster
+// per head.
+//
+// For head h (kv head h / (n_heads / n_kv_heads)) the step computes
+//   s_t = (q_h . k_t) / sqrt(head_dim),  t = 0..pos,
+//   att_h = sum_t softmax(s)_t v_t.
+// The llama2.c pages run this inside the single-file fp32 engine; the KV cache
+// that bounds it is named in the to-do list of
+// "llama2.c｜Baby LLaMA-openAI维基百科" ("未排序的待办事项"), and Flash Attention
+// is suggested as a next step in the QbitAI article on Baby LLaMA 2.
+//
+// Grid (nsplit, n_heads), cluster (nsplit, 1, 1): the nsplit CTAs of a cluster
+// share head h and take positions [r*n/nsplit, (r+1)*n/nsplit), n = pos + 1,
+// so every position count keeps all CTAs busy. The cache is head-major
+// [kv_head][S][head_dim]: a CTA's keys and values are contiguous rows. Each
+// warp walks groups of 8 positions, issuing all key and value loads of a group
+// before the 8 dot products (shuffle reductions) and an online-softmax update.
+// The CTA merges its warps, then stores (max, sum, unnormalised output) into
+// the shared memory of the cluster's rank-0 CTA (distributed shared memory);
+// after one hardware cluster barrier rank 0 merges the nsplit partials with
+// log-sum-exp rescaling and writes att_h. No global atomics, fences or spins.
+#include <cooperative_groups.h>
+#include <math.h>
+
+#include "l2_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace l2 {
+
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kMaxCluster = 16;
+
+// EPL: head elements per lane (head_dim <= 32 * EPL); G: positions per warp
+// iteration (all their key/value loads are in flight together).
+template <int EPL, int G>
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+    constexpr int kGroup = G;
+    constexpr int HDMAX = 32 * EPL;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int nsplit = a.nsplit;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hd = a.head_dim;
+    const int kvh = h / (a.n_heads / a.n_kv_heads);
+
+    __shared__ float s_inbox[kMaxCluster][HDMAX + 2];  // rank 0: partials of the cluster
+    __shared__ float s_m[kAttnWarps], s_l[kAttnWarps];
+    __shared__ float s_o[kAttnWarps][HDMAX];
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    float qr[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        qr[j] = e < hd ? __ldcg(a.q + static_cast<size_t>(h) * hd + e) : 0.0f;
+    }
+    const int n = __ldcg(&a.st->pos) + 1;
+    const int t0 = static_cast<int>(static_cast<long long>(n) * rank / nsplit);
+    const int t1 = static_cast<int>(static_cast<long long>(n) * (rank + 1) / nsplit);
+    const float* Kh = a.k_cache + static_cast<size_t>(kvh) * a.seq_len * hd;
+    const float* Vh = a.v_cache + static_cast<size_t>(kvh) * a.seq_len * hd;
+    const float scale_div = sqrtf(static_cast<float>(hd));
+
+    float m = -INFINITY, l = 0.0f, o[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) o[j] = 0.0f;
+
+    for (int tb = t0 + warp * kGroup; tb < t1; tb += kAttnWarps * kGroup) {
+        float kr[kGroup][EPL], vr[kGroup][EPL];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+            const int t = tb + g;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) {
+                const int e = lane + 32 * j;
+                const bool ok = (t < t1) && (e < hd);
+                kr[g][j] = ok ? __ldcg(Kh + static_cast<size_t>(t) * hd + e) : 0.0f;
+                vr[g][j] = ok ? __ldcg(Vh + static_cast<size_t>(t) * hd + e) : 0.0f;
+            }
+        }
+        float sc[kGroup];
+        float gmax = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+            float p = 0.0f;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) p = fmaf(qr[j], kr[g][j], p);
+            p = warp_sum(p);
+            sc[g] = (tb + g < t1) ? p / scale_div : -INFINITY;
+            gmax = fmaxf(gmax, sc[g]);
+        }
+        const float mnew = fmaxf(m, gmax);
+        const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+        l *= corr;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) o[j] *= corr;
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+            const float p = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+            l += p;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, vr[g][j], o[j]);
+        }
+        m = mnew;
+    }
+
+    // merge the warps of this CTA
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s_o[warp][lane + 32 * j] = o[j];
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+    float* inbox = cluster.map_shared_rank(&s_inbox[rank][0], 0);
+    for (int e = tid; e < hd; e += kAttnThreads) {
+        float acc = 0.0f;
+        for (int w = 0; w < kAttnWarps; ++w)
+            if (s_m[w] != -INFINITY) acc += s_o[w][e] * expf(s_m[w] - M);
+        inbox[e] = acc;
+    }
+    if (tid == 0) {
+        float L = 0.0f;
+        for (int w = 0; w < kAttnWarps; ++w)
+            if (s_m[w] != -INFINITY) L += s_l[w] * expf(s_m[w] - M);
+        inbox[HDMAX] = M;
+        inbox[HDMAX + 1] = L;
+    }
+    cluster.sync();  // partials of every rank are in rank 0's shared memory
+    if (rank != 0) return;
+
+    float Mg = -INFINITY;
+    for (int r = 0; r < nsplit; ++r) Mg = fmaxf(Mg, s_inbox[r][HDMAX]);
+    float Lg = 0.0f;
+    for (int r = 0; r < nsplit; ++r)
+        if (s_inbox[r][HDMAX] != -INFINITY) Lg += s_inbox[r][HDMAX + 1] * expf(s_inbox[r][HDMAX] - Mg);
+    for (int e = tid; e < hd; e += kAttnThreads) {
+        float acc = 0.0f;
+        for (int r = 0; r < nsplit; ++r)
+            if (s_inbox[r][HDMAX] != -INFINITY) acc += s_inbox[r][e] * expf(s_inbox[r][HDMAX] - Mg);
+        a.att[static_cast<size_t>(h) * hd + e] = acc / Lg;
+    }
+}
+
+template <int EPL, int G>
+cudaError_t launch_attn_t(const AttnArgs& a, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.nsplit, a.n_heads);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<EPL, G>, a);
+}
+
+template <int EPL, int G>
+cudaError_t allow_large_clusters() {
+    return cudaFuncSetAttribute(attn_kernel<EPL, G>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                1);
+}
+
+template <int EPL, int G>
+int max_active_clusters(int nsplit, int n_heads) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(nsplit, n_heads);
+    cfg.blockDim = dim3(kAttnThreads);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<EPL, G>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace
+
+int attn_nsplit(int n_heads, int seq_len, int num_sms) {
+    // 16 CTAs per head (a non-portable cluster size) when 8 would leave SMs idle
+    int ns = (n_heads * 8 < num_sms) ? 16 : 8;
+    while (ns > 1 && ns > seq_len) ns >>= 1;
+    return ns;
+}
+
+cudaError_t prepare_attention() {
+    cudaError_t e;
+    if ((e = allow_large_clusters<2, 8>()) != cudaSuccess) return e;
+    if ((e = allow_large_clusters<4, 8>()) != cudaSuccess) return e;
+    return allow_large_clusters<8, 4>();
+}
+
+// Largest usable cluster size <= want for this head_dim (0 if none launches).
+int attn_cluster_ok(int head_dim, int nsplit, int n_heads) {
+    if (head_dim <= 64) return max_active_clusters<2, 8>(nsplit, n_heads);
+    if (head_dim <= 128) return max_active_clusters<4, 8>(nsplit, n_heads);
+    return max_active_clusters<8, 4>(nsplit, n_heads);
+}
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
+    if (a.nsplit < 1 || a.nsplit > kMaxCluster) return cudaErrorInvalidValue;
+    if (a.head_dim <= 64) return launch_attn_t<2, 8>(a, s, pdl);
+    if (a.head_dim <= 128) return launch_attn_t<4, 8>(a, s, pdl);
+    if (a.head_dim <= 256) return launch_attn_t<8, 4>(a, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace l2

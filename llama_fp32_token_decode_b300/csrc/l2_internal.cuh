@@ -1,0 +1,223 @@
+// l2_internal.cuh -- device helpers and launch-parameter structs shared by the
+// kernels of the decode library (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/l2decode.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "this library targets sm_103a (Blackwell) only"
+#endif
+
+namespace l2 {
+
+// Device error word bits (L2State::err).
+enum : int {
+    ERR_TIMEOUT_TMA = 1,   // a bulk-copy completion wait gave up
+    ERR_BAD_PLAN = 2,      // a kernel received an impossible launch plan
+    ERR_NAN = 4,           // the classifier met a NaN logit
+};
+
+// Bound for every device-side spin: about one second at 2 GHz.
+constexpr long long kSpinLimitCycles = 2000000000LL;
+
+// Device-resident decode state of the batch-1 path. The classifier's last CTA
+// advances it, so consecutive forwards need no host round trip.
+struct L2State {
+    int pos;            // position the next forward consumes
+    int token;          // token the next forward consumes
+    int n_prompt;       // generate: prompt length
+    int mode;           // 0 = single forward, 1 = generate
+    int last_argmax;    // greedy choice of the last forward
+    int err;            // ERR_* bits
+    const int* prompt;  // generate: device prompt [n_prompt]
+    int* out_tokens;    // generate: device output [steps]
+    unsigned long long argmax_key;  // packed (orderable value, ~index) max
+    unsigned int cls_done;          // classifier CTAs finished this forward
+    unsigned int pad;
+};
+
+enum Epilogue : int { EPI_QKV_ROPE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_CLASSIFIER = 3 };
+
+// Launch plan of one streaming matvec y = W xs (W row-major [R][K]).
+struct MatvecPlan {
+    int R, K;             // rows, columns
+    int unit;             // rows kept together in one CTA (2 for pair epilogues)
+    int rows_per_stage;   // TR: full rows per ring stage (1 when rows are chunked)
+    int chunks_per_row;   // NCH: >1 splits a row over several stages
+    int chunk_floats;     // floats per chunk (K when NCH == 1)
+    int warps_per_row;    // WPR: consumer warps sharing one row of a slot
+    int rows_per_warp;    // RPW: rows one warp handles per slot
+    int stage_floats;     // ring slot size in floats (multiple of 32)
+    int nstages;          // ring depth
+    int grid;             // CTAs
+    int max_rows_per_cta; // bound used to size the row-result buffer
+    size_t smem_bytes;    // dynamic shared memory
+};
+
+struct MatvecArgs {
+    const float* W;
+    MatvecPlan plan;
+    // prologue: xs = norm(src) * gain (gain != nullptr) or xs = src
+    const float* src;      // input vector [K] (ignored when emb != nullptr)
+    const float* gain;     // RMSNorm gain [K] or nullptr
+    float eps;
+    const float* emb;      // layer-0 QKV: src = emb[token] (token from state)
+    float* x_init;         // layer-0 QKV: CTA 0 copies emb[token] here
+    // epilogue
+    float* out;            // RESIDUAL: x (+=); SWIGLU: hb; CLASSIFIER: logits
+    // QKV + RoPE + KV append
+    float* q_out;          // [d]
+    float* k_cache;        // this layer's K cache, head-major [KVH][S][hd]
+    float* v_cache;        // this layer's V cache
+    const float2* rope;    // [S][hd/2] (cos, sin)
+    int d, kvd, head_dim, seq_len, vocab;
+    // state
+    L2State* st;
+    uint64_t l2_policy;    // createpolicy descriptor for the weight stream
+};
+
+struct AttnArgs {
+    const float* q;        // [d] (RoPE applied)
+    const float* k_cache;  // this layer: [KVH][S][hd]
+    const float* v_cache;
+    float* att;            // [d] output
+    int n_heads, n_kv_heads, head_dim, seq_len;
+    int nsplit;            // CTAs per head = cluster size (<= 16)
+    L2State* st;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase of an mbarrier; false when the bound is hit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kSpinLimitCycles) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t make_policy_evict_last(float frac) {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, %1;" : "=l"(p) : "f"(frac));
+    return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Key that orders (value, index) pairs by value, then by lower index; NaN maps
+// below every number. -0 and +0 compare equal, as in a plain float comparison.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+    if (v != v) {
+        u = 0u;
+    } else {
+        u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ int argmax_key_index(unsigned long long k) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+
+// ---------------------------------------------------------------- host launchers
+
+// matvec.cu
+MatvecPlan plan_matvec(int R, int K, int unit, int num_sms);
+int matvec_threads();
+cudaError_t launch_matvec(int epi, const MatvecArgs& a, cudaStream_t s, bool pdl);
+cudaError_t set_matvec_smem_limits(size_t bytes);
+
+// attention.cu
+int attn_nsplit(int n_heads, int seq_len, int num_sms);
+cudaError_t prepare_attention();
+int attn_cluster_ok(int head_dim, int nsplit, int n_heads);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+
+// layout.cu
+cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
+                                   int cols, cudaStream_t s);
+
+}  // namespace l2
