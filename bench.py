@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Decode throughput of the fp32 Llama-2 decode library on B300.
+
+One step = one greedy generation of the named workload (every forward of its
+prompt and generated positions) through the library's C ABI. Default workload:
+the 7B shape at batch 1 (64-token prompt + 256 generated tokens = 319
+forwards), the largest configuration that fits one GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b|15m|44m|110m]
+    python bench.py --impl reference ...   # the C oracle on the host cores
+    python bench.py --kernel-only 3 --layers 2   # one kernel kind on a reduced-depth
+                                                 # model of the same shape (ncu case)
+
+Prints ONE JSON line (rank 0). N > 1 runs under torchrun: every rank decodes
+its own replica (batch-1 decode does not shard; no collective on the data
+path), `value` is the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode tok/s (fp32, batch 1)"
+DOMINANT_KIND = 3  # W1/W3 + SwiGLU: 44% of the streamed bytes of a 7B-shape step
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "w13_swiglu_7b_shape.md")
+KERNEL_SOURCE = os.path.join(ROOT, "llama_fp32_token_decode_b300", "csrc", "matvec.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="7b", choices=["15m", "44m", "110m", "7b"])
+    ap.add_argument("--cpu-forwards", type=int, default=0,
+                    help="oracle forwards in the CPU-baseline sample (0 = about 20 s worth)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", type=int, default=None,
+                    help="time one kernel kind (0 QKV, 1 attention, 2 Wo, 3 W1/W3, 4 W2, "
+                         "5 classifier) on the workload's shape and exit: the profiling case")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="with --kernel-only: layers of the reduced-depth model (0 = all)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def forwards_of(w) -> int:
+    return w["n_prompt"] + w["steps"] - 1
+
+
+def workload_bytes_per_forward(cfg, pos: float) -> float:
+    """Algorithmic HBM bytes of one batch-1 forward at position pos: every weight
+    except the embedding table, one embedding row, and the KV rows read and
+    written."""
+    d, F, L, V = cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["vocab_size"]
+    kvd = cfg["n_kv_heads"] * (d // cfg["n_heads"])
+    weights = L * (2 * d * d + 2 * d * kvd + 3 * d * F + 2 * d) + d + V * d
+    kv = L * (2 * kvd * (pos + 1) + 2 * kvd)
+    return 4.0 * (weights + d + kv)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6400.0}, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    try:
+        txt = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in txt.splitlines():
+        if ":" in ln and ln.strip().startswith("- "):
+            k, v = ln.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    if vals.get("matvec.cu sha256") != src:
+        return None
+    try:
+        return float(vals["dram bytes per 7B-shape launch (read + write)"])
+    except (KeyError, ValueError):
+        return None
+
+
+def oracle_sample(cfg, blob, prompt, n_fwd: int):
+    """Times the oracle, as it stands, over the first n_fwd forwards."""
+    import oracle
+    m = oracle.Model(cfg, blob)
+    tok = int(prompt[0])
+    t0 = time.perf_counter()
+    for p in range(n_fwd):
+        lg = m.forward(tok, p)
+        tok = int(prompt[p + 1]) if p + 1 < len(prompt) else int(np.argmax(lg))
+    dt = time.perf_counter() - t0
+    m.close()
+    return dt
+
+
+def default_cpu_forwards(name: str) -> int:
+    # about 10-25 s of one core per sample
+    return {"15m": 256, "44m": 120, "110m": 40, "7b": 2}[name]
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = synth.workload(args.workload)
+    cfg = synth.model_config(w)
+    blob = synth.make_blob(cfg, w["seed"])
+    prompt = synth.prompt(w)
+    per_step = max(1, (args.cpu_forwards or default_cpu_forwards(args.workload)) // 2)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, blob, prompt, 1)
+    t = sum(oracle_sample(cfg, blob, prompt, per_step) for _ in range(args.steps))
+    value = args.steps * per_step / t
+    sample = (f"first {per_step} forwards (positions 0..{per_step - 1}) of the {args.workload} "
+              f"workload per step, single-threaded C oracle (-O2, no fast-math)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "global_batch": 1,
+                       "forwards_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def upload_blob_in_pieces(cfg, seed):
+    """The seeded blob drawn in 256 MB pieces straight into a device tensor, so
+    that no rank holds the whole blob in host memory."""
+    import torch
+    n = synth.blob_floats(cfg)
+    d_blob = torch.empty(n, dtype=torch.float32, device="cuda")
+    chunk = 1 << 26
+    host = torch.empty(chunk, dtype=torch.float32).pin_memory()
+    h = host.numpy()
+    off = 0
+    for _, cnt, is_gain in synth.blob_segments(cfg):
+        done = 0
+        while done < cnt:
+            m = min(chunk, cnt - done)
+            if is_gain:
+                h[:m] = 1.0
+            else:
+                synth._lib().synth_fill_normal(seed, synth.STREAM_WEIGHTS, off + done, m,
+                                               synth.WEIGHT_STD, h.ctypes.data,
+                                               os.cpu_count() or 1)
+            d_blob[off + done:off + done + m].copy_(host[:m])
+            done += m
+        off += cnt
+    torch.cuda.synchronize()
+    return d_blob
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import llama_fp32_token_decode_b300 as l2
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    w = synth.workload(args.workload)
+    cfg = synth.model_config(w)
+    n_fwd = forwards_of(w)
+    prompt = synth.prompt(w)
+    steps = w["steps"]
+    keep_host_blob = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+
+    if keep_host_blob:  # the CPU baseline needs the blob on the host
+        blob = synth.make_blob(cfg, w["seed"])
+        dec = l2.Decoder(cfg, blob)
+    else:
+        blob = None
+        d_blob = upload_blob_in_pieces(cfg, w["seed"])
+        dec = l2.Decoder(cfg, d_blob=d_blob)
+        del d_blob
+        torch.cuda.empty_cache()
+
+    stream = torch.cuda.Stream()
+    d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
+    d_out = torch.zeros(steps, dtype=torch.int32, device="cuda")
+
+    def step():
+        l2.l2_generate_device(dec.h, d_prompt, len(prompt), steps, d_out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    ref_tokens = d_out.cpu().numpy().copy()
+
+    # ---- timed region: K generations, inputs resident in HBM
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world)
+    value = world * args.steps * n_fwd / (ms_max / 1e3)
+    assert np.array_equal(d_out.cpu().numpy(), ref_tokens), "generation is not reproducible"
+
+    # ---- end to end through the public host API: pinned host prompt in, tokens out
+    h_prompt = torch.tensor(prompt, dtype=torch.int32).pin_memory().numpy()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        toks = dec.generate(h_prompt, steps)
+    t_e2e = time.perf_counter() - t0
+    t_e2e = max_over_ranks(t_e2e, world)
+    assert np.array_equal(toks, ref_tokens), "host and device entry points disagree"
+    e2e = {"value": world * args.steps * n_fwd / t_e2e, "unit": "tok/s",
+           "h2d_bytes_per_step": int(h_prompt.nbytes), "d2h_bytes_per_step": int(steps * 4)}
+
+    # ---- roofline of the dominant kernel, timed live on the launching stream
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    pos_mid = n_fwd // 2
+    iters = 3 * cfg["n_layers"]
+    k_ms = l2.l2_time_kernel(dec.h, DOMINANT_KIND, pos_mid, iters, stream)
+    k_bytes = l2.l2_kernel_bytes(dec.h, DOMINANT_KIND, pos_mid)
+    achieved = k_bytes / (k_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": profiled_traffic() if args.workload == "7b" else None,
+                "kernel": "matvec_kernel<EPI_SWIGLU> (W1/W3 + SwiGLU)",
+                "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms,
+                "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
+    # whole-step roofline: algorithmic bytes of every forward over the step time
+    step_bytes = sum(workload_bytes_per_forward(cfg, p) for p in range(n_fwd))
+    step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
+    step_roofline = {"achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
+                     "bytes_per_step": step_bytes,
+                     "roofline_tok_s": n_fwd / (step_bytes / (peak * 1e9))}
+
+    # ---- CPU baseline: the oracle as it stands, on a bounded sample, 1 core
+    cpu = None
+    if keep_host_blob:
+        nf = args.cpu_forwards or default_cpu_forwards(args.workload)
+        dt = oracle_sample(cfg, blob, prompt, nf)
+        cpu = {"value": nf / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {nf} forwards (positions 0..{nf - 1}) of the {args.workload} "
+                         f"workload, single-threaded C oracle (-O2, no fast-math), "
+                         f"host has {os.cpu_count()} cores"}
+
+    launches_per_step = n_fwd * (5 * cfg["n_layers"] + 1) + 1
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (random-init N(0,0.02) weights, seeded prompt ids)",
+            "config": {"workload": args.workload, "global_batch": world,
+                       "dim": cfg["dim"], "n_layers": cfg["n_layers"], "n_heads": cfg["n_heads"],
+                       "hidden_dim": cfg["hidden_dim"], "vocab_size": cfg["vocab_size"],
+                       "seq_len": cfg["seq_len"], "n_prompt": w["n_prompt"],
+                       "generated": steps, "forwards_per_step": n_fwd,
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (%.2f GB streamed per forward)" % (
+                           step_bytes / n_fwd / 1e9) if step_bytes / n_fwd > 126e6 else
+                       "weights may stay L2-resident (%.1f MB per forward)" % (
+                           step_bytes / n_fwd / 1e6)},
+            "roofline": roofline, "step_roofline": step_roofline,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dec.close()
+    return 0
+
+
+def run_kernel_only(args):
+    """Small case of one kernel for profilers: the workload's shapes with fewer
+    layers and a 512-position cache (a few GB on the device), one warm-up launch
+    and two timed launches of the chosen kind."""
+    import torch
+
+    import llama_fp32_token_decode_b300 as l2
+    torch.cuda.set_device(0)
+    w = synth.workload(args.workload)
+    cfg = synth.model_config(w)
+    if args.layers:
+        cfg["n_layers"] = args.layers
+    cfg["seq_len"] = min(cfg["seq_len"], 512)
+    blob = synth.make_blob(cfg, w["seed"])
+    with l2.Decoder(cfg, blob) as dec:
+        pos = min(300, cfg["seq_len"] - 1)
+        ms = l2.l2_time_kernel(dec.h, args.kernel_only, pos, 2)
+        b = l2.l2_kernel_bytes(dec.h, args.kernel_only, pos)
+    print(json.dumps({"kernel": l2.KERNEL_KINDS[args.kernel_only], "workload": args.workload,
+                      "layers": cfg["n_layers"], "pos": pos, "launch_ms": ms,
+                      "algorithmic_bytes": b, "GB/s": b / ms / 1e6}), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.kernel_only is not None:
+        return run_kernel_only(args)
+    world, rank, local = dist_setup(args)
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    rc = run_reference(args, world, rank) if args.impl == "reference" else \
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -93,6 +93,14 @@ L2_API size_t l2_blob_floats(const l2_config* cfg);
  * Errors: L2_EINVAL (cfg), L2_EBLOB (size), L2_ENOMEM, L2_ECUDA. */
 L2_API int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_handle** out);
 
+/* As l2_create, with the blob in device memory (d_blob, blob_floats floats,
+ * read only during the call; the caller keeps ownership and may free it when
+ * the call returns). For callers that already hold the weights on the GPU, or
+ * that stream a large blob to the device in pieces instead of holding it in
+ * host memory. Same errors as l2_create. */
+L2_API int l2_create_from_device(const l2_config* cfg, const float* d_blob, size_t blob_floats,
+                                 l2_handle** out);
+
 /* One decode step for B sequences; sequence b consumes token tokens[b] at
  * position pos[b], writes its KV-cache slot pos[b] and attends over slots
  * 0..pos[b] (slots below pos[b] must hold that sequence's earlier steps;

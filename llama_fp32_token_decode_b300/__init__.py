@@ -3,7 +3,7 @@
 Argument marshalling only: every step of the decode path runs in the library's
 CUDA kernels. There is no CPU fallback; importing this package fails loudly when
 the library has not been built (``python llama_fp32_token_decode_b300/build.py``).
-Functions keep the C names: l2_create, l2_forward, l2_forward_device,
+Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
 l2_generate, l2_generate_device, l2_generate_batch, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes.
 """
@@ -25,7 +25,7 @@ ERROR_NAMES = {L2_EINVAL: "L2_EINVAL", L2_ENOMEM: "L2_ENOMEM", L2_ECUDA: "L2_ECU
 KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residual",
                 "classifier_argmax")
 
-EXPORTS = ("l2_blob_floats", "l2_create", "l2_forward", "l2_forward_device", "l2_generate",
+EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes")
 
@@ -56,6 +56,7 @@ _CFG = ctypes.POINTER(L2Config)
 _SIG = {
     "l2_blob_floats": (ctypes.c_size_t, [_CFG]),
     "l2_create": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, ctypes.POINTER(_P)]),
+    "l2_create_from_device": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, ctypes.POINTER(_P)]),
     "l2_forward": (ctypes.c_int, [_P, _P, _P, _I, _P]),
     "l2_forward_device": (ctypes.c_int, [_P, _P, _P, _I, _P, _P]),
     "l2_generate": (ctypes.c_int, [_P, _P, _I, _I, _P]),
@@ -103,6 +104,14 @@ def l2_create(cfg: dict, blob: np.ndarray):
     h = _P()
     c = make_config(cfg)
     _check(_lib.l2_create(ctypes.byref(c), blob.ctypes.data, blob.size, ctypes.byref(h)))
+    return h
+
+
+def l2_create_from_device(cfg: dict, d_blob, n_floats: int):
+    """d_blob: device pointer (int) or a CUDA float32 torch tensor."""
+    h = _P()
+    c = make_config(cfg)
+    _check(_lib.l2_create_from_device(ctypes.byref(c), _ptr(d_blob), n_floats, ctypes.byref(h)))
     return h
 
 
@@ -177,9 +186,12 @@ def _stream(stream):
 class Decoder:
     """Owns one handle; methods forward to the C calls of the same names."""
 
-    def __init__(self, cfg: dict, blob: np.ndarray):
+    def __init__(self, cfg: dict, blob=None, d_blob=None):
         self.cfg = dict(cfg)
-        self.h = l2_create(cfg, blob)
+        if d_blob is not None:
+            self.h = l2_create_from_device(cfg, d_blob, l2_blob_floats(cfg))
+        else:
+            self.h = l2_create(cfg, blob)
 
     def close(self):
         if getattr(self, "h", None):

@@ -230,7 +230,7 @@ int check_device_error(l2_handle* h) {
     return L2_OK;
 }
 
-int upload(l2_handle* h, const float* blob) {
+int upload(l2_handle* h, const float* blob, cudaMemcpyKind kind) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, kvd = h->kvd;
     const size_t o_gatt = V * d, o_wq = o_gatt + L * d, o_wk = o_wq + L * d * d;
@@ -240,7 +240,7 @@ int upload(l2_handle* h, const float* blob) {
     cudaStream_t s = h->stream;
     const size_t fs = sizeof(float);
     auto h2d = [&](float* dst, size_t off, size_t n) {
-        return cudaMemcpyAsync(dst, blob + off, n * fs, cudaMemcpyHostToDevice, s);
+        return cudaMemcpyAsync(dst, blob + off, n * fs, kind, s);
     };
     L2_CUDA(h, h2d(h->emb, 0, V * d));
     L2_CUDA(h, h2d(h->g_att, o_gatt, L * d));
@@ -302,7 +302,8 @@ size_t l2_blob_floats(const l2_config* c) {
     return n;
 }
 
-int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_handle** out) {
+static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floats, bool on_device,
+                       l2_handle** out) {
     if (out) *out = nullptr;
     std::string why;
     if (!out) return fail(nullptr, L2_EINVAL, "out is NULL");
@@ -439,13 +440,18 @@ int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_ha
     if ((e = set_matvec_smem_limits(smem_max)) != cudaSuccess)
         return bail(cuda_fail(h, e, "cudaFuncSetAttribute"));
 
-    // weights: upload + layout pass (pin the caller's blob when possible)
-    const size_t bytes = blob_floats * sizeof(float);
-    const bool pinned = cudaHostRegister(const_cast<float*>(blob), bytes,
-                                         cudaHostRegisterReadOnly) == cudaSuccess;
-    if (!pinned) cudaGetLastError();
-    int rc = upload(h, blob);
-    if (pinned) cudaHostUnregister(const_cast<float*>(blob));
+    // weights: upload + layout pass (pin the caller's host blob when possible)
+    int rc;
+    if (on_device) {
+        rc = upload(h, blob, cudaMemcpyDeviceToDevice);
+    } else {
+        const size_t bytes = blob_floats * sizeof(float);
+        const bool pinned = cudaHostRegister(const_cast<float*>(blob), bytes,
+                                             cudaHostRegisterReadOnly) == cudaSuccess;
+        if (!pinned) cudaGetLastError();
+        rc = upload(h, blob, cudaMemcpyHostToDevice);
+        if (pinned) cudaHostUnregister(const_cast<float*>(blob));
+    }
     if (rc != L2_OK) return bail(rc);
 
     if ((rc = capture(h, 1, &h->fwd1)) != L2_OK) return bail(rc);
@@ -454,6 +460,15 @@ int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_ha
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "create sync"));
     *out = h;
     return L2_OK;
+}
+
+int l2_create(const l2_config* cfg, const float* blob, size_t blob_floats, l2_handle** out) {
+    return create_impl(cfg, blob, blob_floats, false, out);
+}
+
+int l2_create_from_device(const l2_config* cfg, const float* d_blob, size_t blob_floats,
+                          l2_handle** out) {
+    return create_impl(cfg, d_blob, blob_floats, true, out);
 }
 
 void l2_destroy(l2_handle* h) {
