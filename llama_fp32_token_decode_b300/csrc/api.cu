@@ -437,7 +437,7 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
         h->policy = 0;     // evict_first
     }
 
-    if ((e = set_matvec_smem_limits(smem_max)) != cudaSuccess)
+    if ((e = set_matvec_smem_limits()) != cudaSuccess)
         return bail(cuda_fail(h, e, "cudaFuncSetAttribute"));
 
     // weights: upload + layout pass (pin the caller's host blob when possible)

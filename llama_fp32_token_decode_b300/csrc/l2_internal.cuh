@@ -208,7 +208,7 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
 MatvecPlan plan_matvec(int R, int K, int unit, int num_sms);
 int matvec_threads();
 cudaError_t launch_matvec(int epi, const MatvecArgs& a, cudaStream_t s, bool pdl);
-cudaError_t set_matvec_smem_limits(size_t bytes);
+cudaError_t set_matvec_smem_limits();
 
 // attention.cu
 int attn_nsplit(int n_heads, int seq_len, int num_sms);

@@ -395,20 +395,32 @@ cudaError_t launch_one(const MatvecArgs& a, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
-cudaError_t set_matvec_smem_limits(size_t bytes) {
-    const int lim = static_cast<int>(bytes);
-    cudaError_t e;
-    if ((e = cudaFuncSetAttribute(matvec_kernel<EPI_QKV_ROPE>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(matvec_kernel<EPI_RESIDUAL>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(matvec_kernel<EPI_SWIGLU>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(matvec_kernel<EPI_CLASSIFIER>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+namespace {
+
+template <int EPI>
+cudaError_t raise_smem_limit(int optin) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, matvec_kernel<EPI>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(matvec_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(fa.sharedSizeBytes));
+}
+
+}  // namespace
+
+// Sets every instantiation's dynamic shared-memory limit to the most the current
+// device allows. The attribute is process-wide, so it is never set to one
+// handle's smaller need: that would break launches of a larger live handle.
+cudaError_t set_matvec_smem_limits() {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if ((e = raise_smem_limit<EPI_QKV_ROPE>(optin)) != cudaSuccess) return e;
+    if ((e = raise_smem_limit<EPI_RESIDUAL>(optin)) != cudaSuccess) return e;
+    if ((e = raise_smem_limit<EPI_SWIGLU>(optin)) != cudaSuccess) return e;
+    return raise_smem_limit<EPI_CLASSIFIER>(optin);
 }
 
 cudaError_t launch_matvec(int epi, const MatvecArgs& a, cudaStream_t s, bool pdl) {

@@ -139,3 +139,17 @@ def test_kernel_timing_hook(l2):
             ms = l2.l2_time_kernel(dec.h, kind, 3, 4)
             assert 0.0 < ms < 100.0
             assert l2.l2_kernel_bytes(dec.h, kind, 3) > 0
+
+
+def test_two_live_handles_of_different_shapes(l2):
+    # kernel attributes are process-wide: creating a smaller model must not
+    # break launches of a larger model that is still alive
+    big, small = SHAPES["k4096"], SHAPES["tiny_ragged"]
+    bb = synth.make_blob(big, 31, std=0.05)
+    sb = synth.make_blob(small, 32, std=0.05)
+    with l2.Decoder(big, bb) as d1:
+        ref1 = d1.forward([5], [0])
+        with l2.Decoder(small, sb) as d2:
+            ref2 = d2.forward([7], [0])
+            np.testing.assert_array_equal(d1.forward([5], [0]), ref1)
+            np.testing.assert_array_equal(d2.forward([7], [0]), ref2)
