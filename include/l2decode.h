@@ -170,6 +170,42 @@ L2_API int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters
  * (weights + activations + KV rows), batch 1. 0 for an invalid kind. */
 L2_API double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos);
 
+/* Largest vocabulary l2_classify_greedy_noalloc accepts: its logits live in a
+ * fixed device array of this many floats (1 MiB), after a 256-byte state block. */
+#define L2_NOALLOC_MAX_VOCAB 262144
+
+/* Final RMSNorm + vocabulary classifier + greedy argmax of one hidden state,
+ * without allocating any memory. The pages have no counterpart: this is a
+ * library convenience for callers that cannot call cudaMalloc, such as a host
+ * program whose device memory belongs to another framework's arena, or a
+ * serving loop that must not stall its other streams on cudaMalloc/cudaFree.
+ * It computes logits = Wcls * rmsnorm(x, gain) and the lowest index of the
+ * largest logit, with the same kernel as the classifier of l2_forward.
+ *   d_x      device fp32 [dim], the hidden state after the last layer
+ *   d_gain   device fp32 [dim], the final RMSNorm gain
+ *   d_wcls   device fp32 [vocab][dim], row-major classifier
+ *            (all three 16-byte aligned, read only, owned by the caller)
+ *   d_token  device int32 [1], output: the greedy token, or -1 when a
+ *            bounded device wait gave up
+ *   d_logit  device fp32 [1], output, or NULL: the logit of that token
+ * Queued on `stream` (a cudaStream_t, NULL = legacy default stream); returns
+ * without waiting.
+ * Scratch: a file-scope device array of 256 + 4 * L2_NOALLOC_MAX_VOCAB bytes,
+ * which every GPU that loads the library holds until the process exits. All
+ * calls on a device share it and it keeps the last call's contents; each call
+ * clears what must start at zero itself. Calls that overlap on the GPU (on
+ * unordered streams, or from several threads) race on it: order them.
+ * The first call on a device, made with that device current, looks up the
+ * array's device address and sets kernel attributes; make that first call
+ * before any stream capture.
+ * Errors (return code only; l2_last_error does not cover this call):
+ * L2_EINVAL for a NULL input or token pointer, vocab outside
+ * [1, L2_NOALLOC_MAX_VOCAB], dim not a multiple of 4 in [4, 16384], eps < 0 or
+ * a pointer that is not 16-byte aligned; L2_ECUDA when a CUDA call fails. */
+L2_API int l2_classify_greedy_noalloc(const float* d_x, const float* d_gain, const float* d_wcls,
+                                      int32_t dim, int32_t vocab, float norm_eps,
+                                      int32_t* d_token, float* d_logit, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,7 +5,8 @@ CUDA kernels. There is no CPU fallback; importing this package fails loudly when
 the library has not been built (``python llama_fp32_token_decode_b300/build.py``).
 Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
 l2_generate, l2_generate_device, l2_generate_batch, l2_reset, l2_destroy,
-l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes.
+l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
+l2_classify_greedy_noalloc.
 """
 from __future__ import annotations
 
@@ -27,7 +28,9 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_reset", "l2_destroy",
-           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes")
+           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc")
+
+L2_NOALLOC_MAX_VOCAB = 262144
 
 
 class L2Config(ctypes.Structure):
@@ -67,6 +70,8 @@ _SIG = {
     "l2_last_error": (ctypes.c_char_p, [_P]),
     "l2_time_kernel": (ctypes.c_int, [_P, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]),
     "l2_kernel_bytes": (ctypes.c_double, [_P, _I, _I]),
+    "l2_classify_greedy_noalloc": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P, _P,
+                                                  _P]),
 }
 for _name, (_res, _args) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -173,6 +178,15 @@ def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:
 
 def l2_kernel_bytes(h, kind: int, pos: int) -> float:
     return float(_lib.l2_kernel_bytes(h, kind, pos))
+
+
+def l2_classify_greedy_noalloc(d_x, d_gain, d_wcls, dim: int, vocab: int, norm_eps: float,
+                               d_token, d_logit=None, stream=None) -> int:
+    """Greedy token of one hidden state; device buffers (torch tensors or ints).
+    Returns the C return code (no exception: the call has no error text)."""
+    return int(_lib.l2_classify_greedy_noalloc(
+        _ptr(d_x), _ptr(d_gain), _ptr(d_wcls), dim, vocab, norm_eps, _ptr(d_token),
+        _ptr(d_logit) if d_logit is not None else None, _stream(stream)))
 
 
 def _stream(stream):
