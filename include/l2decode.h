@@ -170,6 +170,20 @@ L2_API int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters
  * (weights + activations + KV rows), batch 1. 0 for an invalid kind. */
 L2_API double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos);
 
+/* Test and measurement hook of the batched path's tensor-core GEMM:
+ * C[M][N] = A[M][K] * W[N][K]^T, every matrix fp32 row-major in device memory
+ * owned by the caller (16-byte aligned). The operands are split into tf32
+ * (hi, lo) pairs and multiplied as A_hi W_hi + A_hi W_lo + A_lo W_hi on the
+ * tcgen05 tensor cores with fp32 accumulation (the 3xTF32 scheme), the kernel
+ * that carries every projection of batched decode. Allocates and frees its
+ * split buffers; synchronous on `stream`. With iters > 0 it then times `iters`
+ * launches of the GEMM kernel alone (CUDA events on `stream`) and writes the
+ * mean milliseconds per launch to *ms.
+ * Errors: L2_EINVAL (NULL or misaligned pointer, M or N < 1, K < 4 or not a
+ * multiple of 4, iters < 0), L2_ENOMEM, L2_ECUDA, L2_ETIMEOUT. */
+L2_API int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, int32_t M, int32_t N,
+                          int32_t K, int32_t iters, float* ms, void* stream);
+
 /* Largest vocabulary l2_classify_greedy_noalloc accepts: its logits live in a
  * fixed device array of this many floats (1 MiB), after a 256-byte state block. */
 #define L2_NOALLOC_MAX_VOCAB 262144

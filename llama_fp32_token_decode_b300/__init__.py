@@ -6,7 +6,7 @@ the library has not been built (``python llama_fp32_token_decode_b300/build.py``
 Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
 l2_generate, l2_generate_device, l2_generate_batch, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
-l2_classify_greedy_noalloc.
+l2_classify_greedy_noalloc, l2_gemm_tf32x3.
 """
 from __future__ import annotations
 
@@ -28,7 +28,8 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_reset", "l2_destroy",
-           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc")
+           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
+           "l2_gemm_tf32x3")
 
 L2_NOALLOC_MAX_VOCAB = 262144
 
@@ -70,6 +71,8 @@ _SIG = {
     "l2_last_error": (ctypes.c_char_p, [_P]),
     "l2_time_kernel": (ctypes.c_int, [_P, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]),
     "l2_kernel_bytes": (ctypes.c_double, [_P, _I, _I]),
+    "l2_gemm_tf32x3": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_float),
+                                      _P]),
     "l2_classify_greedy_noalloc": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P, _P,
                                                   _P]),
 }
@@ -178,6 +181,17 @@ def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:
 
 def l2_kernel_bytes(h, kind: int, pos: int) -> float:
     return float(_lib.l2_kernel_bytes(h, kind, pos))
+
+
+def l2_gemm_tf32x3(d_A, d_W, d_C, M: int, N: int, K: int, iters: int = 0, stream=None):
+    """C = A W^T through the 3xTF32 tensor-core kernel (device buffers). Returns
+    the mean ms of `iters` timed launches (None when iters == 0)."""
+    ms = ctypes.c_float()
+    rc = _lib.l2_gemm_tf32x3(_ptr(d_A), _ptr(d_W), _ptr(d_C), M, N, K, iters,
+                             ctypes.byref(ms) if iters else None, _stream(stream))
+    if rc != L2_OK:
+        raise L2Error(rc, "l2_gemm_tf32x3 failed")
+    return float(ms.value) if iters else None
 
 
 def l2_classify_greedy_noalloc(d_x, d_gain, d_wcls, dim: int, vocab: int, norm_eps: float,

@@ -1,0 +1,550 @@
+// gemm_tf32x3.cu -- fp32-accurate tensor-core GEMM of the batched decode step.
+//
+// With B sequences decoded in lockstep, every projection of the Llama-2
+// decode step (the fp32 engine of the llama2.c pages) becomes a dense
+// contraction  C[B][N] = X[B][K] * W[N][K]^T.  fp32 accuracy on the tensor
+// cores comes from the 3xTF32 split: every operand is stored as a pair
+// hi = round_tf32(v), lo = v - hi (exact in fp32), and
+//     C = Xhi*Whi + Xhi*Wlo + Xlo*Whi
+// drops only the Xlo*Wlo term (relative size 2^-22), with fp32 accumulation.
+//
+// Kernel (sm_103a, one 128 x BN output tile per CTA, 128 threads):
+//   * warp 0 lane 0 streams K-blocks of 32 floats (128 bytes, one 128-byte
+//     swizzle row) of Xhi, Xlo, Whi, Wlo into a ring of shared-memory stages
+//     with 3-D TMA tile loads (completion on mbarriers); weight tiles of the
+//     first stages are requested before griddepcontrol.wait, since weights
+//     never depend on the previous kernel;
+//   * warp 1 lane 0 issues tcgen05.mma kind::tf32 (M 128, N BN, K 8) from the
+//     stages into one TMEM accumulator (128 lanes x BN fp32 columns) and frees
+//     each stage with tcgen05.commit;
+//   * all four warps then read the accumulator with tcgen05.ld (warp w owns
+//     TMEM lanes 32w..32w+31 = output rows) and apply the fused epilogue.
+// Every wait is bounded; on a timeout the kernel records ERR_TIMEOUT_TMA,
+// drains its own copies, frees its TMEM and returns.
+#include <math.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "l2_internal.cuh"
+
+namespace l2 {
+
+namespace {
+
+// ------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::tf32, cta_group::1.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride
+// byte offset), leading byte offset unused for this layout (encoded 1),
+// descriptor version 1 (bits 46-48), swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B tf32
+// (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int BN>
+struct Cfg {
+    static constexpr int BM = 128, BK = 32;
+    static constexpr int A_BYTES = BM * BK * 4;  // 16 KB
+    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int STAGES = (BN == 128) ? 3 : 4;
+    static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 256;
+    static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
+};
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mA_hi,
+                       const __grid_constant__ CUtensorMap mA_lo,
+                       const __grid_constant__ CUtensorMap mB_hi,
+                       const __grid_constant__ CUtensorMap mB_lo, const GemmArgs g) {
+    using C = Cfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* gbase = smem_raw + (base - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * C::STAGE);
+    uint64_t* empty = full + S;
+    uint64_t* accb = empty + S;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    __shared__ int s_err;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = (g.M + 127) / 128;
+    const int m0 = (blockIdx.x % mt) * 128;
+    const int n0 = (blockIdx.x / mt) * BN;
+    const int KB = (g.K + 31) / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accb, 1);
+        fence_mbar_init();
+        s_err = 0;
+        prefetch_map(&mA_hi);
+        prefetch_map(&mA_lo);
+        prefetch_map(&mB_hi);
+        prefetch_map(&mB_lo);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    auto a_hi = [&](int s) { return base + static_cast<uint32_t>(s * C::STAGE); };
+    auto a_lo = [&](int s) { return a_hi(s) + C::A_BYTES; };
+    auto b_hi = [&](int s) { return a_hi(s) + 2 * C::A_BYTES; };
+    auto b_lo = [&](int s) { return b_hi(s) + C::B_BYTES; };
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer
+        const int pre = KB < S ? KB : S;
+        for (int kb = 0; kb < pre; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], C::STAGE);
+            tma_load_3d(b_hi(kb), &mB_hi, kb * 32, n0, g.layer, &full[kb]);
+            tma_load_3d(b_lo(kb), &mB_lo, kb * 32, n0, g.layer, &full[kb]);
+        }
+        pdl_wait();  // activations come from the previous kernel
+        for (int kb = 0; kb < pre; ++kb) {
+            tma_load_3d(a_hi(kb), &mA_hi, kb * 32, m0, 0, &full[kb]);
+            tma_load_3d(a_lo(kb), &mA_lo, kb * 32, m0, 0, &full[kb]);
+        }
+        int issued = pre;
+        for (int kb = pre; kb < KB; ++kb) {
+            const int s = kb % S;
+            if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(kb / S - 1) & 1u)) {
+                s_err = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(&full[s], C::STAGE);
+            tma_load_3d(b_hi(s), &mB_hi, kb * 32, n0, g.layer, &full[s]);
+            tma_load_3d(b_lo(s), &mB_lo, kb * 32, n0, g.layer, &full[s]);
+            tma_load_3d(a_hi(s), &mA_hi, kb * 32, m0, 0, &full[s]);
+            tma_load_3d(a_lo(s), &mA_lo, kb * 32, m0, 0, &full[s]);
+            issued = kb + 1;
+        }
+        if (s_err) {  // let the copies in flight land before the CTA leaves
+            for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
+                mbar_wait_bounded(&full[q % S], static_cast<uint32_t>(q / S) & 1u);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        constexpr uint32_t idesc = idesc_tf32(128, BN);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % S;
+            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(kb / S) & 1u)) {
+                s_err = 1;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t ah = sw128_desc(a_hi(s) + 32 * k);
+                const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
+                const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
+                const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
+                mma_tf32(tmem, al, bh, idesc, (kb | k) != 0);
+                mma_tf32(tmem, ah, bl, idesc, 1u);
+                mma_tf32(tmem, ah, bh, idesc, 1u);
+            }
+            mma_commit(&empty[s]);
+        }
+        mma_commit(accb);  // completes once every MMA issued above has
+    }
+    __syncwarp();
+
+    // ---- epilogue
+    if (!mbar_wait_bounded(accb, 0u)) s_err = 1;
+    tc_fence_after();
+    __syncthreads();
+    if (s_err) {
+        if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
+    } else {
+        const int r = m0 + 32 * warp + lane;
+        const bool row_ok = r < g.M;
+        int pos = 0, active = 1;
+        if constexpr (EPI == GEPI_QKV_ROPE) {
+            if (row_ok) {
+                pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
+                active = g.active ? __ldcg(g.active + r) : 1;
+            }
+        }
+        unsigned long long best = 0ull;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            __syncwarp();  // tcgen05.ld is warp-collective
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+            const int gc0 = n0 + 32 * c;
+            if (!row_ok || gc0 >= g.N) continue;
+            const bool full_chunk = gc0 + 32 <= g.N;
+            if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
+                float* o = g.out + static_cast<size_t>(r) * g.ldc + gc0;
+                if (full_chunk && (g.ldc & 3) == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 w = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        if constexpr (EPI == GEPI_RESIDUAL) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4*>(o + j));
+                            w.x += x.x;
+                            w.y += x.y;
+                            w.z += x.z;
+                            w.w += x.w;
+                        }
+                        *reinterpret_cast<float4*>(o + j) = w;
+                    }
+                } else {
+                    for (int j = 0; j < 32 && gc0 + j < g.N; ++j)
+                        o[j] = (EPI == GEPI_RESIDUAL) ? __ldcg(o + j) + v[j] : v[j];
+                }
+            } else if constexpr (EPI == GEPI_SWIGLU) {
+                // interleaved rows: column 2j is the gate, 2j+1 the up projection
+                const size_t F = static_cast<size_t>(g.N) >> 1;
+                float* oh = g.out_hi + static_cast<size_t>(r) * F + (gc0 >> 1);
+                float* ol = g.out_lo + static_cast<size_t>(r) * F + (gc0 >> 1);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    if (gc0 + j + 1 < g.N) {
+                        const float h = silu(v[j]) * v[j + 1];
+                        const float hi = tf32_round(h);
+                        oh[j >> 1] = hi;
+                        ol[j >> 1] = h - hi;
+                    }
+                }
+            } else if constexpr (EPI == GEPI_QKV_ROPE) {
+                if (!active) continue;
+                const int hd = g.head_dim;
+                const float2* rope = g.rope + static_cast<size_t>(pos) * (hd >> 1);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const int gc = gc0 + j;
+                    if (gc + 1 >= g.N) break;
+                    const float x0 = v[j], x1 = v[j + 1];
+                    if (gc < g.d) {
+                        const float2 cs = rope[(gc % hd) >> 1];
+                        float* q = g.q + static_cast<size_t>(r) * g.d + gc;
+                        q[0] = x0 * cs.x - x1 * cs.y;
+                        q[1] = x0 * cs.y + x1 * cs.x;
+                    } else if (gc < g.d + g.kvd) {
+                        const int jj = gc - g.d, kvh = jj / hd, e = jj % hd;
+                        const float2 cs = rope[e >> 1];
+                        float* dst = g.k_cache + static_cast<size_t>(r) * g.cache_seq +
+                                     (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                        dst[0] = x0 * cs.x - x1 * cs.y;
+                        dst[1] = x0 * cs.y + x1 * cs.x;
+                    } else {
+                        const int jj = gc - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
+                        float* dst = g.v_cache + static_cast<size_t>(r) * g.cache_seq +
+                                     (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                        dst[0] = x0;
+                        dst[1] = x1;
+                    }
+                }
+            } else if constexpr (EPI == GEPI_ARGMAX) {
+                float* o = g.out ? g.out + static_cast<size_t>(r) * g.ldc + gc0 : nullptr;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (gc0 + j < g.N) {
+                        if (o) o[j] = v[j];
+                        const unsigned long long k = argmax_key(v[j], gc0 + j);
+                        best = k > best ? k : best;
+                    }
+                }
+            }
+        }
+        if constexpr (EPI == GEPI_ARGMAX) {
+            if (row_ok && best != 0ull) atomicMax(g.argmax_keys + r, best);
+        }
+    }
+
+    // ---- teardown: every tcgen05 access of this CTA is complete
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+__global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restrict__ hi,
+                                  float4* __restrict__ lo, long long n4) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 v = x[i];
+        float4 h;
+        h.x = tf32_round(v.x);
+        h.y = tf32_round(v.y);
+        h.z = tf32_round(v.z);
+        h.w = tf32_round(v.w);
+        hi[i] = h;
+        lo[i] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool pdl) {
+    using C = Cfg<BN>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(C::SMEM));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg{};
+    const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
+    cfg.gridDim = dim3(mt * nt);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI>, m.a_hi, m.a_lo, m.b_hi, m.b_lo,
+                              g);
+}
+
+template <int BN>
+cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool pdl) {
+    switch (epi) {
+        case GEPI_STORE: return launch_t<BN, GEPI_STORE>(m, g, s, pdl);
+        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL>(m, g, s, pdl);
+        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU>(m, g, s, pdl);
+        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE>(m, g, s, pdl);
+        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX>(m, g, s, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+// Tensor map of a fp32 array [layers][rows][inner] (inner contiguous) read in
+// boxes of 32 x box_rows x 1 with the 128-byte swizzle; out-of-range
+// elements read as zero.
+cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, long long rows,
+                          long long layers, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || inner % 4 != 0 || box_rows < 1 ||
+        box_rows > 256)
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(layers)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 4,
+                                   static_cast<cuuint64_t>(inner) * rows * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int gemm_tile_n(int N) { return N >= 8192 ? 128 : 64; }
+
+cudaError_t launch_gemm(int epi, int bn, const GemmMaps& m, const GemmArgs& g, cudaStream_t s,
+                        bool pdl) {
+    if (g.M < 1 || g.N < 1 || g.K < 4 || g.K % 4 != 0) return cudaErrorInvalidValue;
+    if (bn == 128) return launch_bn<128>(epi, m, g, s, pdl);
+    if (bn == 64) return launch_bn<64>(epi, m, g, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s) {
+    if (n % 4 != 0) return cudaErrorInvalidValue;
+    const long long n4 = n / 4;
+    const int blocks = static_cast<int>(n4 / 256 + 1 < 8192 ? n4 / 256 + 1 : 8192);
+    split_tf32_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x),
+                                             reinterpret_cast<float4*>(hi),
+                                             reinterpret_cast<float4*>(lo), n4);
+    return cudaGetLastError();
+}
+
+}  // namespace l2
+
+// ------------------------------------------------------------- test / measurement hook
+
+extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, int32_t M,
+                              int32_t N, int32_t K, int32_t iters, float* ms, void* stream) {
+    using namespace l2;
+    if (!d_A || !d_W || !d_C || M < 1 || N < 1 || K < 4 || K % 4 != 0 || iters < 0 ||
+        (iters > 0 && !ms))
+        return L2_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_A) | reinterpret_cast<uintptr_t>(d_W) |
+         reinterpret_cast<uintptr_t>(d_C)) & 15u)
+        return L2_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t na = static_cast<size_t>(M) * K, nw = static_cast<size_t>(N) * K;
+    const size_t na_pad = (na + 63) & ~static_cast<size_t>(63);
+    const size_t nw_pad = (nw + 63) & ~static_cast<size_t>(63);
+    float* buf = nullptr;
+    cudaError_t e = cudaMalloc(&buf, (2 * na_pad + 2 * nw_pad) * sizeof(float) + 256);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? L2_ENOMEM : L2_ECUDA;
+    float *a_hi = buf, *a_lo = buf + na_pad, *w_hi = a_lo + na_pad, *w_lo = w_hi + nw_pad;
+    int* d_err = reinterpret_cast<int*>(w_lo + nw_pad);
+    int rc = L2_OK;
+    const int bn = gemm_tile_n(N);
+    GemmMaps maps;
+    GemmArgs g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ldc = N;
+    g.out = d_C;
+    g.err = d_err;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    do {
+        if ((e = cudaMemsetAsync(d_err, 0, sizeof(int), s)) != cudaSuccess) break;
+        if ((e = launch_split_tf32(d_A, a_hi, a_lo, static_cast<long long>(na), s)) != cudaSuccess)
+            break;
+        if ((e = launch_split_tf32(d_W, w_hi, w_lo, static_cast<long long>(nw), s)) != cudaSuccess)
+            break;
+        if ((e = make_gemm_map(&maps.a_hi, a_hi, K, M, 1, 128)) != cudaSuccess) break;
+        if ((e = make_gemm_map(&maps.a_lo, a_lo, K, M, 1, 128)) != cudaSuccess) break;
+        if ((e = make_gemm_map(&maps.b_hi, w_hi, K, N, 1, bn)) != cudaSuccess) break;
+        if ((e = make_gemm_map(&maps.b_lo, w_lo, K, N, 1, bn)) != cudaSuccess) break;
+        if ((e = launch_gemm(GEPI_STORE, bn, maps, g, s, false)) != cudaSuccess) break;
+        if (iters > 0) {
+            if ((e = cudaEventCreate(&e0)) != cudaSuccess) break;
+            if ((e = cudaEventCreate(&e1)) != cudaSuccess) break;
+            if ((e = cudaEventRecord(e0, s)) != cudaSuccess) break;
+            for (int i = 0; i < iters && e == cudaSuccess; ++i)
+                e = launch_gemm(GEPI_STORE, bn, maps, g, s, false);
+            if (e != cudaSuccess) break;
+            if ((e = cudaEventRecord(e1, s)) != cudaSuccess) break;
+        }
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) break;
+        if (iters > 0) {
+            float t = 0.0f;
+            if ((e = cudaEventElapsedTime(&t, e0, e1)) != cudaSuccess) break;
+            *ms = t / iters;
+        }
+        int err = 0;
+        if ((e = cudaMemcpy(&err, d_err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) break;
+        if (err) rc = L2_ETIMEOUT;
+    } while (0);
+    if (e != cudaSuccess) rc = (e == cudaErrorInvalidValue) ? L2_EINVAL : L2_ECUDA;
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(buf);
+    return rc;
+}

@@ -2,6 +2,7 @@
 // kernels of the decode library (sm_103a only).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -89,6 +90,41 @@ struct AttnArgs {
     L2State* st;
 };
 
+// Fused epilogues of the batched 3xTF32 GEMM (gemm_tf32x3.cu).
+enum GemmEpilogue : int {
+    GEPI_STORE = 0,     // out[r][c] = acc
+    GEPI_RESIDUAL = 1,  // out[r][c] += acc
+    GEPI_SWIGLU = 2,    // interleaved W1/W3 columns -> hb (tf32 hi/lo pair)
+    GEPI_QKV_ROPE = 3,  // q rows rotated to q; k rotated and v appended to each row's cache
+    GEPI_ARGMAX = 4,    // per-row packed (value, index) atomicMax; logits stored if out != null
+};
+
+// The four operand maps of one GEMM launch: X (hi, lo) [1][Mcap][K] and
+// W (hi, lo) [L][N][K].
+struct GemmMaps {
+    CUtensorMap a_hi, a_lo, b_hi, b_lo;
+};
+
+struct GemmArgs {
+    int M, N, K;          // rows (sequences), output columns, reduction length
+    int layer;            // weight map z coordinate
+    int ldc;              // row stride of out
+    float* out;           // STORE / RESIDUAL / ARGMAX (logits, may be null)
+    float* out_hi;        // SWIGLU: hb hi [M][N/2]
+    float* out_lo;        // SWIGLU: hb lo
+    // QKV + RoPE + KV append
+    float* q;             // [M][d]
+    float* k_cache;       // this layer's K cache of sequence 0; sequence r at + r*cache_seq
+    float* v_cache;
+    const float2* rope;   // [S][hd/2]
+    const int* pos;       // [M] position of each row
+    const int* active;    // [M] 0 = finished sequence (no KV write) or null
+    int d, kvd, head_dim, seq_len;
+    size_t cache_seq;     // floats of one sequence's cache (all layers)
+    unsigned long long* argmax_keys;  // ARGMAX: [M]
+    int* err;             // ERR_* bits
+};
+
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -165,6 +201,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Nearest tf32 value of v (10 explicit mantissa bits, ties away from zero);
+// infinities and NaN pass through. v - tf32_round(v) is exact in fp32.
+__device__ __forceinline__ float tf32_round(float v) {
+    uint32_t u = __float_as_uint(v);
+    if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x1000u) & 0xffffe000u;
+    return __uint_as_float(u);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -215,6 +259,14 @@ int attn_nsplit(int n_heads, int seq_len, int num_sms);
 cudaError_t prepare_attention();
 int attn_cluster_ok(int head_dim, int nsplit, int n_heads);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+
+// gemm_tf32x3.cu
+cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, long long rows,
+                          long long layers, int box_rows);
+int gemm_tile_n(int N);
+cudaError_t launch_gemm(int epi, int bn, const GemmMaps& m, const GemmArgs& g, cudaStream_t s,
+                        bool pdl);
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
 
 // layout.cu
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
