@@ -45,6 +45,26 @@ struct l2_handle {
     int nsplit = 1;
     uint64_t policy = 0;
 
+    // batched path (max_batch > 1): weights as tf32 (hi, lo) pairs, [Mcap][...]
+    // activation rows, per-sequence state and the GEMM operand maps
+    int mcap = 0;
+    float* bw = nullptr;
+    float *qkv_hi = nullptr, *qkv_lo = nullptr, *wo_hi = nullptr, *wo_lo = nullptr;
+    float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
+    float *cls_hi = nullptr, *cls_lo = nullptr;
+    float* bact = nullptr;
+    float *bx = nullptr, *xn_hi = nullptr, *xn_lo = nullptr, *bq = nullptr;
+    float *att_hi = nullptr, *att_lo = nullptr, *hb_hi = nullptr, *hb_lo = nullptr;
+    float* blogits = nullptr;
+    int* bst = nullptr;
+    int *b_pos = nullptr, *b_token = nullptr, *b_active = nullptr, *b_len = nullptr;
+    int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
+    unsigned long long* b_keys = nullptr;
+    GemmMaps m_qkv{}, m_wo{}, m_w13{}, m_w2{}, m_cls{};
+    int bn_qkv = 64, bn_wo = 64, bn_w13 = 64, bn_w2 = 64, bn_cls = 128;
+    cudaGraphExec_t bgraph = nullptr;  // one batched generation step
+    int bgraph_M = 0, bgraph_steps = 0;
+
     cudaStream_t stream = nullptr;
     cudaGraphExec_t fwd1 = nullptr;  // one forward
     cudaGraphExec_t fwdN = nullptr;  // kGraphBatch forwards
@@ -230,6 +250,221 @@ int check_device_error(l2_handle* h) {
     return L2_OK;
 }
 
+// ---------------------------------------------------------------- batched path
+
+// One lockstep step of M sequences: embedding + RMSNorm, then per layer the
+// QKV GEMM (RoPE + KV append), attention, Wo GEMM + residual, RMSNorm, W1/W3
+// GEMM + SwiGLU, W2 GEMM + residual, RMSNorm; the classifier GEMM with the
+// per-row argmax; and the per-sequence advance.
+cudaError_t enqueue_bstep(l2_handle* h, int M, int mode, int steps, bool want_logits,
+                          cudaStream_t s) {
+    const l2_config& c = h->cfg;
+    const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
+    cudaError_t e;
+    BNormArgs n{};
+    n.x = h->bx;
+    n.emb = h->emb;
+    n.token = h->b_token;
+    n.gain = h->g_att;
+    n.xn_hi = h->xn_hi;
+    n.xn_lo = h->xn_lo;
+    n.d = d;
+    n.vocab = V;
+    n.eps = c.norm_eps;
+    if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
+    n.emb = nullptr;
+
+    GemmArgs g0{};
+    g0.M = M;
+    g0.err = &h->st->err;
+    g0.d = d;
+    g0.kvd = h->kvd;
+    g0.head_dim = h->hd;
+    g0.seq_len = c.seq_len;
+    g0.cache_seq = h->cache_seq;
+    g0.rope = h->rope;
+    g0.pos = h->b_pos;
+    g0.active = h->b_active;
+    for (int l = 0; l < L; ++l) {
+        GemmArgs g = g0;
+        g.layer = l;
+        g.N = d + 2 * h->kvd;
+        g.K = d;
+        g.q = h->bq;
+        g.k_cache = h->k_cache + l * h->cache_layer;
+        g.v_cache = h->v_cache + l * h->cache_layer;
+        if ((e = launch_gemm(GEPI_QKV_ROPE, h->bn_qkv, h->m_qkv, g, s, true)) != cudaSuccess) return e;
+
+        BAttnArgs t{};
+        t.q = h->bq;
+        t.k_cache = h->k_cache + l * h->cache_layer;
+        t.v_cache = h->v_cache + l * h->cache_layer;
+        t.att_hi = h->att_hi;
+        t.att_lo = h->att_lo;
+        t.pos = h->b_pos;
+        t.active = h->b_active;
+        t.d = d;
+        t.n_heads = c.n_heads;
+        t.n_kv_heads = c.n_kv_heads;
+        t.head_dim = h->hd;
+        t.seq_len = c.seq_len;
+        t.cache_seq = h->cache_seq;
+        if ((e = launch_battn(t, M, s, true)) != cudaSuccess) return e;
+
+        g = g0;
+        g.layer = l;
+        g.N = d;
+        g.K = d;
+        g.out = h->bx;
+        g.ldc = d;
+        if ((e = launch_gemm(GEPI_RESIDUAL, h->bn_wo, h->m_wo, g, s, true)) != cudaSuccess) return e;
+
+        n.gain = h->g_ffn + static_cast<size_t>(l) * d;
+        if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
+
+        g = g0;
+        g.layer = l;
+        g.N = 2 * F;
+        g.K = d;
+        g.out_hi = h->hb_hi;
+        g.out_lo = h->hb_lo;
+        if ((e = launch_gemm(GEPI_SWIGLU, h->bn_w13, h->m_w13, g, s, true)) != cudaSuccess) return e;
+
+        g = g0;
+        g.layer = l;
+        g.N = d;
+        g.K = F;
+        g.out = h->bx;
+        g.ldc = d;
+        if ((e = launch_gemm(GEPI_RESIDUAL, h->bn_w2, h->m_w2, g, s, true)) != cudaSuccess) return e;
+
+        n.gain = (l + 1 < L) ? h->g_att + static_cast<size_t>(l + 1) * d : h->g_final;
+        if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
+    }
+    GemmArgs g = g0;
+    g.layer = 0;
+    g.N = V;
+    g.K = d;
+    g.out = want_logits ? h->blogits : nullptr;
+    g.ldc = V;
+    g.argmax_keys = h->b_keys;
+    if ((e = launch_gemm(GEPI_ARGMAX, h->bn_cls, h->m_cls, g, s, true)) != cudaSuccess) return e;
+
+    BAdvanceArgs a{};
+    a.M = M;
+    a.mode = mode;
+    a.steps = steps;
+    a.keys = h->b_keys;
+    a.last = h->b_last;
+    a.pos = h->b_pos;
+    a.token = h->b_token;
+    a.active = h->b_active;
+    a.len = h->b_len;
+    a.poff = h->b_poff;
+    a.prompts = h->b_prompts;
+    a.out = h->b_out;
+    return launch_badvance(a, s, true);
+}
+
+// Rows [0, M): active, keys cleared; for generation, pos 0 and the first prompt token.
+__global__ void binit_kernel(int M, int mode, int* pos, int* token, int* active,
+                             const int* len, const int* poff, const int* prompts,
+                             unsigned long long* keys, L2State* st) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b == 0) st->err = 0;
+    if (b >= M) return;
+    active[b] = 1;
+    keys[b] = 0ull;
+    if (mode == 1) {
+        pos[b] = 0;
+        token[b] = prompts[poff[b]];
+    }
+}
+
+// Allocates the batched path's buffers, splits the laid-out weights into tf32
+// pairs and builds the GEMM operand maps.
+int setup_batched(l2_handle* h) {
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, S = c.seq_len;
+    const size_t kvd = h->kvd, B = c.max_batch;
+    h->mcap = static_cast<int>((B + 127) / 128 * 128);
+    const size_t Mc = h->mcap;
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off += align64(n);
+        return o;
+    };
+    const size_t n_qkv = L * (d + 2 * kvd) * d, n_wo = L * d * d, n_w13 = L * 2 * F * d;
+    const size_t n_w2 = L * d * F, n_cls = V * d;
+    const size_t o_qh = take(n_qkv), o_ql = take(n_qkv), o_oh = take(n_wo), o_ol = take(n_wo);
+    const size_t o_uh = take(n_w13), o_ul = take(n_w13), o_dh = take(n_w2), o_dl = take(n_w2);
+    const size_t o_ch = take(n_cls), o_cl = take(n_cls);
+    L2_CUDA(h, cudaMalloc(&h->bw, off * sizeof(float)));
+    h->qkv_hi = h->bw + o_qh; h->qkv_lo = h->bw + o_ql;
+    h->wo_hi = h->bw + o_oh; h->wo_lo = h->bw + o_ol;
+    h->w13_hi = h->bw + o_uh; h->w13_lo = h->bw + o_ul;
+    h->w2_hi = h->bw + o_dh; h->w2_lo = h->bw + o_dl;
+    h->cls_hi = h->bw + o_ch; h->cls_lo = h->bw + o_cl;
+    cudaStream_t s = h->stream;
+    L2_CUDA(h, prepare_gemm());
+    L2_CUDA(h, launch_split_tf32(h->wqkv, h->qkv_hi, h->qkv_lo, n_qkv, s));
+    L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
+    L2_CUDA(h, launch_split_tf32(h->w13, h->w13_hi, h->w13_lo, n_w13, s));
+    L2_CUDA(h, launch_split_tf32(h->w2, h->w2_hi, h->w2_lo, n_w2, s));
+    L2_CUDA(h, launch_split_tf32(h->wcls, h->cls_hi, h->cls_lo, n_cls, s));
+
+    off = 0;
+    const size_t o_x = take(Mc * d), o_nh = take(Mc * d), o_nl = take(Mc * d), o_q = take(Mc * d);
+    const size_t o_ah = take(Mc * d), o_al = take(Mc * d), o_hh = take(Mc * F), o_hl = take(Mc * F);
+    const size_t o_lg = take(B * V);
+    L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
+    L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));
+    h->bx = h->bact + o_x; h->xn_hi = h->bact + o_nh; h->xn_lo = h->bact + o_nl;
+    h->bq = h->bact + o_q; h->att_hi = h->bact + o_ah; h->att_lo = h->bact + o_al;
+    h->hb_hi = h->bact + o_hh; h->hb_lo = h->bact + o_hl; h->blogits = h->bact + o_lg;
+
+    off = 0;
+    const size_t o_pos = take(Mc), o_tok = take(Mc), o_act = take(Mc), o_len = take(Mc);
+    const size_t o_poff = take(Mc), o_last = take(Mc), o_pr = take(B * S), o_out = take(B * S);
+    const size_t o_keys = take(2 * Mc);
+    L2_CUDA(h, cudaMalloc(&h->bst, off * sizeof(int)));
+    L2_CUDA(h, cudaMemsetAsync(h->bst, 0, off * sizeof(int), s));
+    h->b_pos = h->bst + o_pos; h->b_token = h->bst + o_tok; h->b_active = h->bst + o_act;
+    h->b_len = h->bst + o_len; h->b_poff = h->bst + o_poff; h->b_last = h->bst + o_last;
+    h->b_prompts = h->bst + o_pr; h->b_out = h->bst + o_out;
+    h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
+
+    h->bn_qkv = gemm_tile_n(static_cast<int>(d + 2 * kvd));
+    h->bn_wo = gemm_tile_n(static_cast<int>(d));
+    h->bn_w13 = gemm_tile_n(static_cast<int>(2 * F));
+    h->bn_w2 = gemm_tile_n(static_cast<int>(d));
+    h->bn_cls = gemm_tile_n(static_cast<int>(V));
+    const long long D = d, FF = F, LL = L, MC = Mc;
+    struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
+    const MapSpec specs[] = {
+        {&h->m_qkv.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_qkv.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_qkv.b_hi, h->qkv_hi, D, D + 2 * static_cast<long long>(kvd), LL, h->bn_qkv},
+        {&h->m_qkv.b_lo, h->qkv_lo, D, D + 2 * static_cast<long long>(kvd), LL, h->bn_qkv},
+        {&h->m_wo.a_hi, h->att_hi, D, MC, 1, 128}, {&h->m_wo.a_lo, h->att_lo, D, MC, 1, 128},
+        {&h->m_wo.b_hi, h->wo_hi, D, D, LL, h->bn_wo}, {&h->m_wo.b_lo, h->wo_lo, D, D, LL, h->bn_wo},
+        {&h->m_w13.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_w13.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_w13.b_hi, h->w13_hi, D, 2 * FF, LL, h->bn_w13},
+        {&h->m_w13.b_lo, h->w13_lo, D, 2 * FF, LL, h->bn_w13},
+        {&h->m_w2.a_hi, h->hb_hi, FF, MC, 1, 128}, {&h->m_w2.a_lo, h->hb_lo, FF, MC, 1, 128},
+        {&h->m_w2.b_hi, h->w2_hi, FF, D, LL, h->bn_w2}, {&h->m_w2.b_lo, h->w2_lo, FF, D, LL, h->bn_w2},
+        {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->bn_cls},
+        {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->bn_cls},
+    };
+    for (const MapSpec& m : specs) {
+        cudaError_t e = make_gemm_map(m.m, m.p, m.inner, m.rows, m.layers, m.box);
+        if (e != cudaSuccess) return cuda_fail(h, e, "tensor map (cuTensorMapEncodeTiled)");
+    }
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return L2_OK;
+}
+
 int upload(l2_handle* h, const float* blob, cudaMemcpyKind kind) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, kvd = h->kvd;
@@ -277,6 +512,13 @@ int upload(l2_handle* h, const float* blob, cudaMemcpyKind kind) {
 void free_all(l2_handle* h) {
     if (h->fwd1) cudaGraphExecDestroy(h->fwd1);
     if (h->fwdN) cudaGraphExecDestroy(h->fwdN);
+    if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+    cudaFree(h->bw);
+    cudaFree(h->bact);
+    cudaFree(h->bst);
+    h->bgraph = nullptr;
+    h->bw = h->bact = nullptr;
+    h->bst = nullptr;
     if (h->ev0) cudaEventDestroy(h->ev0);
     if (h->ev1) cudaEventDestroy(h->ev1);
     if (h->stream) cudaStreamDestroy(h->stream);
@@ -287,6 +529,38 @@ void free_all(l2_handle* h) {
     h->ev0 = h->ev1 = nullptr;
     h->stream = nullptr;
     h->weights = h->kv = h->act = nullptr;
+}
+
+// Batched forward of M rows whose tokens and positions are already in
+// b_token / b_pos (device values are clamped by the kernels).
+int bforward(l2_handle* h, int M, bool want_logits, cudaStream_t s) {
+    binit_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, 0, h->b_pos, h->b_token, h->b_active,
+                                                 h->b_len, h->b_poff, h->b_prompts, h->b_keys,
+                                                 h->st);
+    L2_CUDA(h, cudaGetLastError());
+    L2_CUDA(h, enqueue_bstep(h, M, 0, 0, want_logits, s));
+    return L2_OK;
+}
+
+int capture_bstep(l2_handle* h, int M, int steps) {
+    if (h->bgraph && h->bgraph_M == M && h->bgraph_steps == steps) return L2_OK;
+    if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+    h->bgraph = nullptr;
+    cudaGraph_t g = nullptr;
+    L2_CUDA(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = enqueue_bstep(h, M, 1, steps, false, h->stream);
+    cudaError_t e2 = cudaStreamEndCapture(h->stream, &g);
+    if (e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_fail(h, e, "batched step launch during capture");
+    }
+    if (e2 != cudaSuccess) return cuda_fail(h, e2, "cudaStreamEndCapture");
+    e = cudaGraphInstantiate(&h->bgraph, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphInstantiate");
+    h->bgraph_M = M;
+    h->bgraph_steps = steps;
+    return L2_OK;
 }
 
 }  // namespace
@@ -453,6 +727,7 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
         if (pinned) cudaHostUnregister(const_cast<float*>(blob));
     }
     if (rc != L2_OK) return bail(rc);
+    if (c.max_batch > 1 && (rc = setup_batched(h)) != L2_OK) return bail(rc);
 
     if ((rc = capture(h, 1, &h->fwd1)) != L2_OK) return bail(rc);
     if ((rc = capture(h, kGraphBatch, &h->fwdN)) != L2_OK) return bail(rc);
@@ -510,8 +785,20 @@ int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_po
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
     if (!d_tokens || !d_pos) return fail(h, L2_EINVAL, "NULL token or position buffer");
-    if (B != 1) return fail(h, L2_EINVAL, "batched forward is not available in this build");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B > 1) {
+        L2_CUDA(h, cudaMemcpyAsync(h->b_token, d_tokens, sizeof(int32_t) * B,
+                                   cudaMemcpyDeviceToDevice, s));
+        L2_CUDA(h, cudaMemcpyAsync(h->b_pos, d_pos, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice,
+                                   s));
+        int rc = bforward(h, B, d_logits != nullptr, s);
+        if (rc != L2_OK) return rc;
+        if (d_logits)
+            L2_CUDA(h, cudaMemcpyAsync(d_logits, h->blogits,
+                                       sizeof(float) * B * static_cast<size_t>(h->cfg.vocab_size),
+                                       cudaMemcpyDeviceToDevice, s));
+        return L2_OK;
+    }
     init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, d_tokens, d_pos, h->cfg.vocab_size,
                                       h->cfg.seq_len, 0, 0, nullptr, nullptr, 0);
     L2_CUDA(h, cudaGetLastError());
@@ -532,7 +819,20 @@ int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t 
         if (tokens[b] < 0 || tokens[b] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
         if (pos[b] < 0 || pos[b] >= h->cfg.seq_len) return fail(h, L2_EINVAL, "position out of range");
     }
-    if (B != 1) return fail(h, L2_EINVAL, "batched forward is not available in this build");
+    if (B > 1) {
+        L2_CUDA(h, cudaMemcpyAsync(h->b_token, tokens, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
+                                   h->stream));
+        L2_CUDA(h, cudaMemcpyAsync(h->b_pos, pos, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
+                                   h->stream));
+        int rc = bforward(h, B, logits_out != nullptr, h->stream);
+        if (rc != L2_OK) return rc;
+        if (logits_out)
+            L2_CUDA(h, cudaMemcpyAsync(logits_out, h->blogits,
+                                       sizeof(float) * B * static_cast<size_t>(h->cfg.vocab_size),
+                                       cudaMemcpyDeviceToHost, h->stream));
+        L2_CUDA(h, cudaStreamSynchronize(h->stream));
+        return check_device_error(h);
+    }
     init_state_kernel<<<1, 1, 0, h->stream>>>(h->st, pos[0], tokens[0], nullptr, nullptr,
                                               h->cfg.vocab_size, h->cfg.seq_len, 0, 0, nullptr,
                                               nullptr, 1);
@@ -583,8 +883,41 @@ int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t s
 int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
                       int32_t steps, int32_t* out_tokens) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
-    (void)prompts; (void)lens; (void)B; (void)steps; (void)out_tokens;
-    return fail(h, L2_EINVAL, "batched generation is not available in this build");
+    if (!prompts || !lens || !out_tokens) return fail(h, L2_EINVAL, "NULL prompts, lens or output");
+    if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
+    if (steps < 1) return fail(h, L2_EINVAL, "steps must be >= 1");
+    const int S = h->cfg.seq_len, V = h->cfg.vocab_size;
+    std::vector<int32_t> poff(B);
+    long long total = 0;
+    int max_len = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 1 || static_cast<long long>(lens[b]) + steps - 1 > S)
+            return fail(h, L2_EINVAL, "need lens[b] >= 1 and lens[b] + steps - 1 <= seq_len");
+        poff[b] = static_cast<int32_t>(total);
+        total += lens[b];
+        max_len = lens[b] > max_len ? lens[b] : max_len;
+    }
+    for (long long i = 0; i < total; ++i)
+        if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    if (h->cfg.max_batch == 1) return l2_generate(h, prompts, lens[0], steps, out_tokens);
+    cudaStream_t s = h->stream;
+    L2_CUDA(h, cudaMemcpyAsync(h->b_prompts, prompts, sizeof(int32_t) * total,
+                               cudaMemcpyHostToDevice, s));
+    L2_CUDA(h, cudaMemcpyAsync(h->b_len, lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
+    L2_CUDA(h, cudaMemcpyAsync(h->b_poff, poff.data(), sizeof(int32_t) * B, cudaMemcpyHostToDevice,
+                               s));
+    binit_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, 1, h->b_pos, h->b_token, h->b_active,
+                                                 h->b_len, h->b_poff, h->b_prompts, h->b_keys,
+                                                 h->st);
+    L2_CUDA(h, cudaGetLastError());
+    int rc = capture_bstep(h, B, steps);
+    if (rc != L2_OK) return rc;
+    const int n = max_len + steps - 1;
+    for (int i = 0; i < n; ++i) L2_CUDA(h, cudaGraphLaunch(h->bgraph, s));
+    L2_CUDA(h, cudaMemcpyAsync(out_tokens, h->b_out, sizeof(int32_t) * B * static_cast<size_t>(steps),
+                               cudaMemcpyDeviceToHost, s));
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return check_device_error(h);
 }
 
 int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,

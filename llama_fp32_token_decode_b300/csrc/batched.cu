@@ -1,0 +1,224 @@
+// batched.cu -- the non-GEMM kernels of batched decode: B independent
+// sequences advance one position per step in lockstep, each with its own
+// position, token and KV cache (the decode step of the llama2.c pages' fp32
+// engine, applied to B sequences at once). The projections of the step run in
+// the 3xTF32 tensor-core GEMM (gemm_tf32x3.cu); this file holds
+//   brmsnorm_kernel   optional embedding gather + RMSNorm, writing the
+//                     normalised rows as tf32 (hi, lo) pairs for the next GEMM
+//   battn_kernel      causal attention of every (sequence, head) over that
+//                     sequence's own cache, ragged lengths pos_b + 1, output
+//                     as a tf32 pair for the Wo GEMM
+//   badvance_kernel   greedy choice per sequence and the move to the next
+//                     position (prompt tokens are forced, then the argmax).
+#include <math.h>
+
+#include "l2_internal.cuh"
+
+namespace l2 {
+
+namespace {
+
+constexpr int kNormThreads = 128;
+constexpr int kBAttnThreads = 128;
+constexpr int kBAttnWarps = kBAttnThreads / 32;
+
+__global__ void __launch_bounds__(kNormThreads) brmsnorm_kernel(const BNormArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = a.d, d4 = d >> 2;
+    float4* x4 = reinterpret_cast<float4*>(a.x + static_cast<size_t>(b) * d);
+    const float4* src4 = x4;
+    if (a.emb != nullptr) {
+        const int tok = min(max(__ldcg(a.token + b), 0), a.vocab - 1);
+        src4 = reinterpret_cast<const float4*>(a.emb + static_cast<size_t>(tok) * d);
+    }
+    __shared__ float s_part[kNormThreads / 32];
+    float ss = 0.0f;
+    for (int i = tid; i < d4; i += kNormThreads) {
+        const float4 v = __ldcg(src4 + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_part[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(d) + a.eps);
+    const float4* g4 = reinterpret_cast<const float4*>(a.gain);
+    float4* hi4 = reinterpret_cast<float4*>(a.xn_hi + static_cast<size_t>(b) * d);
+    float4* lo4 = reinterpret_cast<float4*>(a.xn_lo + static_cast<size_t>(b) * d);
+    for (int i = tid; i < d4; i += kNormThreads) {
+        const float4 v = __ldcg(src4 + i);
+        if (a.emb != nullptr) x4[i] = v;
+        const float4 g = __ldg(g4 + i);
+        const float n0 = g.x * (inv * v.x), n1 = g.y * (inv * v.y);
+        const float n2 = g.z * (inv * v.z), n3 = g.w * (inv * v.w);
+        const float4 h = make_float4(tf32_round(n0), tf32_round(n1), tf32_round(n2), tf32_round(n3));
+        hi4[i] = h;
+        lo4[i] = make_float4(n0 - h.x, n1 - h.y, n2 - h.z, n3 - h.w);
+    }
+}
+
+// One CTA per (head, sequence). The four warps take groups of G positions
+// round-robin; each group's key and value loads are all issued before its G
+// dot products, then an online-softmax update. The warps' partial (max, sum,
+// output) are merged with log-sum-exp rescaling in shared memory.
+template <int EPL, int G>
+__global__ void __launch_bounds__(kBAttnThreads) battn_kernel(const BAttnArgs a) {
+    constexpr int HDMAX = 32 * EPL;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int h = blockIdx.x, b = blockIdx.y;
+    if (a.active != nullptr && __ldcg(a.active + b) == 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hd = a.head_dim;
+    const int kvh = h / (a.n_heads / a.n_kv_heads);
+    const int n = min(max(__ldcg(a.pos + b), 0), a.seq_len - 1) + 1;
+    const float* qrow = a.q + static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
+    const size_t head_off = static_cast<size_t>(b) * a.cache_seq +
+                            static_cast<size_t>(kvh) * a.seq_len * hd;
+    const float* Kh = a.k_cache + head_off;
+    const float* Vh = a.v_cache + head_off;
+    const float scale_div = sqrtf(static_cast<float>(hd));
+
+    float qr[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        qr[j] = e < hd ? __ldcg(qrow + e) : 0.0f;
+    }
+    float m = -INFINITY, l = 0.0f, o[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) o[j] = 0.0f;
+
+    for (int tb = warp * G; tb < n; tb += kBAttnWarps * G) {
+        float kr[G][EPL], vr[G][EPL];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int t = tb + g;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) {
+                const int e = lane + 32 * j;
+                const bool ok = (t < n) && (e < hd);
+                kr[g][j] = ok ? __ldcs(Kh + static_cast<size_t>(t) * hd + e) : 0.0f;
+                vr[g][j] = ok ? __ldcs(Vh + static_cast<size_t>(t) * hd + e) : 0.0f;
+            }
+        }
+        float sc[G];
+        float gmax = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float p = 0.0f;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) p = fmaf(qr[j], kr[g][j], p);
+            p = warp_sum(p);
+            sc[g] = (tb + g < n) ? p / scale_div : -INFINITY;
+            gmax = fmaxf(gmax, sc[g]);
+        }
+        const float mnew = fmaxf(m, gmax);
+        const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+        l *= corr;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) o[j] *= corr;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float p = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+            l += p;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) o[j] = fmaf(p, vr[g][j], o[j]);
+        }
+        m = mnew;
+    }
+
+    __shared__ float s_m[kBAttnWarps], s_l[kBAttnWarps];
+    __shared__ float s_o[kBAttnWarps][HDMAX];
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s_o[warp][lane + 32 * j] = o[j];
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kBAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+    float L = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kBAttnWarps; ++w)
+        if (s_m[w] != -INFINITY) L += s_l[w] * expf(s_m[w] - M);
+    float* ohi = a.att_hi + static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
+    float* olo = a.att_lo + static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
+    for (int e = tid; e < hd; e += kBAttnThreads) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kBAttnWarps; ++w)
+            if (s_m[w] != -INFINITY) acc += s_o[w][e] * expf(s_m[w] - M);
+        const float v = acc / L;
+        const float hi = tf32_round(v);
+        ohi[e] = hi;
+        olo[e] = v - hi;
+    }
+}
+
+__global__ void badvance_kernel(const BAdvanceArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= a.M) return;
+    const unsigned long long k = a.keys[b];
+    a.keys[b] = 0ull;
+    const int idx = (k == 0ull) ? 0 : argmax_key_index(k);
+    a.last[b] = idx;
+    if (a.mode != 1 || a.active[b] == 0) return;
+    const int p = a.pos[b], np = a.len[b];
+    if (p >= np - 1) {
+        const int k_out = p - (np - 1);
+        a.out[static_cast<size_t>(b) * a.steps + k_out] = idx;
+        if (k_out + 1 >= a.steps) {
+            a.active[b] = 0;  // finished: its row is still computed, never used
+            return;
+        }
+    }
+    a.token[b] = (p + 1 < np) ? a.prompts[a.poff[b] + p + 1] : idx;
+    a.pos[b] = p + 1;
+}
+
+template <typename Args, typename Kernel>
+cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, const Args& a, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+}  // namespace
+
+cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl) {
+    if (M < 1 || a.d % 4 != 0) return cudaErrorInvalidValue;
+    return launch_pdl(brmsnorm_kernel, dim3(M), dim3(kNormThreads), a, s, pdl);
+}
+
+cudaError_t launch_battn(const BAttnArgs& a, int M, cudaStream_t s, bool pdl) {
+    if (M < 1) return cudaErrorInvalidValue;
+    const dim3 grid(a.n_heads, M), block(kBAttnThreads);
+    if (a.head_dim <= 64) return launch_pdl(battn_kernel<2, 8>, grid, block, a, s, pdl);
+    if (a.head_dim <= 128) return launch_pdl(battn_kernel<4, 8>, grid, block, a, s, pdl);
+    if (a.head_dim <= 256) return launch_pdl(battn_kernel<8, 4>, grid, block, a, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_badvance(const BAdvanceArgs& a, cudaStream_t s, bool pdl) {
+    if (a.M < 1) return cudaErrorInvalidValue;
+    return launch_pdl(badvance_kernel, dim3((a.M + 127) / 128), dim3(128), a, s, pdl);
+}
+
+}  // namespace l2

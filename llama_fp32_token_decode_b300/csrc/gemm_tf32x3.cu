@@ -399,14 +399,6 @@ EncodeTiledFn encode_fn() {
 template <int BN, int EPI>
 cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool pdl) {
     using C = Cfg<BN>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(C::SMEM));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg{};
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(mt * nt);
@@ -420,6 +412,23 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool 
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI>, m.a_hi, m.a_lo, m.b_hi, m.b_lo,
                               g);
+}
+
+template <int BN, int EPI>
+cudaError_t set_smem() {
+    return cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(Cfg<BN>::SMEM));
+}
+
+template <int BN>
+cudaError_t set_smem_bn() {
+    cudaError_t e;
+    if ((e = set_smem<BN, GEPI_STORE>()) != cudaSuccess) return e;
+    if ((e = set_smem<BN, GEPI_RESIDUAL>()) != cudaSuccess) return e;
+    if ((e = set_smem<BN, GEPI_SWIGLU>()) != cudaSuccess) return e;
+    if ((e = set_smem<BN, GEPI_QKV_ROPE>()) != cudaSuccess) return e;
+    return set_smem<BN, GEPI_ARGMAX>();
 }
 
 template <int BN>
@@ -457,6 +466,13 @@ cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, 
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Raises the dynamic shared-memory limit of every GEMM instantiation on the
+// current device (call before the first launch and outside stream capture).
+cudaError_t prepare_gemm() {
+    cudaError_t e = set_smem_bn<64>();
+    return e != cudaSuccess ? e : set_smem_bn<128>();
 }
 
 int gemm_tile_n(int N) { return N >= 8192 ? 128 : 64; }
@@ -518,6 +534,7 @@ extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, in
             break;
         if ((e = launch_split_tf32(d_W, w_hi, w_lo, static_cast<long long>(nw), s)) != cudaSuccess)
             break;
+        if ((e = prepare_gemm()) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.a_hi, a_hi, K, M, 1, 128)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.a_lo, a_lo, K, M, 1, 128)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.b_hi, w_hi, K, N, 1, bn)) != cudaSuccess) break;

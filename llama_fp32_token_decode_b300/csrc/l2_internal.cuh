@@ -125,6 +125,45 @@ struct GemmArgs {
     int* err;             // ERR_* bits
 };
 
+// Batched decode (batched.cu). Row b of every [M][...] array is sequence b.
+struct BNormArgs {
+    float* x;              // [M][d] residual rows (set to emb[token] when emb != null)
+    const float* emb;      // embedding table [V][d] or null
+    const int* token;      // [M] (used when emb != null)
+    const float* gain;     // [d]
+    float* xn_hi;          // [M][d] normalised rows, tf32 pair
+    float* xn_lo;
+    int d, vocab;
+    float eps;
+};
+
+struct BAttnArgs {
+    const float* q;        // [M][d], RoPE applied
+    const float* k_cache;  // layer l of sequence 0; sequence b at + b * cache_seq
+    const float* v_cache;
+    float* att_hi;         // [M][d] output, tf32 pair
+    float* att_lo;
+    const int* pos;        // [M]
+    const int* active;     // [M] or null
+    int d, n_heads, n_kv_heads, head_dim, seq_len;
+    size_t cache_seq;
+};
+
+struct BAdvanceArgs {
+    int M;
+    int mode;                    // 0 = forward only, 1 = generate
+    int steps;                   // generate: tokens per sequence (row stride of out)
+    unsigned long long* keys;    // [M] packed argmax keys (reset to 0 here)
+    int* last;                   // [M] greedy choice of this step
+    int* pos;
+    int* token;
+    int* active;
+    const int* len;              // [M] prompt lengths
+    const int* poff;             // [M] offsets into prompts
+    const int* prompts;          // concatenated prompts
+    int* out;                    // [M][steps]
+};
+
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -263,10 +302,16 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
 // gemm_tf32x3.cu
 cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, long long rows,
                           long long layers, int box_rows);
+cudaError_t prepare_gemm();
 int gemm_tile_n(int N);
 cudaError_t launch_gemm(int epi, int bn, const GemmMaps& m, const GemmArgs& g, cudaStream_t s,
                         bool pdl);
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
+
+// batched.cu
+cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl);
+cudaError_t launch_battn(const BAttnArgs& a, int M, cudaStream_t s, bool pdl);
+cudaError_t launch_badvance(const BAdvanceArgs& a, cudaStream_t s, bool pdl);
 
 // layout.cu
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
