@@ -4,9 +4,12 @@
 One step = one greedy generation of the named workload (every forward of its
 prompt and generated positions) through the library's C ABI. Default workload:
 the 7B shape at batch 1 (64-token prompt + 256 generated tokens = 319
-forwards), the largest configuration that fits one GPU.
+forwards), the largest configuration that fits one GPU; the default line also
+carries a "batch256" object, the batched workload (256 sequences on the 44M
+shape, prompts of 1-128 tokens, 512 generated tokens each) measured the same
+way.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b|15m|44m|110m]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b|15m|44m|110m|batched]
     python bench.py --impl reference ...   # the C oracle on the host cores
     python bench.py --kernel-only 3 --layers 2   # one kernel kind on a reduced-depth
                                                  # model of the same shape (ncu case)
@@ -35,6 +38,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "decode tok/s (fp32, batch 1)"
+METRIC_BATCHED = "decode tok/s (fp32, batch 256)"
 DOMINANT_KIND = 3  # W1/W3 + SwiGLU: 44% of the streamed bytes of a 7B-shape step
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "w13_swiglu_7b_shape.md")
 KERNEL_SOURCE = os.path.join(ROOT, "llama_fp32_token_decode_b300", "csrc", "matvec.cu")
@@ -46,7 +50,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="7b", choices=["15m", "44m", "110m", "7b"])
+    ap.add_argument("--workload", default="7b", choices=["15m", "44m", "110m", "7b", "batched"])
+    ap.add_argument("--no-batched", action="store_true",
+                    help="default run: skip the batch-256 measurement added to the 7B line")
     ap.add_argument("--cpu-forwards", type=int, default=0,
                     help="oracle forwards in the CPU-baseline sample (0 = about 20 s worth)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -173,6 +179,14 @@ def measured_peaks():
         return {"hbm_gbs": 6400.0}, "fallback"
 
 
+def tf32x3_peak(peaks):
+    """Peak of the 3xTF32 GEMM in fp32-equivalent TFLOP/s: the measured bf16
+    dense peak times the nominal tf32/bf16 ratio (1.1 / 2.25 PFLOP/s), divided
+    by the three tensor passes per product."""
+    bf16 = float(peaks.get("bf16_tflops", 1800.0))
+    return bf16 * (1.1 / 2.25) / 3.0
+
+
 def profiled_traffic():
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
     or None when the summary is missing or the kernel source changed since."""
@@ -210,7 +224,7 @@ def oracle_sample(cfg, blob, prompt, n_fwd: int):
 
 def default_cpu_forwards(name: str) -> int:
     # about 10-25 s of one core per sample
-    return {"15m": 256, "44m": 120, "110m": 40, "7b": 2}[name]
+    return {"15m": 256, "44m": 120, "110m": 40, "7b": 2, "batched": 120}[name]
 
 
 # ---------------------------------------------------------------- reference arm
@@ -221,7 +235,11 @@ def run_reference(args, world, rank):
     w = synth.workload(args.workload)
     cfg = synth.model_config(w)
     blob = synth.make_blob(cfg, w["seed"])
-    prompt = synth.prompt(w)
+    if w["prompt"] == "batch":  # sequences are independent: time sequence 0
+        lens, prompts = synth.batch_inputs(w)
+        prompt = prompts[:lens[0]]
+    else:
+        prompt = synth.prompt(w)
     per_step = max(1, (args.cpu_forwards or default_cpu_forwards(args.workload)) // 2)
     for _ in range(args.warmup):
         oracle_sample(cfg, blob, prompt, 1)
@@ -229,7 +247,8 @@ def run_reference(args, world, rank):
     value = args.steps * per_step / t
     sample = (f"first {per_step} forwards (positions 0..{per_step - 1}) of the {args.workload} "
               f"workload per step, single-threaded C oracle (-O2, no fast-math)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+    line = {"impl": "reference",
+            "metric": METRIC_BATCHED if args.workload == "batched" else METRIC, "value": value, "unit": "tok/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -392,10 +411,172 @@ def run_ours(args, world, rank, local):
             "roofline": roofline, "step_roofline": step_roofline,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": launches_per_step * args.steps}
+    dec.close()
+    del dec
+    if blob is not None:
+        del blob
+    torch.cuda.empty_cache()
+    if args.workload == "7b" and not args.no_batched:
+        # the other half of the metric: batch 256 on the 44M shape, same process
+        line["batch256"] = run_ours_batched(args, world, rank, local, compact=True)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    dec.close()
     return 0
+
+
+BATCHED_KINDS = {  # batched kernel kinds of l2_time_kernel and their launches per step
+    6: "QKV GEMM (+RoPE, KV append)", 7: "attention", 8: "Wo GEMM (+residual)",
+    9: "W1/W3 GEMM (+SwiGLU)", 10: "W2 GEMM (+residual)", 11: "classifier GEMM (+argmax)",
+    12: "RMSNorm"}
+
+
+def batched_gemm_shape(cfg, kind):
+    """(N, K) of a batched GEMM kind, or None for the non-GEMM kinds."""
+    d, F, V = cfg["dim"], cfg["hidden_dim"], cfg["vocab_size"]
+    kvd = cfg["n_kv_heads"] * (d // cfg["n_heads"])
+    return {6: (d + 2 * kvd, d), 8: (d, d), 9: (2 * F, d), 10: (d, F), 11: (V, d)}.get(kind)
+
+
+def run_ours_batched(args, world, rank, local, compact=False):
+    """Batch 256 on the 44M shape: one step = one l2_generate_batch_device of
+    the whole workload (every sequence's prompt and generated positions,
+    lockstep), tokens/s = forwards of all sequences / time."""
+    import torch
+
+    import llama_fp32_token_decode_b300 as l2
+
+    torch.cuda.set_device(local)
+    w = synth.workload("batched")
+    cfg = synth.model_config(w)
+    lens, prompts = synth.batch_inputs(w)
+    B, steps, L = int(w["batch"]), int(w["steps"]), cfg["n_layers"]
+    n_fwd = int(np.sum(lens + steps - 1))           # forwards of all sequences
+    n_lock = int(lens.max()) + steps - 1            # lockstep steps
+    blob = synth.make_blob(cfg, w["seed"])
+    dec = l2.Decoder(cfg, blob)
+    stream = torch.cuda.Stream()
+    d_prompts = torch.tensor(prompts, dtype=torch.int32, device="cuda")
+    d_out = torch.zeros((B, steps), dtype=torch.int32, device="cuda")
+
+    def step():
+        l2.l2_generate_batch_device(dec.h, d_prompts, lens, steps, d_out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    ref_tokens = d_out.cpu().numpy().copy()
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world)
+    value = world * args.steps * n_fwd / (ms_max / 1e3)
+    assert np.array_equal(d_out.cpu().numpy(), ref_tokens), "batched generation is not reproducible"
+
+    # end to end: host prompts in, host tokens out
+    h_prompts = torch.tensor(prompts, dtype=torch.int32).pin_memory().numpy()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        toks = dec.generate_batch(h_prompts, lens, steps)
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    assert np.array_equal(toks, ref_tokens), "host and device batched entry points disagree"
+    e2e = {"value": world * args.steps * n_fwd / t_e2e, "unit": "tok/s",
+           "h2d_bytes_per_step": int(h_prompts.nbytes + lens.nbytes),
+           "d2h_bytes_per_step": int(B * steps * 4)}
+
+    # per-kernel times at the run's mean position, live, on the bench stream
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    p3 = tf32x3_peak(peaks)
+    pos_mid = int(np.mean(lens)) - 1 + steps // 2
+    per = {}
+    for kind, name in BATCHED_KINDS.items():
+        t = l2.l2_time_kernel(dec.h, kind, pos_mid, 3 * L, stream)
+        launches = {11: 1, 12: 2 * L + 1}.get(kind, L)
+        shp = batched_gemm_shape(cfg, kind)
+        flops = 2.0 * B * shp[0] * shp[1] if shp else 0.0
+        per[kind] = {"name": name, "launch_ms": t, "launches_per_step": launches,
+                     "ms_per_step": t * launches, "bytes": l2.l2_kernel_bytes(dec.h, kind, pos_mid),
+                     "flops": flops}
+    total_ms = sum(v["ms_per_step"] for v in per.values())
+    dom = max(per, key=lambda k: per[k]["ms_per_step"])
+    dk = per[dom]
+    if dk["flops"] > 0:
+        ach = dk["flops"] / (dk["launch_ms"] / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": ach, "peak": p3, "unit": "TFLOP/s",
+                    "frac": ach / p3, "traffic": None}
+    else:
+        ach = dk["bytes"] / (dk["launch_ms"] / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "traffic": None}
+    roofline.update({"kernel": dk["name"], "launch_ms": dk["launch_ms"],
+                     "share_of_kernel_time": dk["ms_per_step"] / total_ms,
+                     "peak_source": (f"{peak_kind} bf16_tflops x 1.1/2.25 / 3 (3xTF32)"
+                                     if dk["flops"] > 0 else f"{peak_kind} hbm_gbs (copy)")})
+    g_flops = sum(v["flops"] * v["launches_per_step"] for v in per.values())
+    g_ms = sum(v["ms_per_step"] for v in per.values() if v["flops"] > 0)
+    gemm_phase = {"achieved": g_flops / (g_ms / 1e3) / 1e12, "peak": p3, "unit": "TFLOP/s",
+                  "frac": g_flops / (g_ms / 1e3) / 1e12 / p3, "flops_per_step": g_flops,
+                  "ms_per_step": g_ms}
+    attn = per[7]
+    attn_roof = {"achieved": attn["bytes"] / (attn["launch_ms"] / 1e3) / 1e9, "peak": hbm,
+                 "unit": "GB/s", "frac": attn["bytes"] / (attn["launch_ms"] / 1e3) / 1e9 / hbm,
+                 "pos": pos_mid}
+    kernels = {v["name"]: round(v["ms_per_step"] / total_ms, 4) for v in per.values()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nf = args.cpu_forwards or 60
+        import oracle
+        m = oracle.Model(cfg, blob)
+        tok = int(prompts[0])
+        t0 = time.perf_counter()
+        for p in range(nf):
+            lg = m.forward(tok, p)
+            tok = int(prompts[p + 1]) if p + 1 < lens[0] else int(np.argmax(lg))
+        dt = time.perf_counter() - t0
+        m.close()
+        cpu = {"value": nf / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"sequence 0 of the batched workload, first {nf} forwards, "
+                         f"single-threaded C oracle (-O2, no fast-math); the oracle decodes "
+                         f"sequences one after another"}
+    dec.close()
+    line = {"metric": METRIC_BATCHED, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (random-init N(0,0.02) weights, seeded prompts and lengths)",
+            "config": {"workload": "batched", "global_batch": world * B, "dim": cfg["dim"],
+                       "n_layers": L, "n_heads": cfg["n_heads"],
+                       "hidden_dim": cfg["hidden_dim"], "vocab_size": cfg["vocab_size"],
+                       "seq_len": cfg["seq_len"], "prompt_lens": "U[1,128] seed 4",
+                       "generated_per_sequence": steps, "forwards_per_step": n_fwd,
+                       "lockstep_steps": n_lock, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (KV caches %.1f GB)" % (
+                           B * 2 * L * cfg["seq_len"] * cfg["dim"] * 4 / 1e9)},
+            "roofline": roofline, "gemm_phase_roofline": gemm_phase,
+            "attention_roofline": attn_roof, "kernel_time_shares": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps * (1 + n_lock * (2 + 7 * L + 1))}
+    if compact:
+        for k in ("steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data",
+                  "n_gpus"):
+            line.pop(k, None)
+    return line
 
 
 def run_kernel_only(args):
@@ -429,8 +610,15 @@ def main():
     world, rank, local = dist_setup(args)
     if args.gpus != world and world > 1:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
-    rc = run_reference(args, world, rank) if args.impl == "reference" else \
-        run_ours(args, world, rank, local)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    elif args.workload == "batched":
+        line = run_ours_batched(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        rc = 0
+    else:
+        rc = run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -146,6 +146,14 @@ L2_API int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_p
 L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
                       int32_t steps, int32_t* out_tokens);
 
+/* l2_generate_batch with the prompts and the output in device memory:
+ * d_prompts int32 [sum of lens], d_out int32 [B][steps]; `lens` stays a HOST
+ * array [B] (the lockstep schedule is planned on the host). Queued on
+ * `stream`, returns without waiting. Host-side checks as l2_generate_batch;
+ * device prompt ids are not range-checked (clamped to [0, V)). */
+L2_API int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
+                                    int32_t B, int32_t steps, int32_t* d_out, void* stream);
+
 /* Clears KV cache `seq` (-1: all caches) to zero. Errors: L2_EINVAL. */
 L2_API int l2_reset(l2_handle* h, int32_t seq);
 
@@ -158,16 +166,20 @@ L2_API const char* l2_last_error(const l2_handle* h);
 
 /* Measurement hook: launches one kernel kind of the step `iters` times on
  * `stream`, cycling over layers, bracketed by CUDA events, and writes the mean
- * duration of one launch in milliseconds to *ms. kind: 0 QKV+RoPE,
+ * duration of one launch in milliseconds to *ms. Batch-1 kinds: 0 QKV+RoPE,
  * 1 attention, 2 Wo+residual, 3 W1/W3+SwiGLU, 4 W2+residual,
- * 5 classifier+argmax. It reads and writes the handle's own run state (the
- * KV cache contents are left as they were, except slot `pos` of cache 0).
+ * 5 classifier+argmax. Batched kinds (handles with max_batch > 1; all
+ * max_batch rows at position pos): 6 QKV GEMM, 7 attention, 8 Wo GEMM,
+ * 9 W1/W3 GEMM, 10 W2 GEMM, 11 classifier GEMM + argmax, 12 RMSNorm,
+ * 13 advance. It reads and writes the handle's own run state (the KV cache
+ * contents are left as they were, except slot `pos` of the caches used).
  * Errors: L2_EINVAL, L2_ECUDA. Synchronous. */
 L2_API int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
                    float* ms);
 
 /* Algorithmic bytes one launch of `kind` reads and writes at position pos
- * (weights + activations + KV rows), batch 1. 0 for an invalid kind. */
+ * (fp32 weights once + activations + KV rows; batched kinds count max_batch
+ * rows). 0 for an invalid kind. */
 L2_API double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos);
 
 /* Test and measurement hook of the batched path's tensor-core GEMM:

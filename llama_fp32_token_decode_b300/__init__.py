@@ -24,10 +24,11 @@ ERROR_NAMES = {L2_EINVAL: "L2_EINVAL", L2_ENOMEM: "L2_ENOMEM", L2_ECUDA: "L2_ECU
 
 # kinds of l2_time_kernel / l2_kernel_bytes
 KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residual",
-                "classifier_argmax")
+                "classifier_argmax", "b_qkv_gemm", "b_attention", "b_wo_gemm", "b_w13_gemm",
+                "b_w2_gemm", "b_classifier_gemm", "b_rmsnorm", "b_advance")
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
-           "l2_generate_device", "l2_generate_batch", "l2_reset", "l2_destroy",
+           "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
            "l2_gemm_tf32x3")
 
@@ -66,6 +67,7 @@ _SIG = {
     "l2_generate": (ctypes.c_int, [_P, _P, _I, _I, _P]),
     "l2_generate_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_generate_batch": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
+    "l2_generate_batch_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
     "l2_reset": (ctypes.c_int, [_P, _I]),
     "l2_destroy": (None, [_P]),
     "l2_last_error": (ctypes.c_char_p, [_P]),
@@ -171,6 +173,13 @@ def l2_generate_batch(h, prompts, lens, steps: int) -> np.ndarray:
     _check(_lib.l2_generate_batch(h, prompts.ctypes.data, lens.ctypes.data, lens.size, steps,
                                   out.ctypes.data), h)
     return out
+
+
+def l2_generate_batch_device(h, d_prompts, lens, steps: int, d_out, stream=None) -> None:
+    """d_prompts, d_out: device buffers; lens: host lengths."""
+    lens = _i32(lens).ravel()
+    _check(_lib.l2_generate_batch_device(h, _ptr(d_prompts), lens.ctypes.data, lens.size, steps,
+                                         _ptr(d_out), _stream(stream)), h)
 
 
 def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:

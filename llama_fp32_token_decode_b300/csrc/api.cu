@@ -252,118 +252,136 @@ int check_device_error(l2_handle* h) {
 
 // ---------------------------------------------------------------- batched path
 
+// Kernel kinds of a batched step (l2_time_kernel numbers them 6 + kind).
+enum BKind : int {
+    BK_QKV = 0, BK_ATTN = 1, BK_WO = 2, BK_W13 = 3, BK_W2 = 4, BK_CLS = 5,
+    BK_NORM = 6,      // RMSNorm of the residual rows with gain `gain_sel`
+    BK_ADVANCE = 7,
+    BK_NORM_EMB = 8,  // embedding gather + RMSNorm (step start)
+};
+
+// Launches one kernel of a batched step for layer l on M rows. For BK_NORM the
+// gain is g_ffn[l] (gain_next == false) or the next layer's g_att / g_final.
+cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int steps,
+                         bool want_logits, bool gain_next, cudaStream_t s) {
+    const l2_config& c = h->cfg;
+    const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
+    GemmArgs g{};
+    g.M = M;
+    g.err = &h->st->err;
+    g.layer = l;
+    switch (kind) {
+        case BK_NORM_EMB:
+        case BK_NORM: {
+            BNormArgs n{};
+            n.x = h->bx;
+            n.emb = kind == BK_NORM_EMB ? h->emb : nullptr;
+            n.token = h->b_token;
+            n.gain = kind == BK_NORM_EMB ? h->g_att
+                     : !gain_next        ? h->g_ffn + static_cast<size_t>(l) * d
+                     : (l + 1 < L)       ? h->g_att + static_cast<size_t>(l + 1) * d
+                                         : h->g_final;
+            n.xn_hi = h->xn_hi;
+            n.xn_lo = h->xn_lo;
+            n.d = d;
+            n.vocab = V;
+            n.eps = c.norm_eps;
+            return launch_brmsnorm(n, M, s, true);
+        }
+        case BK_QKV:
+            g.N = d + 2 * h->kvd;
+            g.K = d;
+            g.q = h->bq;
+            g.k_cache = h->k_cache + l * h->cache_layer;
+            g.v_cache = h->v_cache + l * h->cache_layer;
+            g.rope = h->rope;
+            g.pos = h->b_pos;
+            g.active = h->b_active;
+            g.d = d;
+            g.kvd = h->kvd;
+            g.head_dim = h->hd;
+            g.seq_len = c.seq_len;
+            g.cache_seq = h->cache_seq;
+            return launch_gemm(GEPI_QKV_ROPE, h->bn_qkv, h->m_qkv, g, s, true);
+        case BK_ATTN: {
+            BAttnArgs t{};
+            t.q = h->bq;
+            t.k_cache = h->k_cache + l * h->cache_layer;
+            t.v_cache = h->v_cache + l * h->cache_layer;
+            t.att_hi = h->att_hi;
+            t.att_lo = h->att_lo;
+            t.pos = h->b_pos;
+            t.active = h->b_active;
+            t.d = d;
+            t.n_heads = c.n_heads;
+            t.n_kv_heads = c.n_kv_heads;
+            t.head_dim = h->hd;
+            t.seq_len = c.seq_len;
+            t.cache_seq = h->cache_seq;
+            return launch_battn(t, M, s, true);
+        }
+        case BK_WO:
+            g.N = d;
+            g.K = d;
+            g.out = h->bx;
+            g.ldc = d;
+            return launch_gemm(GEPI_RESIDUAL, h->bn_wo, h->m_wo, g, s, true);
+        case BK_W13:
+            g.N = 2 * F;
+            g.K = d;
+            g.out_hi = h->hb_hi;
+            g.out_lo = h->hb_lo;
+            return launch_gemm(GEPI_SWIGLU, h->bn_w13, h->m_w13, g, s, true);
+        case BK_W2:
+            g.N = d;
+            g.K = F;
+            g.out = h->bx;
+            g.ldc = d;
+            return launch_gemm(GEPI_RESIDUAL, h->bn_w2, h->m_w2, g, s, true);
+        case BK_CLS:
+            g.layer = 0;
+            g.N = V;
+            g.K = d;
+            g.out = want_logits ? h->blogits : nullptr;
+            g.ldc = V;
+            g.argmax_keys = h->b_keys;
+            return launch_gemm(GEPI_ARGMAX, h->bn_cls, h->m_cls, g, s, true);
+        case BK_ADVANCE: {
+            BAdvanceArgs a{};
+            a.M = M;
+            a.mode = mode;
+            a.steps = steps;
+            a.keys = h->b_keys;
+            a.last = h->b_last;
+            a.pos = h->b_pos;
+            a.token = h->b_token;
+            a.active = h->b_active;
+            a.len = h->b_len;
+            a.poff = h->b_poff;
+            a.prompts = h->b_prompts;
+            a.out = h->b_out;
+            return launch_badvance(a, s, true);
+        }
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
 // One lockstep step of M sequences: embedding + RMSNorm, then per layer the
 // QKV GEMM (RoPE + KV append), attention, Wo GEMM + residual, RMSNorm, W1/W3
 // GEMM + SwiGLU, W2 GEMM + residual, RMSNorm; the classifier GEMM with the
 // per-row argmax; and the per-sequence advance.
 cudaError_t enqueue_bstep(l2_handle* h, int M, int mode, int steps, bool want_logits,
                           cudaStream_t s) {
-    const l2_config& c = h->cfg;
-    const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
-    cudaError_t e;
-    BNormArgs n{};
-    n.x = h->bx;
-    n.emb = h->emb;
-    n.token = h->b_token;
-    n.gain = h->g_att;
-    n.xn_hi = h->xn_hi;
-    n.xn_lo = h->xn_lo;
-    n.d = d;
-    n.vocab = V;
-    n.eps = c.norm_eps;
-    if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
-    n.emb = nullptr;
-
-    GemmArgs g0{};
-    g0.M = M;
-    g0.err = &h->st->err;
-    g0.d = d;
-    g0.kvd = h->kvd;
-    g0.head_dim = h->hd;
-    g0.seq_len = c.seq_len;
-    g0.cache_seq = h->cache_seq;
-    g0.rope = h->rope;
-    g0.pos = h->b_pos;
-    g0.active = h->b_active;
-    for (int l = 0; l < L; ++l) {
-        GemmArgs g = g0;
-        g.layer = l;
-        g.N = d + 2 * h->kvd;
-        g.K = d;
-        g.q = h->bq;
-        g.k_cache = h->k_cache + l * h->cache_layer;
-        g.v_cache = h->v_cache + l * h->cache_layer;
-        if ((e = launch_gemm(GEPI_QKV_ROPE, h->bn_qkv, h->m_qkv, g, s, true)) != cudaSuccess) return e;
-
-        BAttnArgs t{};
-        t.q = h->bq;
-        t.k_cache = h->k_cache + l * h->cache_layer;
-        t.v_cache = h->v_cache + l * h->cache_layer;
-        t.att_hi = h->att_hi;
-        t.att_lo = h->att_lo;
-        t.pos = h->b_pos;
-        t.active = h->b_active;
-        t.d = d;
-        t.n_heads = c.n_heads;
-        t.n_kv_heads = c.n_kv_heads;
-        t.head_dim = h->hd;
-        t.seq_len = c.seq_len;
-        t.cache_seq = h->cache_seq;
-        if ((e = launch_battn(t, M, s, true)) != cudaSuccess) return e;
-
-        g = g0;
-        g.layer = l;
-        g.N = d;
-        g.K = d;
-        g.out = h->bx;
-        g.ldc = d;
-        if ((e = launch_gemm(GEPI_RESIDUAL, h->bn_wo, h->m_wo, g, s, true)) != cudaSuccess) return e;
-
-        n.gain = h->g_ffn + static_cast<size_t>(l) * d;
-        if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
-
-        g = g0;
-        g.layer = l;
-        g.N = 2 * F;
-        g.K = d;
-        g.out_hi = h->hb_hi;
-        g.out_lo = h->hb_lo;
-        if ((e = launch_gemm(GEPI_SWIGLU, h->bn_w13, h->m_w13, g, s, true)) != cudaSuccess) return e;
-
-        g = g0;
-        g.layer = l;
-        g.N = d;
-        g.K = F;
-        g.out = h->bx;
-        g.ldc = d;
-        if ((e = launch_gemm(GEPI_RESIDUAL, h->bn_w2, h->m_w2, g, s, true)) != cudaSuccess) return e;
-
-        n.gain = (l + 1 < L) ? h->g_att + static_cast<size_t>(l + 1) * d : h->g_final;
-        if ((e = launch_brmsnorm(n, M, s, true)) != cudaSuccess) return e;
+    cudaError_t e = launch_bkind(h, BK_NORM_EMB, 0, M, mode, steps, want_logits, false, s);
+    for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
+        const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_NORM, BK_W13, BK_W2, BK_NORM};
+        for (int i = 0; i < 7 && e == cudaSuccess; ++i)
+            e = launch_bkind(h, seq[i], l, M, mode, steps, want_logits, i == 6, s);
     }
-    GemmArgs g = g0;
-    g.layer = 0;
-    g.N = V;
-    g.K = d;
-    g.out = want_logits ? h->blogits : nullptr;
-    g.ldc = V;
-    g.argmax_keys = h->b_keys;
-    if ((e = launch_gemm(GEPI_ARGMAX, h->bn_cls, h->m_cls, g, s, true)) != cudaSuccess) return e;
-
-    BAdvanceArgs a{};
-    a.M = M;
-    a.mode = mode;
-    a.steps = steps;
-    a.keys = h->b_keys;
-    a.last = h->b_last;
-    a.pos = h->b_pos;
-    a.token = h->b_token;
-    a.active = h->b_active;
-    a.len = h->b_len;
-    a.poff = h->b_poff;
-    a.prompts = h->b_prompts;
-    a.out = h->b_out;
-    return launch_badvance(a, s, true);
+    if (e == cudaSuccess) e = launch_bkind(h, BK_CLS, 0, M, mode, steps, want_logits, false, s);
+    if (e == cudaSuccess) e = launch_bkind(h, BK_ADVANCE, 0, M, mode, steps, want_logits, false, s);
+    return e;
 }
 
 // Rows [0, M): active, keys cleared; for generation, pos 0 and the first prompt token.
@@ -379,6 +397,18 @@ __global__ void binit_kernel(int M, int mode, int* pos, int* token, int* active,
         pos[b] = 0;
         token[b] = prompts[poff[b]];
     }
+}
+
+// Timing set-up: rows [0, M) active at position pos with token 1.
+__global__ void bset_kernel(int M, int pos, int* b_pos, int* token, int* active,
+                            unsigned long long* keys, L2State* st) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b == 0) st->err = 0;
+    if (b >= M) return;
+    b_pos[b] = pos;
+    token[b] = 1;
+    active[b] = 1;
+    keys[b] = 0ull;
 }
 
 // Allocates the batched path's buffers, splits the laid-out weights into tf32
@@ -880,8 +910,9 @@ int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t s
     return check_device_error(h);
 }
 
-int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
-                      int32_t steps, int32_t* out_tokens) {
+static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32_t* lens,
+                               int32_t B, int32_t steps, int32_t* out_tokens, bool on_device,
+                               cudaStream_t stream) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!prompts || !lens || !out_tokens) return fail(h, L2_EINVAL, "NULL prompts, lens or output");
     if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
@@ -897,12 +928,15 @@ int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens,
         total += lens[b];
         max_len = lens[b] > max_len ? lens[b] : max_len;
     }
-    for (long long i = 0; i < total; ++i)
-        if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
-    if (h->cfg.max_batch == 1) return l2_generate(h, prompts, lens[0], steps, out_tokens);
-    cudaStream_t s = h->stream;
+    if (!on_device)
+        for (long long i = 0; i < total; ++i)
+            if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    if (h->cfg.max_batch == 1)
+        return on_device ? l2_generate_device(h, prompts, lens[0], steps, out_tokens, stream)
+                         : l2_generate(h, prompts, lens[0], steps, out_tokens);
+    cudaStream_t s = on_device ? stream : h->stream;
     L2_CUDA(h, cudaMemcpyAsync(h->b_prompts, prompts, sizeof(int32_t) * total,
-                               cudaMemcpyHostToDevice, s));
+                               on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
     L2_CUDA(h, cudaMemcpyAsync(h->b_len, lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
     L2_CUDA(h, cudaMemcpyAsync(h->b_poff, poff.data(), sizeof(int32_t) * B, cudaMemcpyHostToDevice,
                                s));
@@ -915,17 +949,47 @@ int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens,
     const int n = max_len + steps - 1;
     for (int i = 0; i < n; ++i) L2_CUDA(h, cudaGraphLaunch(h->bgraph, s));
     L2_CUDA(h, cudaMemcpyAsync(out_tokens, h->b_out, sizeof(int32_t) * B * static_cast<size_t>(steps),
-                               cudaMemcpyDeviceToHost, s));
+                               on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
+    if (on_device) return L2_OK;
     L2_CUDA(h, cudaStreamSynchronize(s));
     return check_device_error(h);
+}
+
+int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
+                      int32_t steps, int32_t* out_tokens) {
+    return generate_batch_impl(h, prompts, lens, B, steps, out_tokens, false, nullptr);
+}
+
+int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
+                             int32_t B, int32_t steps, int32_t* d_out, void* stream) {
+    return generate_batch_impl(h, d_prompts, lens, B, steps, d_out, true,
+                               static_cast<cudaStream_t>(stream));
 }
 
 int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
                    float* ms) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
-    if (kind < 0 || kind > 5 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
+    if (kind < 0 || kind > 13 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
         return fail(h, L2_EINVAL, "bad kind, iters, pos or output");
+    if (kind >= 6 && h->cfg.max_batch < 2)
+        return fail(h, L2_EINVAL, "batched kernel kinds need a handle with max_batch > 1");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kind >= 6) {
+        const int M = h->cfg.max_batch, bk = kind - 6;
+        bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
+                                                    h->b_keys, h->st);
+        L2_CUDA(h, cudaGetLastError());
+        L2_CUDA(h, launch_bkind(h, bk, 0, M, 0, 0, false, false, s));
+        L2_CUDA(h, cudaEventRecord(h->ev0, s));
+        for (int i = 0; i < iters; ++i)
+            L2_CUDA(h, launch_bkind(h, bk, i % h->cfg.n_layers, M, 0, 0, false, false, s));
+        L2_CUDA(h, cudaEventRecord(h->ev1, s));
+        L2_CUDA(h, cudaEventSynchronize(h->ev1));
+        float t = 0.0f;
+        L2_CUDA(h, cudaEventElapsedTime(&t, h->ev0, h->ev1));
+        *ms = t / iters;
+        return check_device_error(h);
+    }
     init_state_kernel<<<1, 1, 0, s>>>(h->st, pos, 1, nullptr, nullptr, h->cfg.vocab_size,
                                       h->cfg.seq_len, 0, 0, nullptr, nullptr, 1);
     L2_CUDA(h, cudaGetLastError());
@@ -951,6 +1015,20 @@ double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
         case 3: return 4.0 * (2 * F * d + 2 * d + F);
         case 4: return 4.0 * (d * F + F + 2 * d);
         case 5: return 4.0 * (V * d + 2 * d + V);
+        default: break;
+    }
+    // batched kinds: fp32 operands once (weights, input rows), outputs, KV rows
+    const double M = h->cfg.max_batch;
+    if (kind >= 6 && M < 2) return 0.0;
+    switch (kind) {
+        case 6: return 4.0 * ((d + 2 * kvd) * d + M * d + M * (d + 2 * kvd));
+        case 7: return 4.0 * M * (2.0 * (pos + 1) * kvd + 2 * d);
+        case 8: return 4.0 * (d * d + M * d + 2 * M * d);
+        case 9: return 4.0 * (2 * F * d + M * d + M * F);
+        case 10: return 4.0 * (d * F + M * F + 2 * M * d);
+        case 11: return 4.0 * (V * d + M * d);
+        case 12: return 4.0 * (2 * M * d + d);
+        case 13: return 4.0 * 6 * M;
         default: return 0.0;
     }
 }
