@@ -58,7 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", type=int, default=None,
                     help="time one kernel kind (0 QKV, 1 attention, 2 Wo, 3 W1/W3, 4 W2, "
-                         "5 classifier) on the workload's shape and exit: the profiling case")
+                         "5 classifier; 6-13 the batched kinds with --workload batched) on "
+                         "the workload's shape and exit: the profiling case")
     ap.add_argument("--layers", type=int, default=0,
                     help="with --kernel-only: layers of the reduced-depth model (0 = all)")
     return ap.parse_args()
@@ -591,7 +592,8 @@ def run_kernel_only(args):
     cfg = synth.model_config(w)
     if args.layers:
         cfg["n_layers"] = args.layers
-    cfg["seq_len"] = min(cfg["seq_len"], 512)
+    # a short cache keeps the case to a few GB (batched: 256 caches)
+    cfg["seq_len"] = min(cfg["seq_len"], 384 if cfg.get("max_batch", 1) > 1 else 512)
     blob = synth.make_blob(cfg, w["seed"])
     with l2.Decoder(cfg, blob) as dec:
         pos = min(300, cfg["seq_len"] - 1)

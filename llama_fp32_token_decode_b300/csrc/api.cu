@@ -61,7 +61,7 @@ struct l2_handle {
     int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
     unsigned long long* b_keys = nullptr;
     GemmMaps m_qkv{}, m_wo{}, m_w13{}, m_w2{}, m_cls{};
-    int bn_qkv = 64, bn_wo = 64, bn_w13 = 64, bn_w2 = 64, bn_cls = 128;
+    GemmPlan gp_qkv{64, 1}, gp_wo{64, 1}, gp_w13{64, 1}, gp_w2{64, 1}, gp_cls{128, 1};
     cudaGraphExec_t bgraph = nullptr;  // one batched generation step
     int bgraph_M = 0, bgraph_steps = 0;
 
@@ -270,6 +270,10 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
     g.M = M;
     g.err = &h->st->err;
     g.layer = l;
+    // tile width fixed at create (it is the weight maps' box); K split for this M
+    auto plan = [&](const GemmPlan& p, int N, int K) {
+        return GemmPlan{p.bn, plan_split(p.bn, M, N, K, h->num_sms)};
+    };
     switch (kind) {
         case BK_NORM_EMB:
         case BK_NORM: {
@@ -302,7 +306,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
             g.head_dim = h->hd;
             g.seq_len = c.seq_len;
             g.cache_seq = h->cache_seq;
-            return launch_gemm(GEPI_QKV_ROPE, h->bn_qkv, h->m_qkv, g, s, true);
+            return launch_gemm(GEPI_QKV_ROPE, plan(h->gp_qkv, g.N, g.K), h->m_qkv, g, s, true);
         case BK_ATTN: {
             BAttnArgs t{};
             t.q = h->bq;
@@ -325,19 +329,19 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
             g.K = d;
             g.out = h->bx;
             g.ldc = d;
-            return launch_gemm(GEPI_RESIDUAL, h->bn_wo, h->m_wo, g, s, true);
+            return launch_gemm(GEPI_RESIDUAL, plan(h->gp_wo, g.N, g.K), h->m_wo, g, s, true);
         case BK_W13:
             g.N = 2 * F;
             g.K = d;
             g.out_hi = h->hb_hi;
             g.out_lo = h->hb_lo;
-            return launch_gemm(GEPI_SWIGLU, h->bn_w13, h->m_w13, g, s, true);
+            return launch_gemm(GEPI_SWIGLU, plan(h->gp_w13, g.N, g.K), h->m_w13, g, s, true);
         case BK_W2:
             g.N = d;
             g.K = F;
             g.out = h->bx;
             g.ldc = d;
-            return launch_gemm(GEPI_RESIDUAL, h->bn_w2, h->m_w2, g, s, true);
+            return launch_gemm(GEPI_RESIDUAL, plan(h->gp_w2, g.N, g.K), h->m_w2, g, s, true);
         case BK_CLS:
             g.layer = 0;
             g.N = V;
@@ -345,7 +349,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
             g.out = want_logits ? h->blogits : nullptr;
             g.ldc = V;
             g.argmax_keys = h->b_keys;
-            return launch_gemm(GEPI_ARGMAX, h->bn_cls, h->m_cls, g, s, true);
+            return launch_gemm(GEPI_ARGMAX, plan(h->gp_cls, g.N, g.K), h->m_cls, g, s, true);
         case BK_ADVANCE: {
             BAdvanceArgs a{};
             a.M = M;
@@ -465,27 +469,28 @@ int setup_batched(l2_handle* h) {
     h->b_prompts = h->bst + o_pr; h->b_out = h->bst + o_out;
     h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
 
-    h->bn_qkv = gemm_tile_n(static_cast<int>(d + 2 * kvd));
-    h->bn_wo = gemm_tile_n(static_cast<int>(d));
-    h->bn_w13 = gemm_tile_n(static_cast<int>(2 * F));
-    h->bn_w2 = gemm_tile_n(static_cast<int>(d));
-    h->bn_cls = gemm_tile_n(static_cast<int>(V));
+    const int Mb = static_cast<int>(B), sms = h->num_sms;
+    h->gp_qkv = plan_gemm(Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d), sms);
+    h->gp_wo = plan_gemm(Mb, static_cast<int>(d), static_cast<int>(d), sms);
+    h->gp_w13 = plan_gemm(Mb, static_cast<int>(2 * F), static_cast<int>(d), sms);
+    h->gp_w2 = plan_gemm(Mb, static_cast<int>(d), static_cast<int>(F), sms);
+    h->gp_cls = plan_gemm(Mb, static_cast<int>(V), static_cast<int>(d), sms);
     const long long D = d, FF = F, LL = L, MC = Mc;
     struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
     const MapSpec specs[] = {
         {&h->m_qkv.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_qkv.a_lo, h->xn_lo, D, MC, 1, 128},
-        {&h->m_qkv.b_hi, h->qkv_hi, D, D + 2 * static_cast<long long>(kvd), LL, h->bn_qkv},
-        {&h->m_qkv.b_lo, h->qkv_lo, D, D + 2 * static_cast<long long>(kvd), LL, h->bn_qkv},
+        {&h->m_qkv.b_hi, h->qkv_hi, D, D + 2 * static_cast<long long>(kvd), LL, h->gp_qkv.bn},
+        {&h->m_qkv.b_lo, h->qkv_lo, D, D + 2 * static_cast<long long>(kvd), LL, h->gp_qkv.bn},
         {&h->m_wo.a_hi, h->att_hi, D, MC, 1, 128}, {&h->m_wo.a_lo, h->att_lo, D, MC, 1, 128},
-        {&h->m_wo.b_hi, h->wo_hi, D, D, LL, h->bn_wo}, {&h->m_wo.b_lo, h->wo_lo, D, D, LL, h->bn_wo},
+        {&h->m_wo.b_hi, h->wo_hi, D, D, LL, h->gp_wo.bn}, {&h->m_wo.b_lo, h->wo_lo, D, D, LL, h->gp_wo.bn},
         {&h->m_w13.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_w13.a_lo, h->xn_lo, D, MC, 1, 128},
-        {&h->m_w13.b_hi, h->w13_hi, D, 2 * FF, LL, h->bn_w13},
-        {&h->m_w13.b_lo, h->w13_lo, D, 2 * FF, LL, h->bn_w13},
+        {&h->m_w13.b_hi, h->w13_hi, D, 2 * FF, LL, h->gp_w13.bn},
+        {&h->m_w13.b_lo, h->w13_lo, D, 2 * FF, LL, h->gp_w13.bn},
         {&h->m_w2.a_hi, h->hb_hi, FF, MC, 1, 128}, {&h->m_w2.a_lo, h->hb_lo, FF, MC, 1, 128},
-        {&h->m_w2.b_hi, h->w2_hi, FF, D, LL, h->bn_w2}, {&h->m_w2.b_lo, h->w2_lo, FF, D, LL, h->bn_w2},
+        {&h->m_w2.b_hi, h->w2_hi, FF, D, LL, h->gp_w2.bn}, {&h->m_w2.b_lo, h->w2_lo, FF, D, LL, h->gp_w2.bn},
         {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, 128},
-        {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->bn_cls},
-        {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->bn_cls},
+        {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->gp_cls.bn},
+        {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->gp_cls.bn},
     };
     for (const MapSpec& m : specs) {
         cudaError_t e = make_gemm_map(m.m, m.p, m.inner, m.rows, m.layers, m.box);

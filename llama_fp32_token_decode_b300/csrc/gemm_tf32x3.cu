@@ -139,6 +139,120 @@ struct Cfg {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// ---- cluster helpers (split-K reduction through distributed shared memory)
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_peer_i32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Fused epilogue of four consecutive output columns gc..gc+3 (gc % 4 == 0) of
+// row r. pos / active: the row's position and state (QKV only). ARGMAX folds
+// the columns into `best`; the caller publishes it.
+template <int EPI>
+__device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const float (&a)[4], int pos,
+                                     int active, unsigned long long& best) {
+    if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
+        float* o = g.out + static_cast<size_t>(r) * g.ldc + gc;
+        if (gc + 4 <= g.N && (g.ldc & 3) == 0) {
+            float4 w = make_float4(a[0], a[1], a[2], a[3]);
+            if constexpr (EPI == GEPI_RESIDUAL) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
+                w.x += x.x;
+                w.y += x.y;
+                w.z += x.z;
+                w.w += x.w;
+            }
+            *reinterpret_cast<float4*>(o) = w;
+        } else {
+            for (int j = 0; j < 4 && gc + j < g.N; ++j)
+                o[j] = (EPI == GEPI_RESIDUAL) ? __ldcg(o + j) + a[j] : a[j];
+        }
+    } else if constexpr (EPI == GEPI_SWIGLU) {
+        // interleaved rows: column 2j is the gate, 2j+1 the up projection
+        const size_t F = static_cast<size_t>(g.N) >> 1;
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            if (gc + j + 1 < g.N) {
+                const float h = silu(a[j]) * a[j + 1];
+                const float hi = tf32_round(h);
+                const size_t idx = static_cast<size_t>(r) * F + ((gc + j) >> 1);
+                g.out_hi[idx] = hi;
+                g.out_lo[idx] = h - hi;
+            }
+        }
+    } else if constexpr (EPI == GEPI_QKV_ROPE) {
+        if (!active) return;
+        const int hd = g.head_dim;
+        const float2* rope = g.rope + static_cast<size_t>(pos) * (hd >> 1);
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const int c = gc + j;
+            if (c + 1 >= g.N) break;
+            const float x0 = a[j], x1 = a[j + 1];
+            if (c < g.d) {
+                const float2 cs = rope[(c % hd) >> 1];
+                float* q = g.q + static_cast<size_t>(r) * g.d + c;
+                q[0] = x0 * cs.x - x1 * cs.y;
+                q[1] = x0 * cs.y + x1 * cs.x;
+            } else if (c < g.d + g.kvd) {
+                const int jj = c - g.d, kvh = jj / hd, e = jj % hd;
+                const float2 cs = rope[e >> 1];
+                float* dst = g.k_cache + static_cast<size_t>(r) * g.cache_seq +
+                             (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                dst[0] = x0 * cs.x - x1 * cs.y;
+                dst[1] = x0 * cs.y + x1 * cs.x;
+            } else {
+                const int jj = c - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
+                float* dst = g.v_cache + static_cast<size_t>(r) * g.cache_seq +
+                             (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                dst[0] = x0;
+                dst[1] = x1;
+            }
+        }
+    } else if constexpr (EPI == GEPI_ARGMAX) {
+        float* o = g.out ? g.out + static_cast<size_t>(r) * g.ldc + gc : nullptr;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (gc + j < g.N) {
+                if (o) o[j] = a[j];
+                const unsigned long long k = argmax_key(a[j], gc + j);
+                best = k > best ? k : best;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void row_state(const GemmArgs& g, int r, int& pos, int& active) {
+    pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
+    active = g.active ? __ldcg(g.active + r) : 1;
+}
+
+// Grid (S, tiles): blockIdx.x is the K split (the CTA's rank in a cluster of S
+// CTAs that share one 128 x BN output tile), blockIdx.y the tile (M tiles of
+// one N tile adjacent). S == 1: the epilogue reads the accumulator straight
+// from TMEM (thread = row). S > 1: every CTA stages its partial tile in its own
+// shared memory; after a cluster barrier CTA s adds rows
+// [128 s / S, 128 (s+1) / S) of all S partials in rank order (a fixed order:
+// the result does not depend on timing) and applies the epilogue to them.
 template <int BN, int EPI>
 __global__ void __launch_bounds__(128, 1)
     gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mA_hi,
@@ -147,6 +261,7 @@ __global__ void __launch_bounds__(128, 1)
                        const __grid_constant__ CUtensorMap mB_lo, const GemmArgs g) {
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
+    constexpr int PS = BN + 4;  // row stride of the staged partial (floats)
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -158,10 +273,13 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ int s_err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsplit = gridDim.x, split = blockIdx.x;
     const int mt = (g.M + 127) / 128;
-    const int m0 = (blockIdx.x % mt) * 128;
-    const int n0 = (blockIdx.x / mt) * BN;
+    const int m0 = (blockIdx.y % mt) * 128;
+    const int n0 = (blockIdx.y / mt) * BN;
     const int KB = (g.K + 31) / 32;
+    const int kb0 = KB * split / nsplit, kb1 = KB * (split + 1) / nsplit;
+    const int NK = kb1 - kb0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -192,31 +310,33 @@ __global__ void __launch_bounds__(128, 1)
     auto b_lo = [&](int s) { return b_hi(s) + C::B_BYTES; };
 
     if (warp == 0 && lane == 0) {
-        // ---- producer
-        const int pre = KB < S ? KB : S;
-        for (int kb = 0; kb < pre; ++kb) {
-            mbar_arrive_expect_tx(&full[kb], C::STAGE);
-            tma_load_3d(b_hi(kb), &mB_hi, kb * 32, n0, g.layer, &full[kb]);
-            tma_load_3d(b_lo(kb), &mB_lo, kb * 32, n0, g.layer, &full[kb]);
+        // ---- producer: local K-block i is global K-block kb0 + i
+        const int pre = NK < S ? NK : S;
+        for (int i = 0; i < pre; ++i) {
+            const int kc = (kb0 + i) * 32;
+            mbar_arrive_expect_tx(&full[i], C::STAGE);
+            tma_load_3d(b_hi(i), &mB_hi, kc, n0, g.layer, &full[i]);
+            tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
         }
         pdl_wait();  // activations come from the previous kernel
-        for (int kb = 0; kb < pre; ++kb) {
-            tma_load_3d(a_hi(kb), &mA_hi, kb * 32, m0, 0, &full[kb]);
-            tma_load_3d(a_lo(kb), &mA_lo, kb * 32, m0, 0, &full[kb]);
+        for (int i = 0; i < pre; ++i) {
+            const int kc = (kb0 + i) * 32;
+            tma_load_3d(a_hi(i), &mA_hi, kc, m0, 0, &full[i]);
+            tma_load_3d(a_lo(i), &mA_lo, kc, m0, 0, &full[i]);
         }
         int issued = pre;
-        for (int kb = pre; kb < KB; ++kb) {
-            const int s = kb % S;
-            if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(kb / S - 1) & 1u)) {
+        for (int i = pre; i < NK; ++i) {
+            const int s = i % S, kc = (kb0 + i) * 32;
+            if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / S - 1) & 1u)) {
                 s_err = 1;
                 break;
             }
             mbar_arrive_expect_tx(&full[s], C::STAGE);
-            tma_load_3d(b_hi(s), &mB_hi, kb * 32, n0, g.layer, &full[s]);
-            tma_load_3d(b_lo(s), &mB_lo, kb * 32, n0, g.layer, &full[s]);
-            tma_load_3d(a_hi(s), &mA_hi, kb * 32, m0, 0, &full[s]);
-            tma_load_3d(a_lo(s), &mA_lo, kb * 32, m0, 0, &full[s]);
-            issued = kb + 1;
+            tma_load_3d(b_hi(s), &mB_hi, kc, n0, g.layer, &full[s]);
+            tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
+            tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
+            tma_load_3d(a_lo(s), &mA_lo, kc, m0, 0, &full[s]);
+            issued = i + 1;
         }
         if (s_err) {  // let the copies in flight land before the CTA leaves
             for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
@@ -225,9 +345,9 @@ __global__ void __launch_bounds__(128, 1)
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         constexpr uint32_t idesc = idesc_tf32(128, BN);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % S;
-            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(kb / S) & 1u)) {
+        for (int i = 0; i < NK; ++i) {
+            const int s = i % S;
+            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
                 s_err = 1;
                 break;
             }
@@ -238,7 +358,7 @@ __global__ void __launch_bounds__(128, 1)
                 const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
                 const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
                 const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
-                mma_tf32(tmem, al, bh, idesc, (kb | k) != 0);
+                mma_tf32(tmem, al, bh, idesc, (i | k) != 0);
                 mma_tf32(tmem, ah, bl, idesc, 1u);
                 mma_tf32(tmem, ah, bh, idesc, 1u);
             }
@@ -252,104 +372,85 @@ __global__ void __launch_bounds__(128, 1)
     if (!mbar_wait_bounded(accb, 0u)) s_err = 1;
     tc_fence_after();
     __syncthreads();
-    if (s_err) {
-        if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
-    } else {
-        const int r = m0 + 32 * warp + lane;
-        const bool row_ok = r < g.M;
-        int pos = 0, active = 1;
-        if constexpr (EPI == GEPI_QKV_ROPE) {
-            if (row_ok) {
-                pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
-                active = g.active ? __ldcg(g.active + r) : 1;
+    const int row = 32 * warp + lane;  // this thread's TMEM lane = tile row
+    if (nsplit == 1) {
+        if (s_err) {
+            if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
+        } else {
+            const int r = m0 + row;
+            const bool row_ok = r < g.M;
+            int pos = 0, active = 1;
+            if constexpr (EPI == GEPI_QKV_ROPE) {
+                if (row_ok) row_state(g, r, pos, active);
+            }
+            unsigned long long best = 0ull;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+                const int gc0 = n0 + 32 * c;
+                if (!row_ok || gc0 >= g.N) continue;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
+                    if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, pos, active, best);
+                }
+            }
+            if constexpr (EPI == GEPI_ARGMAX) {
+                if (row_ok && best != 0ull) atomicMax(g.argmax_keys + r, best);
             }
         }
-        unsigned long long best = 0ull;
+    } else {
+        // stage this CTA's partial tile (row-major, stride PS) in the ring
+        float* P = reinterpret_cast<float*>(gbase);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
-            __syncwarp();  // tcgen05.ld is warp-collective
+            __syncwarp();
             tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
-            const int gc0 = n0 + 32 * c;
-            if (!row_ok || gc0 >= g.N) continue;
-            const bool full_chunk = gc0 + 32 <= g.N;
-            if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
-                float* o = g.out + static_cast<size_t>(r) * g.ldc + gc0;
-                if (full_chunk && (g.ldc & 3) == 0) {
+            if (NK == 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float4 w = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                        if constexpr (EPI == GEPI_RESIDUAL) {
-                            const float4 x = __ldcg(reinterpret_cast<const float4*>(o + j));
-                            w.x += x.x;
-                            w.y += x.y;
-                            w.z += x.z;
-                            w.w += x.w;
-                        }
-                        *reinterpret_cast<float4*>(o + j) = w;
-                    }
-                } else {
-                    for (int j = 0; j < 32 && gc0 + j < g.N; ++j)
-                        o[j] = (EPI == GEPI_RESIDUAL) ? __ldcg(o + j) + v[j] : v[j];
+                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(P + row * PS + 32 * c + j) =
+                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        cluster_sync_all();  // every partial of the cluster is staged
+        int any_err = 0;
+        for (int q = 0; q < nsplit; ++q) any_err |= ld_peer_i32(map_peer(smem_u32(&s_err), q));
+        if (!any_err) {
+            const int r0 = 128 * split / nsplit, r1 = 128 * (split + 1) / nsplit;
+            const int gpr = BN / 4;  // float4 groups per row
+            const uint32_t pbase = smem_u32(P);
+            for (int t = threadIdx.x; t < (r1 - r0) * gpr; t += 128) {
+                const int lr = r0 + t / gpr, c4 = t % gpr;
+                const int r = m0 + lr, gc = n0 + 4 * c4;
+                if (r >= g.M || gc >= g.N) continue;
+                const uint32_t off = static_cast<uint32_t>((lr * PS + 4 * c4) * 4);
+                float4 acc = ld_peer_f4(map_peer(pbase + off, 0));
+                for (int q = 1; q < nsplit; ++q) {
+                    const float4 v = ld_peer_f4(map_peer(pbase + off, q));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
                 }
-            } else if constexpr (EPI == GEPI_SWIGLU) {
-                // interleaved rows: column 2j is the gate, 2j+1 the up projection
-                const size_t F = static_cast<size_t>(g.N) >> 1;
-                float* oh = g.out_hi + static_cast<size_t>(r) * F + (gc0 >> 1);
-                float* ol = g.out_lo + static_cast<size_t>(r) * F + (gc0 >> 1);
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    if (gc0 + j + 1 < g.N) {
-                        const float h = silu(v[j]) * v[j + 1];
-                        const float hi = tf32_round(h);
-                        oh[j >> 1] = hi;
-                        ol[j >> 1] = h - hi;
-                    }
-                }
-            } else if constexpr (EPI == GEPI_QKV_ROPE) {
-                if (!active) continue;
-                const int hd = g.head_dim;
-                const float2* rope = g.rope + static_cast<size_t>(pos) * (hd >> 1);
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const int gc = gc0 + j;
-                    if (gc + 1 >= g.N) break;
-                    const float x0 = v[j], x1 = v[j + 1];
-                    if (gc < g.d) {
-                        const float2 cs = rope[(gc % hd) >> 1];
-                        float* q = g.q + static_cast<size_t>(r) * g.d + gc;
-                        q[0] = x0 * cs.x - x1 * cs.y;
-                        q[1] = x0 * cs.y + x1 * cs.x;
-                    } else if (gc < g.d + g.kvd) {
-                        const int jj = gc - g.d, kvh = jj / hd, e = jj % hd;
-                        const float2 cs = rope[e >> 1];
-                        float* dst = g.k_cache + static_cast<size_t>(r) * g.cache_seq +
-                                     (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
-                        dst[0] = x0 * cs.x - x1 * cs.y;
-                        dst[1] = x0 * cs.y + x1 * cs.x;
-                    } else {
-                        const int jj = gc - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
-                        float* dst = g.v_cache + static_cast<size_t>(r) * g.cache_seq +
-                                     (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
-                        dst[0] = x0;
-                        dst[1] = x1;
-                    }
-                }
-            } else if constexpr (EPI == GEPI_ARGMAX) {
-                float* o = g.out ? g.out + static_cast<size_t>(r) * g.ldc + gc0 : nullptr;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (gc0 + j < g.N) {
-                        if (o) o[j] = v[j];
-                        const unsigned long long k = argmax_key(v[j], gc0 + j);
-                        best = k > best ? k : best;
-                    }
+                int pos = 0, active = 1;
+                if constexpr (EPI == GEPI_QKV_ROPE) row_state(g, r, pos, active);
+                unsigned long long best = 0ull;
+                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                epi4<EPI>(g, r, gc, a4, pos, active, best);
+                if constexpr (EPI == GEPI_ARGMAX) {
+                    if (best != 0ull) atomicMax(g.argmax_keys + r, best);
                 }
             }
+        } else if (split == 0 && threadIdx.x == 0) {
+            atomicOr(g.err, ERR_TIMEOUT_TMA);
         }
-        if constexpr (EPI == GEPI_ARGMAX) {
-            if (row_ok && best != 0ull) atomicMax(g.argmax_keys + r, best);
-        }
+        cluster_sync_all();  // peers are done reading this CTA's partial
     }
 
     // ---- teardown: every tcgen05 access of this CTA is complete
@@ -397,19 +498,23 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int BN, int EPI>
-cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool pdl) {
+cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStream_t s, bool pdl) {
     using C = Cfg<BN>;
     cudaLaunchConfig_t cfg{};
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
-    cfg.gridDim = dim3(mt * nt);
+    cfg.gridDim = dim3(ksplit, mt * nt);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI>, m.a_hi, m.a_lo, m.b_hi, m.b_lo,
                               g);
 }
@@ -432,13 +537,14 @@ cudaError_t set_smem_bn() {
 }
 
 template <int BN>
-cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, cudaStream_t s, bool pdl) {
+cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cudaStream_t s,
+                      bool pdl) {
     switch (epi) {
-        case GEPI_STORE: return launch_t<BN, GEPI_STORE>(m, g, s, pdl);
-        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL>(m, g, s, pdl);
-        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU>(m, g, s, pdl);
-        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE>(m, g, s, pdl);
-        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX>(m, g, s, pdl);
+        case GEPI_STORE: return launch_t<BN, GEPI_STORE>(m, g, ks, s, pdl);
+        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL>(m, g, ks, s, pdl);
+        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU>(m, g, ks, s, pdl);
+        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE>(m, g, ks, s, pdl);
+        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX>(m, g, ks, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -475,13 +581,42 @@ cudaError_t prepare_gemm() {
     return e != cudaSuccess ? e : set_smem_bn<128>();
 }
 
-int gemm_tile_n(int N) { return N >= 8192 ? 128 : 64; }
+// Tile width and K split of an M x N x K GEMM on `num_sms` SMs: for each
+// width, the split is the largest S <= 8 with tiles * S <= SMs and at least
+// two K-blocks per split; the plan that keeps more SMs busy wins (capped at
+// the SM count), ties going to the wider tile (fewer activation re-reads).
+int plan_split(int bn, int M, int N, int K, int num_sms) {
+    const int KB = (K + 31) / 32, mt = (M + 127) / 128;
+    const int tiles = mt * ((N + bn - 1) / bn);
+    int sp = num_sms / tiles;
+    sp = sp < 1 ? 1 : sp > 8 ? 8 : sp;
+    while (sp > 1 && KB / sp < 2) --sp;
+    return sp;
+}
 
-cudaError_t launch_gemm(int epi, int bn, const GemmMaps& m, const GemmArgs& g, cudaStream_t s,
-                        bool pdl) {
-    if (g.M < 1 || g.N < 1 || g.K < 4 || g.K % 4 != 0) return cudaErrorInvalidValue;
-    if (bn == 128) return launch_bn<128>(epi, m, g, s, pdl);
-    if (bn == 64) return launch_bn<64>(epi, m, g, s, pdl);
+GemmPlan plan_gemm(int M, int N, int K, int num_sms) {
+    GemmPlan best{128, 1};
+    int best_ctas = -1;
+    const int mt = (M + 127) / 128;
+    for (int bn : {128, 64}) {
+        const int tiles = mt * ((N + bn - 1) / bn);
+        const int sp = plan_split(bn, M, N, K, num_sms);
+        int ctas = tiles * sp;
+        if (ctas > num_sms) ctas = num_sms;
+        if (ctas > best_ctas) {
+            best_ctas = ctas;
+            best = GemmPlan{bn, sp};
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
+                        cudaStream_t s, bool pdl) {
+    if (g.M < 1 || g.N < 1 || g.K < 4 || g.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8)
+        return cudaErrorInvalidValue;
+    if (p.bn == 128) return launch_bn<128>(epi, m, g, p.ksplit, s, pdl);
+    if (p.bn == 64) return launch_bn<64>(epi, m, g, p.ksplit, s, pdl);
     return cudaErrorInvalidValue;
 }
 
@@ -518,7 +653,12 @@ extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, in
     float *a_hi = buf, *a_lo = buf + na_pad, *w_hi = a_lo + na_pad, *w_lo = w_hi + nw_pad;
     int* d_err = reinterpret_cast<int*>(w_lo + nw_pad);
     int rc = L2_OK;
-    const int bn = gemm_tile_n(N);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return L2_ECUDA;
+    const GemmPlan plan = plan_gemm(M, N, K, sms);
+    const int bn = plan.bn;
     GemmMaps maps;
     GemmArgs g{};
     g.M = M;
@@ -539,13 +679,13 @@ extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, in
         if ((e = make_gemm_map(&maps.a_lo, a_lo, K, M, 1, 128)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.b_hi, w_hi, K, N, 1, bn)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.b_lo, w_lo, K, N, 1, bn)) != cudaSuccess) break;
-        if ((e = launch_gemm(GEPI_STORE, bn, maps, g, s, false)) != cudaSuccess) break;
+        if ((e = launch_gemm(GEPI_STORE, plan, maps, g, s, false)) != cudaSuccess) break;
         if (iters > 0) {
             if ((e = cudaEventCreate(&e0)) != cudaSuccess) break;
             if ((e = cudaEventCreate(&e1)) != cudaSuccess) break;
             if ((e = cudaEventRecord(e0, s)) != cudaSuccess) break;
             for (int i = 0; i < iters && e == cudaSuccess; ++i)
-                e = launch_gemm(GEPI_STORE, bn, maps, g, s, false);
+                e = launch_gemm(GEPI_STORE, plan, maps, g, s, false);
             if (e != cudaSuccess) break;
             if ((e = cudaEventRecord(e1, s)) != cudaSuccess) break;
         }

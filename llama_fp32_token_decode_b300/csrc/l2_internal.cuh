@@ -302,10 +302,15 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
 // gemm_tf32x3.cu
 cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, long long rows,
                           long long layers, int box_rows);
+struct GemmPlan {
+    int bn;      // output tile width (64 or 128 columns)
+    int ksplit;  // CTAs of a cluster that split K (1..8)
+};
 cudaError_t prepare_gemm();
-int gemm_tile_n(int N);
-cudaError_t launch_gemm(int epi, int bn, const GemmMaps& m, const GemmArgs& g, cudaStream_t s,
-                        bool pdl);
+GemmPlan plan_gemm(int M, int N, int K, int num_sms);
+int plan_split(int bn, int M, int N, int K, int num_sms);
+cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
+                        cudaStream_t s, bool pdl);
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
 
 // batched.cu

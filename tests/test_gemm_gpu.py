@@ -6,7 +6,9 @@ element is normalised by sum_k |A_ik| |W_jk|, the scale every fp32 summation
 error is measured against. A single-pass TF32 product (10-bit mantissa) errs by
 ~1e-4 of that scale; an fp32-accurate product stays near 1e-7. Shapes cover a
 full 128-row tile pair, a ragged M/N/K, K below one 32-float block, the
-vocabulary-sized classifier, and both N tiles (64 and 128).
+vocabulary-sized classifier, both N tiles (64 and 128), and K split over
+clusters of 3, 6 and 8 CTAs (deterministic reduction through distributed
+shared memory).
 """
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(256, 1536, 512), (200, 328, 1376), (1, 64, 4), (130, 4099, 36), (256, 32000, 512),
-          (129, 8192, 64), (256, 512, 1376)]
+          (129, 8192, 64), (256, 512, 1376), (256, 2752, 512), (256, 512, 512)]
 
 
 @pytest.fixture(scope="module")
