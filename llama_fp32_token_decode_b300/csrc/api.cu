@@ -61,7 +61,8 @@ struct l2_handle {
     int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
     unsigned long long* b_keys = nullptr;
     GemmMaps m_qkv{}, m_wo{}, m_w13{}, m_w2{}, m_cls{};
-    GemmPlan gp_qkv{64, 1}, gp_wo{64, 1}, gp_w13{64, 1}, gp_w2{64, 1}, gp_cls{128, 1};
+    GemmPlan gp_qkv{64, 1, 2}, gp_wo{64, 1, 2}, gp_w13{64, 1, 2}, gp_w2{64, 1, 2}, gp_cls{128, 1, 2};
+    GemmOccupancy gocc{};
     cudaGraphExec_t bgraph = nullptr;  // one batched generation step
     int bgraph_M = 0, bgraph_steps = 0;
 
@@ -271,9 +272,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
     g.err = &h->st->err;
     g.layer = l;
     // tile width fixed at create (it is the weight maps' box); K split for this M
-    auto plan = [&](const GemmPlan& p, int N, int K) {
-        return GemmPlan{p.bn, plan_split(p.bn, M, N, K, h->num_sms)};
-    };
+    auto plan = [&](const GemmPlan& p, int N, int K) { return plan_split(h->gocc, p.bn, M, N, K); };
     switch (kind) {
         case BK_NORM_EMB:
         case BK_NORM: {
@@ -441,7 +440,7 @@ int setup_batched(l2_handle* h) {
     h->w2_hi = h->bw + o_dh; h->w2_lo = h->bw + o_dl;
     h->cls_hi = h->bw + o_ch; h->cls_lo = h->bw + o_cl;
     cudaStream_t s = h->stream;
-    L2_CUDA(h, prepare_gemm());
+    L2_CUDA(h, prepare_gemm(&h->gocc));
     L2_CUDA(h, launch_split_tf32(h->wqkv, h->qkv_hi, h->qkv_lo, n_qkv, s));
     L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
     L2_CUDA(h, launch_split_tf32(h->w13, h->w13_hi, h->w13_lo, n_w13, s));
@@ -469,12 +468,12 @@ int setup_batched(l2_handle* h) {
     h->b_prompts = h->bst + o_pr; h->b_out = h->bst + o_out;
     h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
 
-    const int Mb = static_cast<int>(B), sms = h->num_sms;
-    h->gp_qkv = plan_gemm(Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d), sms);
-    h->gp_wo = plan_gemm(Mb, static_cast<int>(d), static_cast<int>(d), sms);
-    h->gp_w13 = plan_gemm(Mb, static_cast<int>(2 * F), static_cast<int>(d), sms);
-    h->gp_w2 = plan_gemm(Mb, static_cast<int>(d), static_cast<int>(F), sms);
-    h->gp_cls = plan_gemm(Mb, static_cast<int>(V), static_cast<int>(d), sms);
+    const int Mb = static_cast<int>(B);
+    h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
+    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d));
+    h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d));
+    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F));
+    h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d));
     const long long D = d, FF = F, LL = L, MC = Mc;
     struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
     const MapSpec specs[] = {

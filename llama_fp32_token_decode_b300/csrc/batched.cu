@@ -162,6 +162,132 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_kernel(const BAttnArgs a)
     }
 }
 
+// Vectorised variant for head_dim % 4 == 0 and head_dim <= 4 * LPR: a row of
+// the cache is read by LPR lanes with 16-byte loads (32 / LPR rows per warp
+// load), G row slots per iteration, so a warp keeps 2 * G * 32/LPR rows of K
+// and V in flight. Each lane group (one row slot) runs its own online softmax
+// over its positions; groups merge by shuffles, warps through shared memory.
+template <int LPR, int G, int MINB>
+__global__ void __launch_bounds__(kBAttnThreads, MINB) battn4_kernel(const BAttnArgs a) {
+    constexpr int RPW = 32 / LPR;  // rows per warp load
+    constexpr int HD4MAX = LPR;    // float4 chunks of a row
+    pdl_launch_dependents();
+    pdl_wait();
+    const int h = blockIdx.x, b = blockIdx.y;
+    if (a.active != nullptr && __ldcg(a.active + b) == 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hd = a.head_dim, hd4 = hd >> 2;
+    const int c4 = lane % LPR, slot = lane / LPR;
+    const bool lane_on = c4 < hd4;
+    const int kvh = h / (a.n_heads / a.n_kv_heads);
+    const int n = min(max(__ldcg(a.pos + b), 0), a.seq_len - 1) + 1;
+    const size_t head_off = static_cast<size_t>(b) * a.cache_seq +
+                            static_cast<size_t>(kvh) * a.seq_len * hd;
+    const float4* K4 = reinterpret_cast<const float4*>(a.k_cache + head_off);
+    const float4* V4 = reinterpret_cast<const float4*>(a.v_cache + head_off);
+    const float4 q = lane_on ? __ldcg(reinterpret_cast<const float4*>(
+                                   a.q + static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd) + c4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float scale_div = sqrtf(static_cast<float>(hd));
+
+    float m = -INFINITY, l = 0.0f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int PER_IT = G * RPW;  // positions per warp iteration
+    for (int tb = warp * PER_IT; tb < n; tb += kBAttnWarps * PER_IT) {
+        float4 kr[G], vr[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int t = tb + g * RPW + slot;
+            const bool ok = lane_on && t < n;
+            kr[g] = ok ? __ldcg(K4 + static_cast<size_t>(t) * hd4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[g] = ok ? __ldcg(V4 + static_cast<size_t>(t) * hd4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float sc[G];
+        float gmax = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float p = q.x * kr[g].x;
+            p = fmaf(q.y, kr[g].y, p);
+            p = fmaf(q.z, kr[g].z, p);
+            p = fmaf(q.w, kr[g].w, p);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            sc[g] = (tb + g * RPW + slot < n) ? p / scale_div : -INFINITY;
+            gmax = fmaxf(gmax, sc[g]);
+        }
+        if (gmax == -INFINITY) continue;  // this slot has no positions left
+        const float mnew = fmaxf(m, gmax);
+        const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+        l *= corr;
+        o.x *= corr;
+        o.y *= corr;
+        o.z *= corr;
+        o.w *= corr;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float p = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+            l += p;
+            o.x = fmaf(p, vr[g].x, o.x);
+            o.y = fmaf(p, vr[g].y, o.y);
+            o.z = fmaf(p, vr[g].z, o.z);
+            o.w = fmaf(p, vr[g].w, o.w);
+        }
+        m = mnew;
+    }
+    // merge the row slots of this warp (lanes c4 + LPR * slot)
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float l2v = __shfl_xor_sync(0xffffffffu, l, off);
+        float4 o2;
+        o2.x = __shfl_xor_sync(0xffffffffu, o.x, off);
+        o2.y = __shfl_xor_sync(0xffffffffu, o.y, off);
+        o2.z = __shfl_xor_sync(0xffffffffu, o.z, off);
+        o2.w = __shfl_xor_sync(0xffffffffu, o.w, off);
+        const float M = fmaxf(m, m2);
+        const float f1 = (m == -INFINITY) ? 0.0f : expf(m - M);
+        const float f2 = (m2 == -INFINITY) ? 0.0f : expf(m2 - M);
+        l = l * f1 + l2v * f2;
+        o.x = o.x * f1 + o2.x * f2;
+        o.y = o.y * f1 + o2.y * f2;
+        o.z = o.z * f1 + o2.z * f2;
+        o.w = o.w * f1 + o2.w * f2;
+        m = M;
+    }
+    __shared__ float s_m[kBAttnWarps], s_l[kBAttnWarps];
+    __shared__ float4 s_o[kBAttnWarps][HD4MAX];
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+    if (slot == 0) s_o[warp][c4] = o;
+    __syncthreads();
+    if (tid < hd4) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kBAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+        float L = 0.0f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kBAttnWarps; ++w) {
+            if (s_m[w] == -INFINITY) continue;
+            const float f = expf(s_m[w] - M);
+            L += s_l[w] * f;
+            const float4 v = s_o[w][tid];
+            acc.x += v.x * f;
+            acc.y += v.y * f;
+            acc.z += v.z * f;
+            acc.w += v.w * f;
+        }
+        const float4 r = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+        const float4 hi = make_float4(tf32_round(r.x), tf32_round(r.y), tf32_round(r.z), tf32_round(r.w));
+        const size_t off = static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
+        reinterpret_cast<float4*>(a.att_hi + off)[tid] = hi;
+        reinterpret_cast<float4*>(a.att_lo + off)[tid] =
+            make_float4(r.x - hi.x, r.y - hi.y, r.z - hi.z, r.w - hi.w);
+    }
+}
+
 __global__ void badvance_kernel(const BAdvanceArgs a) {
     pdl_launch_dependents();
     pdl_wait();
@@ -210,6 +336,10 @@ cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl)
 cudaError_t launch_battn(const BAttnArgs& a, int M, cudaStream_t s, bool pdl) {
     if (M < 1) return cudaErrorInvalidValue;
     const dim3 grid(a.n_heads, M), block(kBAttnThreads);
+    if (a.head_dim % 4 == 0 && a.d % 4 == 0) {
+        if (a.head_dim <= 64) return launch_pdl(battn4_kernel<16, 4, 8>, grid, block, a, s, pdl);
+        if (a.head_dim <= 128) return launch_pdl(battn4_kernel<32, 4, 8>, grid, block, a, s, pdl);
+    }
     if (a.head_dim <= 64) return launch_pdl(battn_kernel<2, 8>, grid, block, a, s, pdl);
     if (a.head_dim <= 128) return launch_pdl(battn_kernel<4, 8>, grid, block, a, s, pdl);
     if (a.head_dim <= 256) return launch_pdl(battn_kernel<8, 4>, grid, block, a, s, pdl);

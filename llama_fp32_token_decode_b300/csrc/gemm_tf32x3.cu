@@ -130,9 +130,15 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 4;  // 16 KB
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
-    static constexpr int STAGES = (BN == 128) ? 3 : 4;
+    static constexpr int STAGES = (BN == 128) ? 3 : 4;  // deepest ring that fits
     static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
     static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 256;
+    // dynamic shared memory of a launch with a ring of `stages` slots (>= 2: the
+    // split-K staging of the partial tile reuses the first two slots)
+    static constexpr size_t smem_for(int stages) {
+        return 1024 + static_cast<size_t>(stages) * STAGE + 256;
+    }
+    static_assert(128 * (BN + 4) * 4 <= 2 * STAGE, "partial tile must fit in two slots");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
 };
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(128, 1)
                        const __grid_constant__ CUtensorMap mB_hi,
                        const __grid_constant__ CUtensorMap mB_lo, const GemmArgs g) {
     using C = Cfg<BN>;
-    constexpr int S = C::STAGES;
+    const int S = g.stages;     // ring depth of this launch (2..C::STAGES)
     constexpr int PS = BN + 4;  // row stride of the staged partial (floats)
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -504,7 +510,7 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(ksplit, mt * nt);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = C::smem_for(g.stages);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -574,47 +580,94 @@ cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Raises the dynamic shared-memory limit of every GEMM instantiation on the
-// current device (call before the first launch and outside stream capture).
-cudaError_t prepare_gemm() {
-    cudaError_t e = set_smem_bn<64>();
-    return e != cudaSuccess ? e : set_smem_bn<128>();
+template <int BN>
+int active_clusters(int ksplit, int stages) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ksplit, 1024);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE>, &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
-// Tile width and K split of an M x N x K GEMM on `num_sms` SMs: for each
-// width, the split is the largest S <= 8 with tiles * S <= SMs and at least
-// two K-blocks per split; the plan that keeps more SMs busy wins (capped at
-// the SM count), ties going to the wider tile (fewer activation re-reads).
-int plan_split(int bn, int M, int N, int K, int num_sms) {
+// Raises the dynamic shared-memory limit of every GEMM instantiation on the
+// current device and measures how many clusters of each launch shape run at
+// once (call before the first launch and outside stream capture).
+cudaError_t prepare_gemm(GemmOccupancy* occ) {
+    cudaError_t e = set_smem_bn<64>();
+    if (e == cudaSuccess) e = set_smem_bn<128>();
+    if (e != cudaSuccess || occ == nullptr) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&occ->num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+        cudaSuccess)
+        return e;
+    for (int sp = 1; sp <= 8; ++sp)
+        for (int st = 2; st <= 4; ++st) {
+            occ->clusters[0][sp][st] = st <= Cfg<64>::STAGES ? active_clusters<64>(sp, st) : 0;
+            occ->clusters[1][sp][st] = st <= Cfg<128>::STAGES ? active_clusters<128>(sp, st) : 0;
+        }
+    return cudaSuccess;
+}
+
+// K split and ring depth for a tile width: the largest split S <= 8 that keeps
+// at least two K-blocks per CTA and runs every cluster in one wave; the ring
+// holds one CTA's K-blocks, at least 2 and at most what fits.
+GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
     const int KB = (K + 31) / 32, mt = (M + 127) / 128;
     const int tiles = mt * ((N + bn - 1) / bn);
-    int sp = num_sms / tiles;
-    sp = sp < 1 ? 1 : sp > 8 ? 8 : sp;
-    while (sp > 1 && KB / sp < 2) --sp;
-    return sp;
+    const int max_st = bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+    auto depth = [&](int sp) {
+        const int per = (KB + sp - 1) / sp;
+        return per < 2 ? 2 : per > max_st ? max_st : per;
+    };
+    for (int sp = 8; sp > 1; --sp) {
+        if (KB / sp < 2) continue;
+        const int st = depth(sp);
+        if (tiles <= occ.clusters[bn == 128][sp][st]) return GemmPlan{bn, sp, st};
+    }
+    return GemmPlan{bn, 1, depth(1)};
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int num_sms) {
-    GemmPlan best{128, 1};
-    int best_ctas = -1;
+// Tile width and split of an M x N x K GEMM: the plan that keeps more SMs
+// busy in its first wave wins, ties going to the wider tile (fewer
+// activation re-reads).
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K) {
+    GemmPlan best{128, 1, Cfg<128>::STAGES};
+    long long best_ctas = -1;
     const int mt = (M + 127) / 128;
     for (int bn : {128, 64}) {
-        const int tiles = mt * ((N + bn - 1) / bn);
-        const int sp = plan_split(bn, M, N, K, num_sms);
-        int ctas = tiles * sp;
-        if (ctas > num_sms) ctas = num_sms;
+        const GemmPlan p = plan_split(occ, bn, M, N, K);
+        long long ctas = static_cast<long long>(mt) * ((N + bn - 1) / bn) * p.ksplit;
+        if (ctas > occ.num_sms) ctas = occ.num_sms;
         if (ctas > best_ctas) {
             best_ctas = ctas;
-            best = GemmPlan{bn, sp};
+            best = p;
         }
     }
     return best;
 }
 
-cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
+cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g0,
                         cudaStream_t s, bool pdl) {
-    if (g.M < 1 || g.N < 1 || g.K < 4 || g.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8)
+    const int max_st = p.bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+    if (g0.M < 1 || g0.N < 1 || g0.K < 4 || g0.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8 ||
+        p.stages < 2 || p.stages > max_st)
         return cudaErrorInvalidValue;
+    GemmArgs g = g0;
+    g.stages = p.stages;
     if (p.bn == 128) return launch_bn<128>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 64) return launch_bn<64>(epi, m, g, p.ksplit, s, pdl);
     return cudaErrorInvalidValue;
@@ -653,11 +706,9 @@ extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, in
     float *a_hi = buf, *a_lo = buf + na_pad, *w_hi = a_lo + na_pad, *w_lo = w_hi + nw_pad;
     int* d_err = reinterpret_cast<int*>(w_lo + nw_pad);
     int rc = L2_OK;
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return L2_ECUDA;
-    const GemmPlan plan = plan_gemm(M, N, K, sms);
+    GemmOccupancy occ{};
+    if (prepare_gemm(&occ) != cudaSuccess) return L2_ECUDA;
+    const GemmPlan plan = plan_gemm(occ, M, N, K);
     const int bn = plan.bn;
     GemmMaps maps;
     GemmArgs g{};
@@ -674,7 +725,6 @@ extern "C" int l2_gemm_tf32x3(const float* d_A, const float* d_W, float* d_C, in
             break;
         if ((e = launch_split_tf32(d_W, w_hi, w_lo, static_cast<long long>(nw), s)) != cudaSuccess)
             break;
-        if ((e = prepare_gemm()) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.a_hi, a_hi, K, M, 1, 128)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.a_lo, a_lo, K, M, 1, 128)) != cudaSuccess) break;
         if ((e = make_gemm_map(&maps.b_hi, w_hi, K, N, 1, bn)) != cudaSuccess) break;

@@ -123,6 +123,7 @@ struct GemmArgs {
     size_t cache_seq;     // floats of one sequence's cache (all layers)
     unsigned long long* argmax_keys;  // ARGMAX: [M]
     int* err;             // ERR_* bits
+    int stages;           // ring depth (set by launch_gemm from the plan)
 };
 
 // Batched decode (batched.cu). Row b of every [M][...] array is sequence b.
@@ -305,10 +306,17 @@ cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, 
 struct GemmPlan {
     int bn;      // output tile width (64 or 128 columns)
     int ksplit;  // CTAs of a cluster that split K (1..8)
+    int stages;  // shared-memory ring depth
 };
-cudaError_t prepare_gemm();
-GemmPlan plan_gemm(int M, int N, int K, int num_sms);
-int plan_split(int bn, int M, int N, int K, int num_sms);
+// Clusters of each (tile width, split, ring depth) that the device runs at
+// once, measured with cudaOccupancyMaxActiveClusters at set-up.
+struct GemmOccupancy {
+    int clusters[2][9][5];  // [bn == 128][ksplit][stages]
+    int num_sms;
+};
+cudaError_t prepare_gemm(GemmOccupancy* occ);
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K);
+GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K);
 cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
