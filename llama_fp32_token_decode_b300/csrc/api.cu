@@ -263,11 +263,12 @@ enum BKind : int {
 
 // Launches one kernel of a batched step for layer l on M rows. For BK_NORM the
 // gain is g_ffn[l] (gain_next == false) or the next layer's g_att / g_final.
-cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int steps,
+cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mode, int steps,
                          bool want_logits, bool gain_next, cudaStream_t s) {
     const l2_config& c = h->cfg;
     const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
     GemmArgs g{};
+    g.row0 = row0;
     g.M = M;
     g.err = &h->st->err;
     g.layer = l;
@@ -277,6 +278,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
         case BK_NORM_EMB:
         case BK_NORM: {
             BNormArgs n{};
+            n.row0 = row0;
             n.x = h->bx;
             n.emb = kind == BK_NORM_EMB ? h->emb : nullptr;
             n.token = h->b_token;
@@ -308,6 +310,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
             return launch_gemm(GEPI_QKV_ROPE, plan(h->gp_qkv, g.N, g.K), h->m_qkv, g, s, true);
         case BK_ATTN: {
             BAttnArgs t{};
+            t.row0 = row0;
             t.q = h->bq;
             t.k_cache = h->k_cache + l * h->cache_layer;
             t.v_cache = h->v_cache + l * h->cache_layer;
@@ -351,6 +354,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
             return launch_gemm(GEPI_ARGMAX, plan(h->gp_cls, g.N, g.K), h->m_cls, g, s, true);
         case BK_ADVANCE: {
             BAdvanceArgs a{};
+            a.row0 = row0;
             a.M = M;
             a.mode = mode;
             a.steps = steps;
@@ -370,21 +374,29 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int M, int mode, int ste
     }
 }
 
-// One lockstep step of M sequences: embedding + RMSNorm, then per layer the
-// QKV GEMM (RoPE + KV append), attention, Wo GEMM + residual, RMSNorm, W1/W3
-// GEMM + SwiGLU, W2 GEMM + residual, RMSNorm; the classifier GEMM with the
-// per-row argmax; and the per-sequence advance.
-cudaError_t enqueue_bstep(l2_handle* h, int M, int mode, int steps, bool want_logits,
-                          cudaStream_t s) {
-    cudaError_t e = launch_bkind(h, BK_NORM_EMB, 0, M, mode, steps, want_logits, false, s);
+// Kernels of one lockstep step of rows [row0, row0 + M), in order: embedding
+// + RMSNorm, then per layer the QKV GEMM (RoPE + KV append), attention, Wo
+// GEMM + residual, RMSNorm, W1/W3 GEMM + SwiGLU, W2 GEMM + residual, RMSNorm;
+// the classifier GEMM with the per-row argmax; and the per-sequence advance.
+cudaError_t enqueue_rows(l2_handle* h, int row0, int M, int mode, int steps, bool want_logits,
+                         cudaStream_t s) {
+    cudaError_t e = launch_bkind(h, BK_NORM_EMB, 0, row0, M, mode, steps, want_logits, false, s);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
         const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_NORM, BK_W13, BK_W2, BK_NORM};
         for (int i = 0; i < 7 && e == cudaSuccess; ++i)
-            e = launch_bkind(h, seq[i], l, M, mode, steps, want_logits, i == 6, s);
+            e = launch_bkind(h, seq[i], l, row0, M, mode, steps, want_logits, i == 6, s);
     }
-    if (e == cudaSuccess) e = launch_bkind(h, BK_CLS, 0, M, mode, steps, want_logits, false, s);
-    if (e == cudaSuccess) e = launch_bkind(h, BK_ADVANCE, 0, M, mode, steps, want_logits, false, s);
+    if (e == cudaSuccess)
+        e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, false, s);
+    if (e == cudaSuccess)
+        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, false, s);
     return e;
+}
+
+// One lockstep step of M sequences (rows [0, M)) on stream s.
+cudaError_t enqueue_bstep(l2_handle* h, int M, int mode, int steps, bool want_logits,
+                          cudaStream_t s) {
+    return enqueue_rows(h, 0, M, mode, steps, want_logits, s);
 }
 
 // Rows [0, M): active, keys cleared; for generation, pos 0 and the first prompt token.
@@ -983,10 +995,10 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
         bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
                                                     h->b_keys, h->st);
         L2_CUDA(h, cudaGetLastError());
-        L2_CUDA(h, launch_bkind(h, bk, 0, M, 0, 0, false, false, s));
+        L2_CUDA(h, launch_bkind(h, bk, 0, 0, M, 0, 0, false, false, s));
         L2_CUDA(h, cudaEventRecord(h->ev0, s));
         for (int i = 0; i < iters; ++i)
-            L2_CUDA(h, launch_bkind(h, bk, i % h->cfg.n_layers, M, 0, 0, false, false, s));
+            L2_CUDA(h, launch_bkind(h, bk, i % h->cfg.n_layers, 0, M, 0, 0, false, false, s));
         L2_CUDA(h, cudaEventRecord(h->ev1, s));
         L2_CUDA(h, cudaEventSynchronize(h->ev1));
         float t = 0.0f;

@@ -25,7 +25,7 @@ constexpr int kBAttnWarps = kBAttnThreads / 32;
 __global__ void __launch_bounds__(kNormThreads) brmsnorm_kernel(const BNormArgs a) {
     pdl_launch_dependents();
     pdl_wait();
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = a.row0 + blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, d4 = d >> 2;
     float4* x4 = reinterpret_cast<float4*>(a.x + static_cast<size_t>(b) * d);
     const float4* src4 = x4;
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_kernel(const BAttnArgs a)
     constexpr int HDMAX = 32 * EPL;
     pdl_launch_dependents();
     pdl_wait();
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, b = a.row0 + blockIdx.y;
     if (a.active != nullptr && __ldcg(a.active + b) == 0) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hd = a.head_dim;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kBAttnThreads, MINB) battn4_kernel(const BAttn
     constexpr int HD4MAX = LPR;    // float4 chunks of a row
     pdl_launch_dependents();
     pdl_wait();
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, b = a.row0 + blockIdx.y;
     if (a.active != nullptr && __ldcg(a.active + b) == 0) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hd = a.head_dim, hd4 = hd >> 2;
@@ -291,8 +291,9 @@ __global__ void __launch_bounds__(kBAttnThreads, MINB) battn4_kernel(const BAttn
 __global__ void badvance_kernel(const BAdvanceArgs a) {
     pdl_launch_dependents();
     pdl_wait();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= a.M) return;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= a.M) return;
+    const int b = a.row0 + i;
     const unsigned long long k = a.keys[b];
     a.keys[b] = 0ull;
     const int idx = (k == 0ull) ? 0 : argmax_key_index(k);

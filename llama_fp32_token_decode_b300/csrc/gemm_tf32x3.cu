@@ -281,8 +281,9 @@ __global__ void __launch_bounds__(128, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsplit = gridDim.x, split = blockIdx.x;
     const int mt = (g.M + 127) / 128;
-    const int m0 = (blockIdx.y % mt) * 128;
+    const int m0 = g.row0 + (blockIdx.y % mt) * 128;  // first row of this tile
     const int n0 = (blockIdx.y / mt) * BN;
+    const int m_end = g.row0 + g.M;                   // rows of this launch end here
     const int KB = (g.K + 31) / 32;
     const int kb0 = KB * split / nsplit, kb1 = KB * (split + 1) / nsplit;
     const int NK = kb1 - kb0;
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(128, 1)
             if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
         } else {
             const int r = m0 + row;
-            const bool row_ok = r < g.M;
+            const bool row_ok = r < m_end;
             int pos = 0, active = 1;
             if constexpr (EPI == GEPI_QKV_ROPE) {
                 if (row_ok) row_state(g, r, pos, active);
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(128, 1)
             for (int t = threadIdx.x; t < (r1 - r0) * gpr; t += 128) {
                 const int lr = r0 + t / gpr, c4 = t % gpr;
                 const int r = m0 + lr, gc = n0 + 4 * c4;
-                if (r >= g.M || gc >= g.N) continue;
+                if (r >= m_end || gc >= g.N) continue;
                 const uint32_t off = static_cast<uint32_t>((lr * PS + 4 * c4) * 4);
                 float4 acc = ld_peer_f4(map_peer(pbase + off, 0));
                 for (int q = 1; q < nsplit; ++q) {
@@ -624,7 +625,9 @@ cudaError_t prepare_gemm(GemmOccupancy* occ) {
 
 // K split and ring depth for a tile width: the largest split S <= 8 that keeps
 // at least two K-blocks per CTA and runs every cluster in one wave; the ring
-// holds one CTA's K-blocks, at least 2 and at most what fits.
+// holds one CTA's K-blocks, at least 2 and at most what fits. (Measured on the
+// batched decode GEMMs: two co-resident CTAs per SM with 2-slot rings are no
+// faster than one CTA per SM with a deeper ring.)
 GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
     const int KB = (K + 31) / 32, mt = (M + 127) / 128;
     const int tiles = mt * ((N + bn - 1) / bn);

@@ -106,7 +106,8 @@ struct GemmMaps {
 };
 
 struct GemmArgs {
-    int M, N, K;          // rows (sequences), output columns, reduction length
+    int row0;             // first row (sequence) of this launch
+    int M, N, K;          // rows (sequences) from row0, output columns, reduction length
     int layer;            // weight map z coordinate
     int ldc;              // row stride of out
     float* out;           // STORE / RESIDUAL / ARGMAX (logits, may be null)
@@ -128,7 +129,8 @@ struct GemmArgs {
 
 // Batched decode (batched.cu). Row b of every [M][...] array is sequence b.
 struct BNormArgs {
-    float* x;              // [M][d] residual rows (set to emb[token] when emb != null)
+    int row0;              // rows row0 .. row0 + gridDim.x - 1
+    float* x;              // [rows][d] residual rows (set to emb[token] when emb != null)
     const float* emb;      // embedding table [V][d] or null
     const int* token;      // [M] (used when emb != null)
     const float* gain;     // [d]
@@ -139,7 +141,8 @@ struct BNormArgs {
 };
 
 struct BAttnArgs {
-    const float* q;        // [M][d], RoPE applied
+    int row0;              // sequences row0 .. row0 + gridDim.y - 1
+    const float* q;        // [rows][d], RoPE applied
     const float* k_cache;  // layer l of sequence 0; sequence b at + b * cache_seq
     const float* v_cache;
     float* att_hi;         // [M][d] output, tf32 pair
@@ -151,6 +154,7 @@ struct BAttnArgs {
 };
 
 struct BAdvanceArgs {
+    int row0;                    // rows row0 .. row0 + M - 1
     int M;
     int mode;                    // 0 = forward only, 1 = generate
     int steps;                   // generate: tokens per sequence (row stride of out)
