@@ -124,6 +124,9 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Dynamic shared memory one CTA may use (227 KB opt-in, minus static use).
+constexpr size_t kMaxDynSmem = 227 * 1024 - 64;
+
 template <int BN>
 struct Cfg {
     static constexpr int BM = 128, BK = 32;
@@ -132,13 +135,19 @@ struct Cfg {
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int STAGES = (BN == 128) ? 3 : 4;  // deepest ring that fits
     static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
-    static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 256;
-    // dynamic shared memory of a launch with a ring of `stages` slots (>= 2: the
-    // split-K staging of the partial tile reuses the first two slots)
-    static constexpr size_t smem_for(int stages) {
-        return 1024 + static_cast<size_t>(stages) * STAGE + 256;
+    static constexpr int PS = BN + 4;  // row stride (floats) of a staged partial tile
+    // split-K receive buffer: one slot per peer, ceil(128 / S) rows of PS floats
+    __host__ __device__ static constexpr size_t recv_bytes(int ksplit) {
+        return ksplit > 1 ? static_cast<size_t>(ksplit - 1) * ((128 + ksplit - 1) / ksplit) * PS * 4
+                          : 0;
     }
-    static_assert(128 * (BN + 4) * 4 <= 2 * STAGE, "partial tile must fit in two slots");
+    // dynamic shared memory of a launch: alignment slack, a ring of `stages`
+    // slots (>= 2: the staged partial tile reuses the first two), the receive
+    // buffer of a split launch, barriers
+    __host__ __device__ static constexpr size_t smem_for(int stages, int ksplit) {
+        return 1024 + static_cast<size_t>(stages) * STAGE + recv_bytes(ksplit) + 256;
+    }
+    static_assert(128 * PS * 4 <= 2 * STAGE, "partial tile must fit in two slots");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
 };
@@ -147,27 +156,33 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // ---- cluster helpers (split-K reduction through distributed shared memory)
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
+// Generic-proxy shared-memory writes become visible to bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ int ld_peer_i32(uint32_t addr) {
-    int v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
+// Bulk copy of `bytes` from this CTA's shared memory into a peer's (dst and
+// bar are shared::cluster addresses from mapa), completion counted on bar.
+__device__ __forceinline__ void bulk_s2peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Fused epilogue of four consecutive output columns gc..gc+3 (gc % 4 == 0) of
@@ -266,20 +281,23 @@ __global__ void __launch_bounds__(128, 1)
                        const __grid_constant__ CUtensorMap mB_hi,
                        const __grid_constant__ CUtensorMap mB_lo, const GemmArgs g) {
     using C = Cfg<BN>;
-    const int S = g.stages;     // ring depth of this launch (2..C::STAGES)
-    constexpr int PS = BN + 4;  // row stride of the staged partial (floats)
+    const int S = g.stages;       // ring depth of this launch (2..C::STAGES)
+    constexpr int PS = C::PS;     // row stride of the staged partial (floats)
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* gbase = smem_raw + (base - raw);
-    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * C::STAGE);
+    const int nsplit = gridDim.x, split = blockIdx.x;
+    const uint32_t recv_base = base + static_cast<uint32_t>(S * C::STAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * C::STAGE +
+                                                 C::recv_bytes(nsplit));
     uint64_t* empty = full + S;
     uint64_t* accb = empty + S;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    uint64_t* recvb = accb + 1;  // split-K: the peers' slices of this CTA's rows
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
     __shared__ int s_err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nsplit = gridDim.x, split = blockIdx.x;
     const int mt = (g.M + 127) / 128;
     const int m0 = g.row0 + (blockIdx.y % mt) * 128;  // first row of this tile
     const int n0 = (blockIdx.y / mt) * BN;
@@ -294,6 +312,7 @@ __global__ void __launch_bounds__(128, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(accb, 1);
+        mbar_init(recvb, 1);
         fence_mbar_init();
         s_err = 0;
         prefetch_map(&mA_hi);
@@ -310,6 +329,9 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
+    // split-K: announce this CTA's initialised barriers to the cluster now and
+    // collect the peers' announcements only before pushing to them
+    if (nsplit > 1) cluster_arrive_release();
 
     auto a_hi = [&](int s) { return base + static_cast<uint32_t>(s * C::STAGE); };
     auto a_lo = [&](int s) { return a_hi(s) + C::A_BYTES; };
@@ -425,25 +447,66 @@ __global__ void __launch_bounds__(128, 1)
                 *reinterpret_cast<float4*>(P + row * PS + 32 * c + j) =
                     make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
-        cluster_sync_all();  // every partial of the cluster is staged
-        int any_err = 0;
-        for (int q = 0; q < nsplit; ++q) any_err |= ld_peer_i32(map_peer(smem_u32(&s_err), q));
-        if (!any_err) {
-            const int r0 = 128 * split / nsplit, r1 = 128 * (split + 1) / nsplit;
-            const int gpr = BN / 4;  // float4 groups per row
-            const uint32_t pbase = smem_u32(P);
-            for (int t = threadIdx.x; t < (r1 - r0) * gpr; t += 128) {
+        fence_proxy_async_smem();
+        __syncthreads();
+        cluster_wait_acquire();  // every peer's barriers are initialised
+        const int R = (128 + nsplit - 1) / nsplit;  // rows of a receive slot
+        const int r0 = 128 * split / nsplit, r1 = 128 * (split + 1) / nsplit;
+        const uint32_t pbase = smem_u32(P);
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(recvb, static_cast<uint32_t>((nsplit - 1) * (r1 - r0) * PS * 4));
+            // push rows [128q/S, 128(q+1)/S) of this partial to their owner q
+            for (int q = 0; q < nsplit; ++q) {
+                if (q == split) continue;
+                const int q0 = 128 * q / nsplit, q1 = 128 * (q + 1) / nsplit;
+                const int slot = split < q ? split : split - 1;  // slot of this sender at q
+                bulk_s2peer(map_peer(recv_base + static_cast<uint32_t>(slot * R * PS * 4), q),
+                            pbase + static_cast<uint32_t>(q0 * PS * 4),
+                            static_cast<uint32_t>((q1 - q0) * PS * 4), map_peer(smem_u32(recvb), q));
+            }
+        }
+        const int gpr = BN / 4;  // float4 groups per row
+        // residual: this thread's first rows of x are loaded while the slices travel
+        constexpr int kPre = 4;
+        float4 xpre[kPre];
+        if constexpr (EPI == GEPI_RESIDUAL) {
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int t = threadIdx.x + 128 * u;
+                const int lr = r0 + t / gpr, gc = n0 + 4 * (t % gpr);
+                const int r = m0 + lr;
+                xpre[u] = (t < (r1 - r0) * gpr && r < m_end && gc + 4 <= g.N && (g.ldc & 3) == 0)
+                              ? __ldcg(reinterpret_cast<const float4*>(
+                                    g.out + static_cast<size_t>(r) * g.ldc + gc))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        const bool got = mbar_wait_bounded(recvb, 0u);
+        if (!got) s_err = 1;
+        if (!s_err) {
+            const float* recv = reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
+            const int ngroups = (r1 - r0) * gpr;
+            // group t: row r0 + t / gpr, columns 4 (t % gpr) .. + 3 of the tile; the
+            // partials are added in rank order (a fixed order, whoever arrived first)
+            auto group = [&](int t, bool have_x, float4 x) {
                 const int lr = r0 + t / gpr, c4 = t % gpr;
                 const int r = m0 + lr, gc = n0 + 4 * c4;
-                if (r >= m_end || gc >= g.N) continue;
-                const uint32_t off = static_cast<uint32_t>((lr * PS + 4 * c4) * 4);
-                float4 acc = ld_peer_f4(map_peer(pbase + off, 0));
-                for (int q = 1; q < nsplit; ++q) {
-                    const float4 v = ld_peer_f4(map_peer(pbase + off, q));
+                if (r >= m_end || gc >= g.N) return;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < nsplit; ++q) {
+                    const float* src = (q == split)
+                        ? P + lr * PS
+                        : recv + static_cast<size_t>((q < split ? q : q - 1) * R + (lr - r0)) * PS;
+                    const float4 v = *reinterpret_cast<const float4*>(src + 4 * c4);
                     acc.x += v.x;
                     acc.y += v.y;
                     acc.z += v.z;
                     acc.w += v.w;
+                }
+                if (have_x) {  // residual with its row already loaded
+                    *reinterpret_cast<float4*>(g.out + static_cast<size_t>(r) * g.ldc + gc) =
+                        make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
+                    return;
                 }
                 int pos = 0, active = 1;
                 if constexpr (EPI == GEPI_QKV_ROPE) row_state(g, r, pos, active);
@@ -453,11 +516,22 @@ __global__ void __launch_bounds__(128, 1)
                 if constexpr (EPI == GEPI_ARGMAX) {
                     if (best != 0ull) atomicMax(g.argmax_keys + r, best);
                 }
+            };
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int t = threadIdx.x + 128 * u;
+                if (t < ngroups) {
+                    const int gc = n0 + 4 * (t % gpr);
+                    const bool hx = (EPI == GEPI_RESIDUAL) && gc + 4 <= g.N && (g.ldc & 3) == 0;
+                    group(t, hx, xpre[u]);
+                }
             }
-        } else if (split == 0 && threadIdx.x == 0) {
+            for (int t = threadIdx.x + 128 * kPre; t < ngroups; t += 128)
+                group(t, false, make_float4(0.f, 0.f, 0.f, 0.f));
+        } else if (threadIdx.x == 0) {
             atomicOr(g.err, ERR_TIMEOUT_TMA);
         }
-        cluster_sync_all();  // peers are done reading this CTA's partial
+        if (threadIdx.x == 0) bulk_commit_and_wait_read();  // this CTA's pushes have read P
     }
 
     // ---- teardown: every tcgen05 access of this CTA is complete
@@ -511,7 +585,7 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(ksplit, mt * nt);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = C::smem_for(g.stages);
+    cfg.dynamicSmemBytes = C::smem_for(g.stages, ksplit);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -530,7 +604,7 @@ template <int BN, int EPI>
 cudaError_t set_smem() {
     return cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(Cfg<BN>::SMEM));
+                                static_cast<int>(kMaxDynSmem));
 }
 
 template <int BN>
@@ -581,12 +655,19 @@ cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Whether a ring of `stages` slots (and the receive buffer of a split launch)
+// fits in one CTA's shared memory.
+template <int BN>
+bool fits(int stages, int ksplit) {
+    return stages <= Cfg<BN>::STAGES && Cfg<BN>::smem_for(stages, ksplit) <= kMaxDynSmem;
+}
+
 template <int BN>
 int active_clusters(int ksplit, int stages) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ksplit, 1024);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages);
+    cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages, ksplit);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ksplit;
@@ -617,8 +698,8 @@ cudaError_t prepare_gemm(GemmOccupancy* occ) {
         return e;
     for (int sp = 1; sp <= 8; ++sp)
         for (int st = 2; st <= 4; ++st) {
-            occ->clusters[0][sp][st] = st <= Cfg<64>::STAGES ? active_clusters<64>(sp, st) : 0;
-            occ->clusters[1][sp][st] = st <= Cfg<128>::STAGES ? active_clusters<128>(sp, st) : 0;
+            occ->clusters[0][sp][st] = fits<64>(st, sp) ? active_clusters<64>(sp, st) : 0;
+            occ->clusters[1][sp][st] = fits<128>(st, sp) ? active_clusters<128>(sp, st) : 0;
         }
     return cudaSuccess;
 }
@@ -634,7 +715,9 @@ GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
     const int max_st = bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
     auto depth = [&](int sp) {
         const int per = (KB + sp - 1) / sp;
-        return per < 2 ? 2 : per > max_st ? max_st : per;
+        int st = per < 2 ? 2 : per > max_st ? max_st : per;
+        while (st > 2 && !(bn == 128 ? fits<128>(st, sp) : fits<64>(st, sp))) --st;
+        return st;
     };
     for (int sp = 8; sp > 1; --sp) {
         if (KB / sp < 2) continue;
