@@ -59,7 +59,10 @@ extern "C" {
  * (openai.wiki "训练示例"); larger shapes follow the same architecture.
  * Requirements: all sizes > 0; dim % n_heads == 0; head_dim = dim / n_heads
  * even and <= 256; n_heads % n_kv_heads == 0; dim % 4 == 0;
- * hidden_dim % 4 == 0; 1 <= max_batch <= 1024. */
+ * hidden_dim % 4 == 0; 1 <= max_batch <= 1024; 0 <= max_prefill <= 1024.
+ * max_batch sequences get a KV cache each; the tensor-core path (batched
+ * decode, prefill) is set up when max_batch > 1 or max_prefill > 1, with
+ * row buffers for max(max_batch, max_prefill) rows. */
 typedef struct {
     int32_t dim;               /* d, width of the residual stream            */
     int32_t hidden_dim;        /* F, SwiGLU hidden width                     */
@@ -72,6 +75,7 @@ typedef struct {
     float norm_eps;            /* 1e-5                                       */
     int32_t max_batch;         /* sequences one handle can decode at once    */
     int32_t shared_classifier; /* 1: classifier = embedding table (no Wcls)  */
+    int32_t max_prefill;       /* prompt positions one prefill pass takes    */
 } l2_config;
 
 typedef struct l2_handle l2_handle;
@@ -129,6 +133,36 @@ L2_API int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_
  * prompt id outside [0, V). Synchronous. */
 L2_API int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
                 int32_t* out_tokens);
+
+/* Parallel prompt prefill of sequence 0 (cache 0): the n tokens at positions
+ * pos0 .. pos0+n-1 go through one causal pass in which every projection is a
+ * tensor-core GEMM over the n positions (3xTF32, fp32 accuracy) and position p
+ * attends over cache slots 0..p; it writes cache slots pos0 .. pos0+n-1 and
+ * computes the logits of every position, exactly what n consecutive
+ * l2_forward calls compute (up to summation order). Slots below pos0 must
+ * hold the sequence's earlier positions. The pages' engine feeds a prompt one
+ * token per forward (新智元 article, "使用指南"); this pass computes the same
+ * positions at once, so the weights are read once for the whole prompt.
+ * tokens: host [n]; logits_out: host [n][V] or NULL.
+ * Errors: L2_EINVAL for n < 1, n > max(max_batch, max_prefill) (or a handle
+ * without the tensor-core path), pos0 < 0, pos0 + n > S, or a token outside
+ * [0, V). Synchronous. */
+L2_API int l2_prefill(l2_handle* h, const int32_t* tokens, int32_t n, int32_t pos0,
+                      float* logits_out);
+
+/* l2_generate with the prompt taken by one prefill pass (l2_prefill) instead
+ * of n_prompt decode forwards; then steps-1 decode forwards as l2_generate.
+ * Same output contract as l2_generate: out_tokens[k] is the argmax at position
+ * n_prompt-1+k. Extra error: L2_EINVAL when n_prompt exceeds the prefill
+ * capacity. Synchronous. */
+L2_API int l2_generate_prefill(l2_handle* h, const int32_t* prompt, int32_t n_prompt,
+                               int32_t steps, int32_t* out_tokens);
+
+/* l2_generate_prefill with device buffers (d_prompt int32 [n_prompt], d_out
+ * int32 [steps]), queued on `stream`; returns without waiting. Device prompt
+ * ids are not range-checked (clamped). */
+L2_API int l2_generate_prefill_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
+                                      int32_t steps, int32_t* d_out, void* stream);
 
 /* l2_generate with device buffers: d_prompt int32 [n_prompt], d_out int32
  * [steps]; queued on `stream`, returns without waiting. Host-side checks as

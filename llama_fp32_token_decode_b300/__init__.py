@@ -4,7 +4,8 @@ Argument marshalling only: every step of the decode path runs in the library's
 CUDA kernels. There is no CPU fallback; importing this package fails loudly when
 the library has not been built (``python llama_fp32_token_decode_b300/build.py``).
 Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
-l2_generate, l2_generate_device, l2_generate_batch, l2_reset, l2_destroy,
+l2_generate, l2_generate_device, l2_generate_batch, l2_generate_batch_device,
+l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
 l2_classify_greedy_noalloc, l2_gemm_tf32x3.
 """
@@ -28,7 +29,8 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
                 "b_w2_gemm", "b_classifier_gemm", "b_rmsnorm", "b_advance")
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
-           "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device", "l2_reset", "l2_destroy",
+           "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device", "l2_prefill",
+           "l2_generate_prefill", "l2_generate_prefill_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
            "l2_gemm_tf32x3")
 
@@ -41,7 +43,7 @@ class L2Config(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("vocab_size", ctypes.c_int32),
                 ("seq_len", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("norm_eps", ctypes.c_float), ("max_batch", ctypes.c_int32),
-                ("shared_classifier", ctypes.c_int32)]
+                ("shared_classifier", ctypes.c_int32), ("max_prefill", ctypes.c_int32)]
 
 
 class L2Error(RuntimeError):
@@ -68,6 +70,9 @@ _SIG = {
     "l2_generate_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_generate_batch": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
     "l2_generate_batch_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
+    "l2_prefill": (ctypes.c_int, [_P, _P, _I, _I, _P]),
+    "l2_generate_prefill": (ctypes.c_int, [_P, _P, _I, _I, _P]),
+    "l2_generate_prefill_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_reset": (ctypes.c_int, [_P, _I]),
     "l2_destroy": (None, [_P]),
     "l2_last_error": (ctypes.c_char_p, [_P]),
@@ -88,7 +93,8 @@ def make_config(cfg: dict) -> L2Config:
     return L2Config(cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["n_heads"],
                     cfg.get("n_kv_heads") or cfg["n_heads"], cfg["vocab_size"], cfg["seq_len"],
                     cfg.get("rope_theta", 10000.0), cfg.get("norm_eps", 1e-5),
-                    cfg.get("max_batch", 1), cfg.get("shared_classifier", 0))
+                    cfg.get("max_batch", 1), cfg.get("shared_classifier", 0),
+                    cfg.get("max_prefill", 0))
 
 
 def _check(rc: int, h=None):
@@ -165,6 +171,29 @@ def l2_generate(h, prompt, steps: int) -> np.ndarray:
 def l2_generate_device(h, d_prompt, n_prompt: int, steps: int, d_out, stream=None) -> None:
     _check(_lib.l2_generate_device(h, _ptr(d_prompt), n_prompt, steps, _ptr(d_out),
                                    _stream(stream)), h)
+
+
+def l2_prefill(h, tokens, pos0: int, vocab_size: int, want_logits: bool = True):
+    """One causal prefill pass of sequence 0; returns logits [n][V] (or None)."""
+    tokens = _i32(tokens).ravel()
+    out = np.empty((tokens.size, vocab_size), np.float32) if want_logits else None
+    _check(_lib.l2_prefill(h, tokens.ctypes.data, tokens.size, pos0,
+                           out.ctypes.data if want_logits else None), h)
+    return out
+
+
+def l2_generate_prefill(h, prompt, steps: int) -> np.ndarray:
+    prompt = _i32(prompt).ravel()
+    out = np.empty(steps, np.int32)
+    _check(_lib.l2_generate_prefill(h, prompt.ctypes.data, prompt.size, steps, out.ctypes.data),
+           h)
+    return out
+
+
+def l2_generate_prefill_device(h, d_prompt, n_prompt: int, steps: int, d_out,
+                               stream=None) -> None:
+    _check(_lib.l2_generate_prefill_device(h, _ptr(d_prompt), n_prompt, steps, _ptr(d_out),
+                                           _stream(stream)), h)
 
 
 def l2_generate_batch(h, prompts, lens, steps: int) -> np.ndarray:
@@ -249,6 +278,12 @@ class Decoder:
 
     def generate(self, prompt, steps: int) -> np.ndarray:
         return l2_generate(self.h, prompt, steps)
+
+    def prefill(self, tokens, pos0: int = 0, want_logits: bool = True):
+        return l2_prefill(self.h, tokens, pos0, self.cfg["vocab_size"], want_logits)
+
+    def generate_prefill(self, prompt, steps: int) -> np.ndarray:
+        return l2_generate_prefill(self.h, prompt, steps)
 
     def generate_batch(self, prompts, lens, steps: int) -> np.ndarray:
         return l2_generate_batch(self.h, prompts, lens, steps)

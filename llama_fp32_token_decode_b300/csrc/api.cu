@@ -48,6 +48,7 @@ struct l2_handle {
     // batched path (max_batch > 1): weights as tf32 (hi, lo) pairs, [Mcap][...]
     // activation rows, per-sequence state and the GEMM operand maps
     int mcap = 0;
+    int rows = 0;                      // max(max_batch, max_prefill): row buffers of the GEMM path
     float* bw = nullptr;
     float *qkv_hi = nullptr, *qkv_lo = nullptr, *wo_hi = nullptr, *wo_lo = nullptr;
     float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
@@ -59,6 +60,7 @@ struct l2_handle {
     int* bst = nullptr;
     int *b_pos = nullptr, *b_token = nullptr, *b_active = nullptr, *b_len = nullptr;
     int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
+    int* b_seq = nullptr;              // KV cache of each row (prefill: all 0)
     unsigned long long* b_keys = nullptr;
     GemmMaps m_qkv{}, m_wo{}, m_w13{}, m_w2{}, m_cls{};
     GemmPlan gp_qkv{64, 1, 2}, gp_wo{64, 1, 2}, gp_w13{64, 1, 2}, gp_w2{64, 1, 2}, gp_cls{128, 1, 2};
@@ -118,6 +120,7 @@ bool config_valid(const l2_config* c, std::string* why) {
     if (c->vocab_size > (1 << 24)) return bad("vocab_size <= 2^24");
     if (c->seq_len > (1 << 20)) return bad("seq_len <= 2^20");
     if (c->max_batch > 1024) return bad("max_batch <= 1024");
+    if (c->max_prefill < 0 || c->max_prefill > 1024) return bad("0 <= max_prefill <= 1024");
     if (!(c->norm_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("norm_eps >= 0 and rope_theta > 0");
     if (c->shared_classifier != 0 && c->shared_classifier != 1) return bad("shared_classifier is 0 or 1");
     return true;
@@ -264,7 +267,7 @@ enum BKind : int {
 // Launches one kernel of a batched step for layer l on M rows. For BK_NORM the
 // gain is g_ffn[l] (gain_next == false) or the next layer's g_att / g_final.
 cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mode, int steps,
-                         bool want_logits, bool gain_next, cudaStream_t s) {
+                         bool want_logits, bool gain_next, cudaStream_t s, bool prefill = false) {
     const l2_config& c = h->cfg;
     const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
     GemmArgs g{};
@@ -302,6 +305,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.rope = h->rope;
             g.pos = h->b_pos;
             g.active = h->b_active;
+            g.seq = prefill ? h->b_seq : nullptr;
             g.d = d;
             g.kvd = h->kvd;
             g.head_dim = h->hd;
@@ -318,6 +322,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             t.att_lo = h->att_lo;
             t.pos = h->b_pos;
             t.active = h->b_active;
+            t.seq = prefill ? h->b_seq : nullptr;
             t.d = d;
             t.n_heads = c.n_heads;
             t.n_kv_heads = c.n_kv_heads;
@@ -378,19 +383,53 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
 // + RMSNorm, then per layer the QKV GEMM (RoPE + KV append), attention, Wo
 // GEMM + residual, RMSNorm, W1/W3 GEMM + SwiGLU, W2 GEMM + residual, RMSNorm;
 // the classifier GEMM with the per-row argmax; and the per-sequence advance.
+// `prefill`: every row is a position of sequence 0 (cache 0, row positions
+// in b_pos) instead of a sequence of its own.
 cudaError_t enqueue_rows(l2_handle* h, int row0, int M, int mode, int steps, bool want_logits,
-                         cudaStream_t s) {
-    cudaError_t e = launch_bkind(h, BK_NORM_EMB, 0, row0, M, mode, steps, want_logits, false, s);
+                         cudaStream_t s, bool prefill = false) {
+    cudaError_t e =
+        launch_bkind(h, BK_NORM_EMB, 0, row0, M, mode, steps, want_logits, false, s, prefill);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
         const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_NORM, BK_W13, BK_W2, BK_NORM};
         for (int i = 0; i < 7 && e == cudaSuccess; ++i)
-            e = launch_bkind(h, seq[i], l, row0, M, mode, steps, want_logits, i == 6, s);
+            e = launch_bkind(h, seq[i], l, row0, M, mode, steps, want_logits, i == 6, s, prefill);
     }
     if (e == cudaSuccess)
-        e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, false, s);
+        e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, false, s, prefill);
     if (e == cudaSuccess)
-        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, false, s);
+        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, false, s, prefill);
     return e;
+}
+
+// Prefill rows [0, n): token tokens[r] at position pos0 + r of cache 0.
+__global__ void prefill_setup_kernel(int n, int pos0, const int* tokens, int vocab, int* b_token,
+                                     int* b_pos, int* b_seq, int* b_active,
+                                     unsigned long long* keys, L2State* st) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r == 0) st->err = 0;
+    if (r >= n) return;
+    b_token[r] = min(max(tokens[r], 0), vocab - 1);
+    b_pos[r] = pos0 + r;
+    b_seq[r] = 0;
+    b_active[r] = 1;
+    keys[r] = 0ull;
+}
+
+// After a prefill of positions 0..n-1: the argmax of position n-1 is the first
+// generated token; the batch-1 decode state continues at position n.
+__global__ void prefill_handoff_kernel(L2State* st, const int* last, int n, const int* prompt,
+                                       int* out) {
+    const int idx = last[n - 1];
+    out[0] = idx;
+    st->pos = n;
+    st->token = idx;
+    st->n_prompt = n;
+    st->mode = 1;
+    st->prompt = prompt;
+    st->out_tokens = out;
+    st->last_argmax = idx;
+    st->argmax_key = 0ull;
+    st->cls_done = 0u;
 }
 
 // One lockstep step of M sequences (rows [0, M)) on stream s.
@@ -432,7 +471,8 @@ int setup_batched(l2_handle* h) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size, S = c.seq_len;
     const size_t kvd = h->kvd, B = c.max_batch;
-    h->mcap = static_cast<int>((B + 127) / 128 * 128);
+    const size_t RW = static_cast<size_t>(h->rows);  // row capacity (>= B)
+    h->mcap = static_cast<int>((RW + 127) / 128 * 128);
     const size_t Mc = h->mcap;
     size_t off = 0;
     auto take = [&](size_t n) {
@@ -462,7 +502,7 @@ int setup_batched(l2_handle* h) {
     off = 0;
     const size_t o_x = take(Mc * d), o_nh = take(Mc * d), o_nl = take(Mc * d), o_q = take(Mc * d);
     const size_t o_ah = take(Mc * d), o_al = take(Mc * d), o_hh = take(Mc * F), o_hl = take(Mc * F);
-    const size_t o_lg = take(B * V);
+    const size_t o_lg = take(RW * V);
     L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
     L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));
     h->bx = h->bact + o_x; h->xn_hi = h->bact + o_nh; h->xn_lo = h->bact + o_nl;
@@ -472,15 +512,16 @@ int setup_batched(l2_handle* h) {
     off = 0;
     const size_t o_pos = take(Mc), o_tok = take(Mc), o_act = take(Mc), o_len = take(Mc);
     const size_t o_poff = take(Mc), o_last = take(Mc), o_pr = take(B * S), o_out = take(B * S);
-    const size_t o_keys = take(2 * Mc);
+    const size_t o_seq = take(Mc), o_keys = take(2 * Mc);
     L2_CUDA(h, cudaMalloc(&h->bst, off * sizeof(int)));
     L2_CUDA(h, cudaMemsetAsync(h->bst, 0, off * sizeof(int), s));
     h->b_pos = h->bst + o_pos; h->b_token = h->bst + o_tok; h->b_active = h->bst + o_act;
     h->b_len = h->bst + o_len; h->b_poff = h->bst + o_poff; h->b_last = h->bst + o_last;
     h->b_prompts = h->bst + o_pr; h->b_out = h->bst + o_out;
+    h->b_seq = h->bst + o_seq;
     h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
 
-    const int Mb = static_cast<int>(B);
+    const int Mb = static_cast<int>(RW);
     h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
     h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d));
     h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d));
@@ -773,7 +814,8 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
         if (pinned) cudaHostUnregister(const_cast<float*>(blob));
     }
     if (rc != L2_OK) return bail(rc);
-    if (c.max_batch > 1 && (rc = setup_batched(h)) != L2_OK) return bail(rc);
+    h->rows = c.max_batch > c.max_prefill ? c.max_batch : c.max_prefill;
+    if (h->rows > 1 && (rc = setup_batched(h)) != L2_OK) return bail(rc);
 
     if ((rc = capture(h, 1, &h->fwd1)) != L2_OK) return bail(rc);
     if ((rc = capture(h, kGraphBatch, &h->fwdN)) != L2_OK) return bail(rc);
@@ -969,6 +1011,83 @@ static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32
     if (on_device) return L2_OK;
     L2_CUDA(h, cudaStreamSynchronize(s));
     return check_device_error(h);
+}
+
+// Queues prefill rows [0, n) of cache 0 at positions pos0.. (tokens: device).
+static int enqueue_prefill(l2_handle* h, const int32_t* d_tokens, int32_t n, int32_t pos0,
+                           bool want_logits, cudaStream_t s) {
+    prefill_setup_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, pos0, d_tokens, h->cfg.vocab_size,
+                                                         h->b_token, h->b_pos, h->b_seq,
+                                                         h->b_active, h->b_keys, h->st);
+    L2_CUDA(h, cudaGetLastError());
+    L2_CUDA(h, enqueue_rows(h, 0, n, 0, 0, want_logits, s, true));
+    return L2_OK;
+}
+
+static int prefill_checks(l2_handle* h, int32_t n, int32_t pos0) {
+    if (h->rows < 2) return fail(h, L2_EINVAL, "handle has no prefill path (max_prefill and max_batch <= 1)");
+    if (n < 1 || n > h->rows) return fail(h, L2_EINVAL, "prefill length outside [1, max(max_batch, max_prefill)]");
+    if (pos0 < 0 || static_cast<long long>(pos0) + n > h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "prefill positions outside [0, seq_len)");
+    return L2_OK;
+}
+
+int l2_prefill(l2_handle* h, const int32_t* tokens, int32_t n, int32_t pos0, float* logits_out) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!tokens) return fail(h, L2_EINVAL, "NULL tokens");
+    int rc = prefill_checks(h, n, pos0);
+    if (rc != L2_OK) return rc;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
+    cudaStream_t s = h->stream;
+    L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, tokens, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s));
+    if ((rc = enqueue_prefill(h, h->d_prompt, n, pos0, logits_out != nullptr, s)) != L2_OK) return rc;
+    if (logits_out)
+        L2_CUDA(h, cudaMemcpyAsync(logits_out, h->blogits,
+                                   sizeof(float) * n * static_cast<size_t>(h->cfg.vocab_size),
+                                   cudaMemcpyDeviceToHost, s));
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return check_device_error(h);
+}
+
+static int generate_prefill_impl(l2_handle* h, const int32_t* prompt, int32_t n_prompt,
+                                 int32_t steps, int32_t* out, bool on_device, cudaStream_t stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!prompt || !out) return fail(h, L2_EINVAL, "NULL prompt or output");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    int rc = prefill_checks(h, n_prompt, 0);
+    if (rc != L2_OK) return rc;
+    cudaStream_t s = on_device ? stream : h->stream;
+    const int32_t* d_prompt = prompt;
+    int32_t* d_out = on_device ? out : h->d_out;
+    if (!on_device) {
+        for (int i = 0; i < n_prompt; ++i)
+            if (prompt[i] < 0 || prompt[i] >= h->cfg.vocab_size)
+                return fail(h, L2_EINVAL, "prompt id out of range");
+        L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, prompt, sizeof(int32_t) * n_prompt,
+                                   cudaMemcpyHostToDevice, s));
+        d_prompt = h->d_prompt;
+    }
+    if ((rc = enqueue_prefill(h, d_prompt, n_prompt, 0, false, s)) != L2_OK) return rc;
+    prefill_handoff_kernel<<<1, 1, 0, s>>>(h->st, h->b_last, n_prompt, d_prompt, d_out);
+    L2_CUDA(h, cudaGetLastError());
+    if ((rc = run_forwards(h, steps - 1, s)) != L2_OK) return rc;
+    if (on_device) return L2_OK;
+    L2_CUDA(h, cudaMemcpyAsync(out, h->d_out, sizeof(int32_t) * steps, cudaMemcpyDeviceToHost, s));
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return check_device_error(h);
+}
+
+int l2_generate_prefill(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
+                        int32_t* out_tokens) {
+    return generate_prefill_impl(h, prompt, n_prompt, steps, out_tokens, false, nullptr);
+}
+
+int l2_generate_prefill_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
+                               int32_t steps, int32_t* d_out, void* stream) {
+    return generate_prefill_impl(h, d_prompt, n_prompt, steps, d_out, true,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,

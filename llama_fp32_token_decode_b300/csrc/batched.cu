@@ -5,9 +5,10 @@
 // the 3xTF32 tensor-core GEMM (gemm_tf32x3.cu); this file holds
 //   brmsnorm_kernel   optional embedding gather + RMSNorm, writing the
 //                     normalised rows as tf32 (hi, lo) pairs for the next GEMM
-//   battn_kernel      causal attention of every (sequence, head) over that
-//                     sequence's own cache, ragged lengths pos_b + 1, output
-//                     as a tf32 pair for the Wo GEMM
+//   battn_kernel      causal attention of every (row, head) over the row's KV
+//                     cache (its own sequence's; in a prefill every row is a
+//                     position of one sequence), ragged lengths pos + 1,
+//                     output as a tf32 pair for the Wo GEMM
 //   badvance_kernel   greedy choice per sequence and the move to the next
 //                     position (prompt tokens are forced, then the argmax).
 #include <math.h>
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_kernel(const BAttnArgs a)
     const int kvh = h / (a.n_heads / a.n_kv_heads);
     const int n = min(max(__ldcg(a.pos + b), 0), a.seq_len - 1) + 1;
     const float* qrow = a.q + static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
-    const size_t head_off = static_cast<size_t>(b) * a.cache_seq +
+    const size_t head_off = static_cast<size_t>(a.seq ? __ldcg(a.seq + b) : b) * a.cache_seq +
                             static_cast<size_t>(kvh) * a.seq_len * hd;
     const float* Kh = a.k_cache + head_off;
     const float* Vh = a.v_cache + head_off;
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kBAttnThreads, MINB) battn4_kernel(const BAttn
     const bool lane_on = c4 < hd4;
     const int kvh = h / (a.n_heads / a.n_kv_heads);
     const int n = min(max(__ldcg(a.pos + b), 0), a.seq_len - 1) + 1;
-    const size_t head_off = static_cast<size_t>(b) * a.cache_seq +
+    const size_t head_off = static_cast<size_t>(a.seq ? __ldcg(a.seq + b) : b) * a.cache_seq +
                             static_cast<size_t>(kvh) * a.seq_len * hd;
     const float4* K4 = reinterpret_cast<const float4*>(a.k_cache + head_off);
     const float4* V4 = reinterpret_cast<const float4*>(a.v_cache + head_off);

@@ -237,13 +237,13 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
             } else if (c < g.d + g.kvd) {
                 const int jj = c - g.d, kvh = jj / hd, e = jj % hd;
                 const float2 cs = rope[e >> 1];
-                float* dst = g.k_cache + static_cast<size_t>(r) * g.cache_seq +
+                float* dst = g.k_cache + static_cast<size_t>(g.seq ? __ldcg(g.seq + r) : r) * g.cache_seq +
                              (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
                 dst[1] = x0 * cs.y + x1 * cs.x;
             } else {
                 const int jj = c - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
-                float* dst = g.v_cache + static_cast<size_t>(r) * g.cache_seq +
+                float* dst = g.v_cache + static_cast<size_t>(g.seq ? __ldcg(g.seq + r) : r) * g.cache_seq +
                              (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
                 dst[0] = x0;
                 dst[1] = x1;

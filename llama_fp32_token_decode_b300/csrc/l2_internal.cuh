@@ -120,6 +120,7 @@ struct GemmArgs {
     const float2* rope;   // [S][hd/2]
     const int* pos;       // [M] position of each row
     const int* active;    // [M] 0 = finished sequence (no KV write) or null
+    const int* seq;       // [M] KV cache of each row, or null (row r uses cache r)
     int d, kvd, head_dim, seq_len;
     size_t cache_seq;     // floats of one sequence's cache (all layers)
     unsigned long long* argmax_keys;  // ARGMAX: [M]
@@ -149,6 +150,7 @@ struct BAttnArgs {
     float* att_lo;
     const int* pos;        // [M]
     const int* active;     // [M] or null
+    const int* seq;        // [M] KV cache of each row, or null (row b uses cache b)
     int d, n_heads, n_kv_heads, head_dim, seq_len;
     size_t cache_seq;
 };
