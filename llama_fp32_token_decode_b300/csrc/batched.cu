@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kNormThreads) brmsnorm_kernel(const BNormArgs 
         const float n2 = g.z * (inv * v.z), n3 = g.w * (inv * v.w);
         const float4 h = make_float4(tf32_round(n0), tf32_round(n1), tf32_round(n2), tf32_round(n3));
         hi4[i] = h;
-        lo4[i] = make_float4(n0 - h.x, n1 - h.y, n2 - h.z, n3 - h.w);
+        lo4[i] = make_float4(tf32_round(n0 - h.x), tf32_round(n1 - h.y), tf32_round(n2 - h.z),
+                             tf32_round(n3 - h.w));
     }
 }
 
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_kernel(const BAttnArgs a)
         const float v = acc / L;
         const float hi = tf32_round(v);
         ohi[e] = hi;
-        olo[e] = v - hi;
+        olo[e] = tf32_round(v - hi);
     }
 }
 
@@ -285,7 +286,8 @@ __global__ void __launch_bounds__(kBAttnThreads, MINB) battn4_kernel(const BAttn
         const size_t off = static_cast<size_t>(b) * a.d + static_cast<size_t>(h) * hd;
         reinterpret_cast<float4*>(a.att_hi + off)[tid] = hi;
         reinterpret_cast<float4*>(a.att_lo + off)[tid] =
-            make_float4(r.x - hi.x, r.y - hi.y, r.z - hi.z, r.w - hi.w);
+            make_float4(tf32_round(r.x - hi.x), tf32_round(r.y - hi.y), tf32_round(r.z - hi.z),
+                        tf32_round(r.w - hi.w));
     }
 }
 

@@ -134,7 +134,7 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int STAGES = (BN == 128) ? 3 : 4;  // deepest ring that fits
-    static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators (chunk drain)
     static constexpr int PS = BN + 4;  // row stride (floats) of a staged partial tile
     // split-K receive buffer: one slot per peer, ceil(128 / S) rows of PS floats
     __host__ __device__ static constexpr size_t recv_bytes(int ksplit) {
@@ -217,7 +217,7 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
                 const float hi = tf32_round(h);
                 const size_t idx = static_cast<size_t>(r) * F + ((gc + j) >> 1);
                 g.out_hi[idx] = hi;
-                g.out_lo[idx] = h - hi;
+                g.out_lo[idx] = tf32_round(h - hi);
             }
         }
     } else if constexpr (EPI == GEPI_QKV_ROPE) {
@@ -269,13 +269,38 @@ __device__ __forceinline__ void row_state(const GemmArgs& g, int r, int& pos, in
 
 // Grid (S, tiles): blockIdx.x is the K split (the CTA's rank in a cluster of S
 // CTAs that share one 128 x BN output tile), blockIdx.y the tile (M tiles of
-// one N tile adjacent). S == 1: the epilogue reads the accumulator straight
-// from TMEM (thread = row). S > 1: every CTA stages its partial tile in its own
-// shared memory; after a cluster barrier CTA s adds rows
-// [128 s / S, 128 (s+1) / S) of all S partials in rank order (a fixed order:
-// the result does not depend on timing) and applies the epilogue to them.
-template <int BN, int EPI>
-__global__ void __launch_bounds__(128, 1)
+// one N tile adjacent). Warps 0-3 own TMEM lane quarters 0-3 (tile rows
+// 32w..32w+31) and run the epilogue. Without the chunk drain (four warps)
+// warp 0 lane 0 issues TMA and warp 1 lane 0 the MMAs before joining the
+// epilogue; with it (six warps) warps 0-3 drain chunks during the mainloop,
+// so TMA and MMA issue move to warps 4 and 5.
+//
+// Accumulation precision: the tensor core adds into its fp32 accumulator
+// without round-to-nearest. Measured against float64 (M 64, N 512): letting
+// one accumulator absorb all of K gives a relative L2 error that grows with K
+// and is biased toward zero (7.7e-5 at K = 11008, 2.3e-4 at 32768; a
+// sequential fp32 loop gives 1.9e-6 and 3.3e-6), while the error of a chunk
+// of c K-blocks is about 2.3e-7 * c whatever K is. So the MMAs of every
+// kChunk K-blocks go into one of two TMEM accumulators in turn, and warps 0-3
+// drain each finished chunk into registers with ordinary fp32 additions while
+// the next chunk accumulates in the other buffer (accfull / accfree
+// barriers): about 5e-7 at any K.
+//
+// S == 1: the epilogue runs on the register sums (thread = row). S > 1: every
+// CTA stages its partial tile in its own shared memory and pushes each peer's
+// row slice into that peer's receive buffer (bulk copy, completion on the
+// peer's mbarrier); CTA s adds rows [128 s / S, 128 (s+1) / S) of the S
+// partials in rank order (a fixed order: the result does not depend on
+// timing) and applies the epilogue to them.
+constexpr int gemm_threads(bool drain) { return drain ? 192 : 128; }
+constexpr int kChunk = 2;         // K-blocks per TMEM accumulation chunk (DRAIN)
+constexpr int kDrainAbove = 16;   // a CTA with more K-blocks than this drains chunks
+
+// DRAIN == false (a CTA's K range is at most kDrainAbove K-blocks, error below
+// about 4e-6): one accumulator takes the whole range and the epilogue reads it
+// from TMEM 32 columns at a time, without a register copy of the tile row.
+template <int BN, int EPI, bool DRAIN>
+__global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mA_hi,
                        const __grid_constant__ CUtensorMap mA_lo,
                        const __grid_constant__ CUtensorMap mB_hi,
@@ -292,8 +317,9 @@ __global__ void __launch_bounds__(128, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * C::STAGE +
                                                  C::recv_bytes(nsplit));
     uint64_t* empty = full + S;
-    uint64_t* accb = empty + S;
-    uint64_t* recvb = accb + 1;  // split-K: the peers' slices of this CTA's rows
+    uint64_t* accfull = empty + S;   // [2] chunk accumulated in TMEM buffer b
+    uint64_t* accfree = accfull + 2; // [2] TMEM buffer b drained
+    uint64_t* recvb = accfree + 2;   // split-K: the peers' slices of this CTA's rows
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
     __shared__ int s_err;
 
@@ -305,13 +331,18 @@ __global__ void __launch_bounds__(128, 1)
     const int KB = (g.K + 31) / 32;
     const int kb0 = KB * split / nsplit, kb1 = KB * (split + 1) / nsplit;
     const int NK = kb1 - kb0;
+    constexpr int CH = DRAIN ? kChunk : (1 << 30);   // K-blocks per accumulation chunk
+    const int NCH = DRAIN ? (NK + CH - 1) / CH : 1;  // chunks (the last drains in the epilogue)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accb, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accfree[b], 4);
+        }
         mbar_init(recvb, 1);
         fence_mbar_init();
         s_err = 0;
@@ -338,74 +369,116 @@ __global__ void __launch_bounds__(128, 1)
     auto b_hi = [&](int s) { return a_hi(s) + 2 * C::A_BYTES; };
     auto b_lo = [&](int s) { return b_hi(s) + C::B_BYTES; };
 
-    if (warp == 0 && lane == 0) {
-        // ---- producer: local K-block i is global K-block kb0 + i
-        const int pre = NK < S ? NK : S;
-        for (int i = 0; i < pre; ++i) {
-            const int kc = (kb0 + i) * 32;
-            mbar_arrive_expect_tx(&full[i], C::STAGE);
-            tma_load_3d(b_hi(i), &mB_hi, kc, n0, g.layer, &full[i]);
-            tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
-        }
-        pdl_wait();  // activations come from the previous kernel
-        for (int i = 0; i < pre; ++i) {
-            const int kc = (kb0 + i) * 32;
-            tma_load_3d(a_hi(i), &mA_hi, kc, m0, 0, &full[i]);
-            tma_load_3d(a_lo(i), &mA_lo, kc, m0, 0, &full[i]);
-        }
-        int issued = pre;
-        for (int i = pre; i < NK; ++i) {
-            const int s = i % S, kc = (kb0 + i) * 32;
-            if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / S - 1) & 1u)) {
-                s_err = 1;
-                break;
+    float R[DRAIN ? BN : 1];  // DRAIN, warps 0-3: this thread's row, summed over chunks
+#pragma unroll
+    for (int j = 0; j < (DRAIN ? BN : 1); ++j) R[j] = 0.0f;
+
+    constexpr int kProdWarp = DRAIN ? 4 : 0, kMmaWarp = DRAIN ? 5 : 1;
+    if (warp == kProdWarp && (DRAIN || lane == 0)) {
+        if (lane == 0) {
+            // ---- producer: local K-block i is global K-block kb0 + i
+            const int pre = NK < S ? NK : S;
+            for (int i = 0; i < pre; ++i) {
+                const int kc = (kb0 + i) * 32;
+                mbar_arrive_expect_tx(&full[i], C::STAGE);
+                tma_load_3d(b_hi(i), &mB_hi, kc, n0, g.layer, &full[i]);
+                tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
             }
-            mbar_arrive_expect_tx(&full[s], C::STAGE);
-            tma_load_3d(b_hi(s), &mB_hi, kc, n0, g.layer, &full[s]);
-            tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
-            tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
-            tma_load_3d(a_lo(s), &mA_lo, kc, m0, 0, &full[s]);
-            issued = i + 1;
+            pdl_wait();  // activations come from the previous kernel
+            for (int i = 0; i < pre; ++i) {
+                const int kc = (kb0 + i) * 32;
+                tma_load_3d(a_hi(i), &mA_hi, kc, m0, 0, &full[i]);
+                tma_load_3d(a_lo(i), &mA_lo, kc, m0, 0, &full[i]);
+            }
+            int issued = pre;
+            for (int i = pre; i < NK; ++i) {
+                const int s = i % S, kc = (kb0 + i) * 32;
+                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / S - 1) & 1u)) {
+                    s_err = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], C::STAGE);
+                tma_load_3d(b_hi(s), &mB_hi, kc, n0, g.layer, &full[s]);
+                tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
+                tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
+                tma_load_3d(a_lo(s), &mA_lo, kc, m0, 0, &full[s]);
+                issued = i + 1;
+            }
+            if (s_err) {  // let the copies in flight land before the CTA leaves
+                for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
+                    mbar_wait_bounded(&full[q % S], static_cast<uint32_t>(q / S) & 1u);
+            }
         }
-        if (s_err) {  // let the copies in flight land before the CTA leaves
-            for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
-                mbar_wait_bounded(&full[q % S], static_cast<uint32_t>(q / S) & 1u);
+    } else if (warp == kMmaWarp && (DRAIN || lane == 0)) {
+        if (lane == 0) {
+            // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1
+            constexpr uint32_t idesc = idesc_tf32(128, BN);
+            for (int i = 0; i < NK; ++i) {
+                const int c = i / CH, w = i % CH, buf = c & 1;
+                if (w == 0 && c >= 2 &&
+                    !mbar_wait_bounded(&accfree[buf], static_cast<uint32_t>(c / 2 - 1) & 1u)) {
+                    s_err = 1;
+                    break;
+                }
+                const int s = i % S;
+                if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
+                    s_err = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = tmem + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t ah = sw128_desc(a_hi(s) + 32 * k);
+                    const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
+                    const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
+                    const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
+                    mma_tf32(acc, al, bh, idesc, (w | k) != 0);
+                    mma_tf32(acc, ah, bl, idesc, 1u);
+                    mma_tf32(acc, ah, bh, idesc, 1u);
+                }
+                mma_commit(&empty[s]);
+                if (w == CH - 1 || i == NK - 1) mma_commit(&accfull[buf]);
+            }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        constexpr uint32_t idesc = idesc_tf32(128, BN);
-        for (int i = 0; i < NK; ++i) {
-            const int s = i % S;
-            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
+    } else if constexpr (!DRAIN) {
+        // the other lanes wait below for the single accumulator
+    } else {
+        // ---- warps 0-3: drain every chunk into registers (fp32 round-to-nearest adds)
+        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        for (int c = 0; c < NCH; ++c) {
+            const int buf = c & 1;
+            if (!mbar_wait_bounded(&accfull[buf], static_cast<uint32_t>(c / 2) & 1u)) {
                 s_err = 1;
                 break;
             }
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t ah = sw128_desc(a_hi(s) + 32 * k);
-                const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
-                const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
-                const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
-                mma_tf32(tmem, al, bh, idesc, (i | k) != 0);
-                mma_tf32(tmem, ah, bl, idesc, 1u);
-                mma_tf32(tmem, ah, bh, idesc, 1u);
+            for (int j = 0; j < BN / 32; ++j) {
+                float v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective
+                tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * BN + 32 * j), v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) R[32 * j + t] += v[t];
             }
-            mma_commit(&empty[s]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accfree[buf]);
         }
-        mma_commit(accb);  // completes once every MMA issued above has
     }
     __syncwarp();
+    if constexpr (!DRAIN) {
+        // ---- all four warps: wait for the single accumulator (read in the epilogue)
+        if (NK > 0 && !mbar_wait_bounded(&accfull[0], 0u)) s_err = 1;
+        tc_fence_after();
+    }
+    __syncthreads();  // mainloop and drain done; s_err settled
+    const int row = 32 * warp + lane;  // warps 0-3: this thread's tile row
 
-    // ---- epilogue
-    if (!mbar_wait_bounded(accb, 0u)) s_err = 1;
-    tc_fence_after();
-    __syncthreads();
-    const int row = 32 * warp + lane;  // this thread's TMEM lane = tile row
     if (nsplit == 1) {
         if (s_err) {
             if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
-        } else {
+        } else if (warp < 4) {
             const int r = m0 + row;
             const bool row_ok = r < m_end;
             int pos = 0, active = 1;
@@ -413,17 +486,30 @@ __global__ void __launch_bounds__(128, 1)
                 if (row_ok) row_state(g, r, pos, active);
             }
             unsigned long long best = 0ull;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                float v[32];
-                __syncwarp();  // tcgen05.ld is warp-collective
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
-                const int gc0 = n0 + 32 * c;
-                if (!row_ok || gc0 >= g.N) continue;
+            if constexpr (DRAIN) {
+                if (row_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
-                    if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, pos, active, best);
+                    for (int j = 0; j < BN; j += 4) {
+                        const int gc = n0 + j;
+                        if (gc < g.N) {
+                            const float a4[4] = {R[j], R[j + 1], R[j + 2], R[j + 3]};
+                            epi4<EPI>(g, r, gc, a4, pos, active, best);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+                    const int gc0 = n0 + 32 * c;
+                    if (!row_ok || gc0 >= g.N) continue;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
+                        if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, pos, active, best);
+                    }
                 }
             }
             if constexpr (EPI == GEPI_ARGMAX) {
@@ -433,24 +519,33 @@ __global__ void __launch_bounds__(128, 1)
     } else {
         // stage this CTA's partial tile (row-major, stride PS) in the ring
         float* P = reinterpret_cast<float*>(gbase);
+        if (warp < 4) {
+            if constexpr (DRAIN) {
+#pragma unroll
+                for (int j = 0; j < BN; j += 4)
+                    *reinterpret_cast<float4*>(P + row * PS + j) =
+                        make_float4(R[j], R[j + 1], R[j + 2], R[j + 3]);
+            } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            __syncwarp();
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
-            if (NK == 0) {
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+                    if (NK == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(P + row * PS + 32 * c + j) =
+                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
             }
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(P + row * PS + 32 * c + j) =
-                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncthreads();
         cluster_wait_acquire();  // every peer's barriers are initialised
-        const int R = (128 + nsplit - 1) / nsplit;  // rows of a receive slot
+        const int R_ = (128 + nsplit - 1) / nsplit;  // rows of a receive slot
         const int r0 = 128 * split / nsplit, r1 = 128 * (split + 1) / nsplit;
         const uint32_t pbase = smem_u32(P);
         if (threadIdx.x == 0) {
@@ -460,78 +555,82 @@ __global__ void __launch_bounds__(128, 1)
                 if (q == split) continue;
                 const int q0 = 128 * q / nsplit, q1 = 128 * (q + 1) / nsplit;
                 const int slot = split < q ? split : split - 1;  // slot of this sender at q
-                bulk_s2peer(map_peer(recv_base + static_cast<uint32_t>(slot * R * PS * 4), q),
+                bulk_s2peer(map_peer(recv_base + static_cast<uint32_t>(slot * R_ * PS * 4), q),
                             pbase + static_cast<uint32_t>(q0 * PS * 4),
                             static_cast<uint32_t>((q1 - q0) * PS * 4), map_peer(smem_u32(recvb), q));
             }
         }
-        const int gpr = BN / 4;  // float4 groups per row
-        // residual: this thread's first rows of x are loaded while the slices travel
-        constexpr int kPre = 4;
-        float4 xpre[kPre];
-        if constexpr (EPI == GEPI_RESIDUAL) {
+        if (warp < 4) {
+            const int gpr = BN / 4;  // float4 groups per row
+            // residual: this thread's first rows of x are loaded while the slices travel
+            constexpr int kPre = 4;
+            float4 xpre[kPre];
 #pragma unroll
             for (int u = 0; u < kPre; ++u) {
-                const int t = threadIdx.x + 128 * u;
-                const int lr = r0 + t / gpr, gc = n0 + 4 * (t % gpr);
-                const int r = m0 + lr;
-                xpre[u] = (t < (r1 - r0) * gpr && r < m_end && gc + 4 <= g.N && (g.ldc & 3) == 0)
-                              ? __ldcg(reinterpret_cast<const float4*>(
-                                    g.out + static_cast<size_t>(r) * g.ldc + gc))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                xpre[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (EPI == GEPI_RESIDUAL) {
+                    const int t = threadIdx.x + 128 * u;
+                    const int lr = r0 + t / gpr, gc = n0 + 4 * (t % gpr);
+                    const int r = m0 + lr;
+                    if (t < (r1 - r0) * gpr && r < m_end && gc + 4 <= g.N && (g.ldc & 3) == 0)
+                        xpre[u] = __ldcg(reinterpret_cast<const float4*>(
+                            g.out + static_cast<size_t>(r) * g.ldc + gc));
+                }
             }
-        }
-        const bool got = mbar_wait_bounded(recvb, 0u);
-        if (!got) s_err = 1;
-        if (!s_err) {
-            const float* recv = reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
-            const int ngroups = (r1 - r0) * gpr;
-            // group t: row r0 + t / gpr, columns 4 (t % gpr) .. + 3 of the tile; the
-            // partials are added in rank order (a fixed order, whoever arrived first)
-            auto group = [&](int t, bool have_x, float4 x) {
-                const int lr = r0 + t / gpr, c4 = t % gpr;
-                const int r = m0 + lr, gc = n0 + 4 * c4;
-                if (r >= m_end || gc >= g.N) return;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int q = 0; q < nsplit; ++q) {
-                    const float* src = (q == split)
-                        ? P + lr * PS
-                        : recv + static_cast<size_t>((q < split ? q : q - 1) * R + (lr - r0)) * PS;
-                    const float4 v = *reinterpret_cast<const float4*>(src + 4 * c4);
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-                if (have_x) {  // residual with its row already loaded
-                    *reinterpret_cast<float4*>(g.out + static_cast<size_t>(r) * g.ldc + gc) =
-                        make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
-                    return;
-                }
-                int pos = 0, active = 1;
-                if constexpr (EPI == GEPI_QKV_ROPE) row_state(g, r, pos, active);
-                unsigned long long best = 0ull;
-                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-                epi4<EPI>(g, r, gc, a4, pos, active, best);
-                if constexpr (EPI == GEPI_ARGMAX) {
-                    if (best != 0ull) atomicMax(g.argmax_keys + r, best);
-                }
-            };
+            const bool got = mbar_wait_bounded(recvb, 0u);
+            if (!got) s_err = 1;
+            if (!s_err) {
+                const float* recv =
+                    reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
+                const int ngroups = (r1 - r0) * gpr;
+                // group t: row r0 + t / gpr, columns 4 (t % gpr) .. + 3 of the tile; the
+                // partials are added in rank order (a fixed order, whoever arrived first)
+                auto group = [&](int t, bool have_x, float4 x) {
+                    const int lr = r0 + t / gpr, c4 = t % gpr;
+                    const int r = m0 + lr, gc = n0 + 4 * c4;
+                    if (r >= m_end || gc >= g.N) return;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < nsplit; ++q) {
+                        const float* src =
+                            (q == split) ? P + lr * PS
+                                         : recv + static_cast<size_t>((q < split ? q : q - 1) * R_ +
+                                                                      (lr - r0)) * PS;
+                        const float4 v = *reinterpret_cast<const float4*>(src + 4 * c4);
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                        acc.w += v.w;
+                    }
+                    if (have_x) {  // residual with its row already loaded
+                        *reinterpret_cast<float4*>(g.out + static_cast<size_t>(r) * g.ldc + gc) =
+                            make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
+                        return;
+                    }
+                    int pos = 0, active = 1;
+                    if constexpr (EPI == GEPI_QKV_ROPE) row_state(g, r, pos, active);
+                    unsigned long long best = 0ull;
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                    epi4<EPI>(g, r, gc, a4, pos, active, best);
+                    if constexpr (EPI == GEPI_ARGMAX) {
+                        if (best != 0ull) atomicMax(g.argmax_keys + r, best);
+                    }
+                };
 #pragma unroll
-            for (int u = 0; u < kPre; ++u) {
-                const int t = threadIdx.x + 128 * u;
-                if (t < ngroups) {
-                    const int gc = n0 + 4 * (t % gpr);
-                    const bool hx = (EPI == GEPI_RESIDUAL) && gc + 4 <= g.N && (g.ldc & 3) == 0;
-                    group(t, hx, xpre[u]);
+                for (int u = 0; u < kPre; ++u) {
+                    const int t = threadIdx.x + 128 * u;
+                    if (t < ngroups) {
+                        const int gc = n0 + 4 * (t % gpr);
+                        const bool hx = (EPI == GEPI_RESIDUAL) && gc + 4 <= g.N && (g.ldc & 3) == 0;
+                        group(t, hx, xpre[u]);
+                    }
                 }
+                for (int t = threadIdx.x + 128 * kPre; t < ngroups; t += 128)
+                    group(t, false, make_float4(0.f, 0.f, 0.f, 0.f));
+            } else if (threadIdx.x == 0) {
+                atomicOr(g.err, ERR_TIMEOUT_TMA);
             }
-            for (int t = threadIdx.x + 128 * kPre; t < ngroups; t += 128)
-                group(t, false, make_float4(0.f, 0.f, 0.f, 0.f));
-        } else if (threadIdx.x == 0) {
-            atomicOr(g.err, ERR_TIMEOUT_TMA);
+            if (threadIdx.x == 0) bulk_commit_and_wait_read();  // this CTA's pushes have read P
         }
-        if (threadIdx.x == 0) bulk_commit_and_wait_read();  // this CTA's pushes have read P
     }
 
     // ---- teardown: every tcgen05 access of this CTA is complete
@@ -551,7 +650,9 @@ __global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restri
         h.z = tf32_round(v.z);
         h.w = tf32_round(v.w);
         hi[i] = h;
-        lo[i] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+        // lo rounded to tf32 as well: the tensor core would otherwise truncate it
+        lo[i] = make_float4(tf32_round(v.x - h.x), tf32_round(v.y - h.y), tf32_round(v.z - h.z),
+                            tf32_round(v.w - h.w));
     }
 }
 
@@ -578,13 +679,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool DRAIN>
 cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStream_t s, bool pdl) {
     using C = Cfg<BN>;
     cudaLaunchConfig_t cfg{};
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(ksplit, mt * nt);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(gemm_threads(DRAIN));
     cfg.dynamicSmemBytes = C::smem_for(g.stages, ksplit);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -596,13 +697,17 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI>, m.a_hi, m.a_lo, m.b_hi, m.b_lo,
-                              g);
+    return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI, DRAIN>, m.a_hi, m.a_lo, m.b_hi,
+                              m.b_lo, g);
 }
 
 template <int BN, int EPI>
 cudaError_t set_smem() {
-    return cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxDynSmem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kMaxDynSmem));
 }
@@ -617,17 +722,27 @@ cudaError_t set_smem_bn() {
     return set_smem<BN, GEPI_ARGMAX>();
 }
 
+template <int BN, bool DRAIN>
+cudaError_t launch_bd(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cudaStream_t s,
+                      bool pdl) {
+    switch (epi) {
+        case GEPI_STORE: return launch_t<BN, GEPI_STORE, DRAIN>(m, g, ks, s, pdl);
+        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL, DRAIN>(m, g, ks, s, pdl);
+        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU, DRAIN>(m, g, ks, s, pdl);
+        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE, DRAIN>(m, g, ks, s, pdl);
+        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX, DRAIN>(m, g, ks, s, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// The drained variant when some CTA's share of K exceeds kDrainAbove K-blocks.
 template <int BN>
 cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cudaStream_t s,
                       bool pdl) {
-    switch (epi) {
-        case GEPI_STORE: return launch_t<BN, GEPI_STORE>(m, g, ks, s, pdl);
-        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL>(m, g, ks, s, pdl);
-        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU>(m, g, ks, s, pdl);
-        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE>(m, g, ks, s, pdl);
-        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX>(m, g, ks, s, pdl);
-        default: return cudaErrorInvalidValue;
-    }
+    const int KB = (g.K + 31) / 32;
+    const int per_cta = (KB + ks - 1) / ks;
+    if (per_cta > kDrainAbove) return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
+    return launch_bd<BN, false>(epi, m, g, ks, s, pdl);
 }
 
 }  // namespace
@@ -666,7 +781,7 @@ template <int BN>
 int active_clusters(int ksplit, int stages) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ksplit, 1024);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(gemm_threads(true));
     cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages, ksplit);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -676,7 +791,7 @@ int active_clusters(int ksplit, int stages) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE, true>, &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;

@@ -53,3 +53,21 @@ def test_gemm_rejects_bad_sizes(l2):
     for M, N, K in [(0, 8, 8), (8, 0, 8), (8, 8, 6), (8, 8, 0)]:
         with pytest.raises(l2.L2Error):
             l2.l2_gemm_tf32x3(d, d, d, M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 11008), (32, 512, 32768), (256, 512, 4096)])
+def test_gemm_long_k_accuracy_is_fp32_class(l2, M, N, K):
+    # relative L2 error of the whole product against float64: an fp32 GEMM with
+    # round-to-nearest accumulation stays near 1e-6 at these lengths, while
+    # letting the tensor core's accumulator absorb all of K grows linearly
+    # (about 2e-5 at K = 11008, 6e-5 at 32768)
+    import torch
+    rng = np.random.default_rng(K + N)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    W = (0.02 * rng.standard_normal((N, K))).astype(np.float32)
+    ref = A.astype(np.float64) @ W.astype(np.float64).T
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    l2.l2_gemm_tf32x3(torch.from_numpy(A).cuda(), torch.from_numpy(W).cuda(), dC, M, N, K)
+    C = dC.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(C - ref) / np.linalg.norm(ref)
+    assert rel < 3e-6, rel
