@@ -78,6 +78,10 @@ def load(path: str):
     L.oracle_swiglu.argtypes = [P, P, P, i32]
     L.oracle_argmax.restype = i32
     L.oracle_argmax.argtypes = [P, i32]
+    L.oracle_sample.restype = i32
+    L.oracle_sample.argtypes = [P, i32, ctypes.c_float, ctypes.c_float, ctypes.c_float, P]
+    L.oracle_generate_sampled.restype = ctypes.c_int
+    L.oracle_generate_sampled.argtypes = [P, P, i32, i32, ctypes.c_float, ctypes.c_float, P, P, P]
     return L
 
 
@@ -139,6 +143,22 @@ class Model:
         return (out, lt) if trace else out
 
 
+    def generate_sampled(self, prompt, steps: int, temperature: float, topp: float, uniforms):
+        """(tokens[steps], margins[steps]) drawn with oracle_sample."""
+        prompt = np.ascontiguousarray(prompt, dtype=np.int32)
+        u = _f32(uniforms)
+        if u.size < steps:
+            raise ValueError("need one uniform number per generated token")
+        out = np.empty(steps, dtype=np.int32)
+        mg = np.empty(steps, dtype=np.float32)
+        rc = self._lib.oracle_generate_sampled(self._h, prompt.ctypes.data, prompt.size, steps,
+                                               temperature, topp, u.ctypes.data, out.ctypes.data,
+                                               mg.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_generate_sampled rejected its arguments")
+        return out, mg
+
+
 # Building blocks (numpy in, numpy out).
 
 def rmsnorm(x, g, eps: float = 1e-5) -> np.ndarray:
@@ -188,3 +208,11 @@ def swiglu(h1, h3) -> np.ndarray:
 def argmax(v) -> int:
     v = _f32(v)
     return int(lib().oracle_argmax(v.ctypes.data, v.size))
+
+
+def sample(logits, temperature: float, topp: float, u: float):
+    """(token, margin) drawn from logits with oracle_sample."""
+    v = _f32(logits)
+    mg = ctypes.c_float()
+    t = lib().oracle_sample(v.ctypes.data, v.size, temperature, topp, u, ctypes.byref(mg))
+    return int(t), float(mg.value)

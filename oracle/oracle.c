@@ -209,6 +209,128 @@ int32_t oracle_argmax(const float* v, int32_t n) {
     return best;
 }
 
+/* Sampling instead of the greedy choice. The pages print sampled stories and
+ * mention the engine's "C sampling code" (openai.wiki, "未排序的待办事项")
+ * without giving its rule; the reading taken here:
+ *   temperature <= 0: the greedy choice (lowest index of the largest logit);
+ *   otherwise p_i = expf((l_i - max_j l_j) / temperature) in fp32, total =
+ *   their sum; with 0 < topp < 1 the nucleus is the smallest set of highest
+ *   p (sorted by p, ties by lower index) whose sum reaches topp * total,
+ *   widened to every token whose p equals the last one taken; otherwise the
+ *   nucleus is every token. With r = u * (sum of p over the nucleus), the
+ *   sampled token is the first nucleus member, in increasing index order,
+ *   whose running sum exceeds r (the last member if none does).
+ * u in [0, 1) is the uniform random number of this draw, supplied by the
+ * caller. Sums are sequential fp32. margin_out (nullable) receives the
+ * smallest distance, relative to the nucleus mass, between a running sum and
+ * the value it was compared with (r, or topp * total): a decision with a tiny
+ * margin can flip under a different summation order. */
+typedef struct {
+    float p;
+    int32_t i;
+} prob_index;
+
+static int by_p_desc(const void* a, const void* b) {
+    const prob_index* x = (const prob_index*)a;
+    const prob_index* y = (const prob_index*)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return (x->i > y->i) - (x->i < y->i);
+}
+
+int32_t oracle_sample(const float* logits, int32_t n, float temperature, float topp, float u,
+                      float* margin_out) {
+    if (margin_out) *margin_out = 1.0f;
+    if (!(temperature > 0.0f)) return oracle_argmax(logits, n);
+    float mx = logits[0];
+    for (int32_t i = 1; i < n; ++i)
+        if (logits[i] > mx) mx = logits[i];
+    float* p = (float*)malloc(sizeof(float) * (size_t)n);
+    float total = 0.0f;
+    for (int32_t i = 0; i < n; ++i) {
+        p[i] = expf((logits[i] - mx) / temperature);
+        total += p[i];
+    }
+    float v = 0.0f;  /* nucleus: p >= v */
+    float margin = 1.0f;
+    if (topp > 0.0f && topp < 1.0f) {
+        prob_index* s = (prob_index*)malloc(sizeof(prob_index) * (size_t)n);
+        for (int32_t i = 0; i < n; ++i) {
+            s[i].p = p[i];
+            s[i].i = i;
+        }
+        qsort(s, (size_t)n, sizeof(prob_index), by_p_desc);
+        const float target = topp * total;
+        float cum = 0.0f;
+        v = s[n - 1].p;
+        for (int32_t k = 0; k < n; ++k) {
+            const float before = cum;
+            cum += s[k].p;
+            if (cum >= target) {
+                v = s[k].p;
+                margin = fminf(cum - target, target - before) / total;
+                break;
+            }
+        }
+        free(s);
+    }
+    float mass = 0.0f;
+    for (int32_t i = 0; i < n; ++i)
+        if (p[i] >= v) mass += p[i];
+    const float r = u * mass;
+    float cum = 0.0f;
+    int32_t pick = -1, last = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (p[i] < v) continue;
+        last = i;
+        const float before = cum;
+        cum += p[i];
+        if (cum > r) {
+            pick = i;
+            margin = fminf(margin, fminf(cum - r, r - before) / mass);
+            break;
+        }
+    }
+    if (pick < 0) {
+        pick = last;
+        margin = 0.0f;
+    }
+    free(p);
+    if (margin_out) *margin_out = margin;
+    return pick;
+}
+
+/* oracle_generate with sampling: the token chosen at position p >= n_prompt-1
+ * is oracle_sample(logits, temperature, topp, uniforms[p - (n_prompt - 1)]).
+ * margins_out (nullable): [steps], the margin of each draw. */
+int oracle_generate_sampled(oracle_model* m, const int32_t* prompt, int32_t n_prompt,
+                            int32_t steps, float temperature, float topp, const float* uniforms,
+                            int32_t* out_tokens, float* margins_out) {
+    const oracle_config* c = &m->c;
+    if (n_prompt < 1 || steps < 1 || n_prompt + steps - 1 > c->seq_len) return -1;
+    float* logits = (float*)malloc(sizeof(float) * (size_t)c->vocab_size);
+    int32_t token = prompt[0];
+    for (int32_t pos = 0; pos < n_prompt + steps - 1; ++pos) {
+        if (oracle_forward(m, token, pos, logits, NULL) != 0) {
+            free(logits);
+            return -1;
+        }
+        if (pos + 1 < n_prompt) {
+            token = prompt[pos + 1];
+            continue;
+        }
+        const int32_t k = pos - (n_prompt - 1);
+        float mg = 1.0f;
+        const int32_t pick =
+            oracle_sample(logits, c->vocab_size, temperature, topp, uniforms[k], &mg);
+        out_tokens[k] = pick;
+        if (margins_out) margins_out[k] = mg;
+        token = pick;
+    }
+    free(logits);
+    return 0;
+}
+
 /* The decode step, in the order the Llama-2 architecture applies it. */
 int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_out,
                    float* x_trace) {

@@ -62,6 +62,19 @@ int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_ou
 int oracle_generate(oracle_model* m, const int32_t* prompt, int32_t n_prompt, int32_t steps,
                     int32_t* out_tokens, float* logits_trace);
 
+/* Sampling instead of greedy (see oracle.c for the rule): the token drawn
+ * from logits[n] at the given temperature and top-p with the uniform number
+ * u in [0, 1); margin_out (nullable) receives how close the draw was to a
+ * decision boundary, relative to the nucleus mass. */
+int32_t oracle_sample(const float* logits, int32_t n, float temperature, float topp, float u,
+                      float* margin_out);
+
+/* oracle_generate drawing every generated token with oracle_sample and
+ * uniforms[k] (k = 0 .. steps-1); margins_out (nullable): [steps]. */
+int oracle_generate_sampled(oracle_model* m, const int32_t* prompt, int32_t n_prompt,
+                            int32_t steps, float temperature, float topp, const float* uniforms,
+                            int32_t* out_tokens, float* margins_out);
+
 /* Building blocks, exported so that tests can pin each one. */
 void oracle_rmsnorm(float* out, const float* x, const float* g, int32_t n, float eps);
 void oracle_matvec(float* y, const float* W, const float* x, int32_t rows, int32_t cols);

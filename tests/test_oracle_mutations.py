@@ -13,6 +13,7 @@ import pytest
 import oracle
 import test_oracle_components as comp
 import test_oracle_model as model
+import test_oracle_sampling as samp
 
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
 
@@ -48,6 +49,15 @@ MUTANTS = {
     "argmax_last_tie": [("if (v[i] > v[best]) best = i;", "if (v[i] >= v[best]) best = i;")],
     "generate_feeds_prompt_late": [("token = (pos + 1 < n_prompt) ? prompt[pos + 1] : best;",
                                     "token = (pos < n_prompt) ? prompt[pos] : best;")],
+    "sample_temperature_multiplies": [("p[i] = expf((logits[i] - mx) / temperature);",
+                                       "p[i] = expf((logits[i] - mx) * temperature);")],
+    "sample_nucleus_drops_last": [("            if (cum >= target) {\n                v = s[k].p;",
+                                   "            if (cum >= target) {\n                v = s[k > 0 ? k - 1 : 0].p;")],
+    "sample_walks_rank_order": [("        if (p[i] < v) continue;\n        last = i;",
+                                 "        if (p[i] < v) continue;\n        if (i == 0 && n > 1 && p[1] > p[0]) continue;\n        last = i;")],
+    "sample_r_over_total": [("const float r = u * mass;", "const float r = u * total;")],
+    "sample_prompt_positions": [("const int32_t k = pos - (n_prompt - 1);\n        float mg",
+                                 "const int32_t k = pos - n_prompt + 1 > 0 ? pos - n_prompt + 1 : 0;\n        if (pos == n_prompt - 1) continue;\n        float mg")],
 }
 
 
@@ -57,6 +67,7 @@ def _pins():
     fns += [lambda: comp.test_argmax_last_and_first(n) for n in (1, 2, 31999)]
     fns += [model.test_handworked_two_layer_model, model.test_zero_layer_weights_closed_form,
             model.test_generate_feeds_prompt_then_greedy]
+    fns += [getattr(samp, n) for n in dir(samp) if n.startswith("test_")]
     for p in model.test_incremental_decode_equals_full_causal_recompute.pytestmark[0].args[1]:
         fns.append(lambda p=p: model.test_incremental_decode_equals_full_causal_recompute(p))
     return fns
