@@ -170,6 +170,29 @@ L2_API int l2_generate_prefill_device(l2_handle* h, const int32_t* d_prompt, int
 L2_API int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt, int32_t steps,
                        int32_t* d_out, void* stream);
 
+/* l2_generate drawing every generated token from the softmax of the logits
+ * instead of taking the greedy choice. The pages print sampled stories and
+ * mention the engine's C sampling code without stating its rule; the rule
+ * taken: temperature 0 is the greedy choice; otherwise
+ * p_i = exp((l_i - max) / temperature); with topp < 1 only the smallest set of
+ * highest p whose mass reaches topp * total is kept (widened to ties of the
+ * last token taken); the token is the first kept token, in increasing index
+ * order, whose running sum of p exceeds u * (kept mass).
+ * uniforms: host [steps], the caller's uniform random numbers in [0, 1), one
+ * per generated token (the draws are reproducible from them).
+ * Errors: as l2_generate, plus L2_EINVAL for temperature < 0, topp outside
+ * (0, 1] or a uniform number outside [0, 1). Synchronous. */
+L2_API int l2_generate_sample(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
+                              float temperature, float topp, const float* uniforms,
+                              int32_t* out_tokens);
+
+/* l2_generate_sample with device buffers: d_prompt int32 [n_prompt],
+ * d_uniforms fp32 [steps], d_out int32 [steps]; queued on `stream`, returns
+ * without waiting. Device values are not range-checked. */
+L2_API int l2_generate_sample_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
+                                     int32_t steps, float temperature, float topp,
+                                     const float* d_uniforms, int32_t* d_out, void* stream);
+
 /* Greedy generation for B independent sequences in lockstep (batched
  * decode). prompts: host, the B prompts concatenated; lens: host [B], each
  * >= 1; out_tokens: host [B][steps]. Sequence b runs forwards at positions

@@ -5,7 +5,8 @@ CUDA kernels. There is no CPU fallback; importing this package fails loudly when
 the library has not been built (``python llama_fp32_token_decode_b300/build.py``).
 Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
 l2_generate, l2_generate_device, l2_generate_batch, l2_generate_batch_device,
-l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_reset, l2_destroy,
+l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_generate_sample,
+l2_generate_sample_device, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
 l2_classify_greedy_noalloc, l2_gemm_tf32x3.
 """
@@ -30,7 +31,8 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device", "l2_prefill",
-           "l2_generate_prefill", "l2_generate_prefill_device", "l2_reset", "l2_destroy",
+           "l2_generate_prefill", "l2_generate_prefill_device", "l2_generate_sample",
+           "l2_generate_sample_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
            "l2_gemm_tf32x3")
 
@@ -71,6 +73,9 @@ _SIG = {
     "l2_generate_batch": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
     "l2_generate_batch_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
     "l2_prefill": (ctypes.c_int, [_P, _P, _I, _I, _P]),
+    "l2_generate_sample": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, ctypes.c_float, _P, _P]),
+    "l2_generate_sample_device": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, ctypes.c_float,
+                                                 _P, _P, _P]),
     "l2_generate_prefill": (ctypes.c_int, [_P, _P, _I, _I, _P]),
     "l2_generate_prefill_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_reset": (ctypes.c_int, [_P, _I]),
@@ -196,6 +201,24 @@ def l2_generate_prefill_device(h, d_prompt, n_prompt: int, steps: int, d_out,
                                            _stream(stream)), h)
 
 
+def l2_generate_sample(h, prompt, steps: int, temperature: float, topp: float,
+                       uniforms) -> np.ndarray:
+    prompt = _i32(prompt).ravel()
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).ravel()
+    if u.size < steps:
+        raise ValueError("need one uniform number per generated token")
+    out = np.empty(steps, np.int32)
+    _check(_lib.l2_generate_sample(h, prompt.ctypes.data, prompt.size, steps, temperature, topp,
+                                   u.ctypes.data, out.ctypes.data), h)
+    return out
+
+
+def l2_generate_sample_device(h, d_prompt, n_prompt: int, steps: int, temperature: float,
+                              topp: float, d_uniforms, d_out, stream=None) -> None:
+    _check(_lib.l2_generate_sample_device(h, _ptr(d_prompt), n_prompt, steps, temperature, topp,
+                                          _ptr(d_uniforms), _ptr(d_out), _stream(stream)), h)
+
+
 def l2_generate_batch(h, prompts, lens, steps: int) -> np.ndarray:
     prompts, lens = _i32(prompts).ravel(), _i32(lens).ravel()
     out = np.empty((lens.size, steps), np.int32)
@@ -284,6 +307,10 @@ class Decoder:
 
     def generate_prefill(self, prompt, steps: int) -> np.ndarray:
         return l2_generate_prefill(self.h, prompt, steps)
+
+    def generate_sample(self, prompt, steps: int, temperature: float, topp: float,
+                        uniforms) -> np.ndarray:
+        return l2_generate_sample(self.h, prompt, steps, temperature, topp, uniforms)
 
     def generate_batch(self, prompts, lens, steps: int) -> np.ndarray:
         return l2_generate_batch(self.h, prompts, lens, steps)

@@ -38,8 +38,9 @@ struct l2_handle {
     float *x = nullptr, *q = nullptr, *att = nullptr, *hb = nullptr, *logits = nullptr;
     float2* rope = nullptr;
     L2State* st = nullptr;
-    int* ibuf = nullptr;             // prompt [S] + out [S]
+    int* ibuf = nullptr;             // prompt [S] + out [S] + uniforms [S]
     int *d_prompt = nullptr, *d_out = nullptr;
+    float* d_uniforms = nullptr;     // sampling: one uniform number per generated token
 
     MatvecPlan p_qkv{}, p_wo{}, p_w13{}, p_w2{}, p_cls{};
     int nsplit = 1;
@@ -71,6 +72,8 @@ struct l2_handle {
     cudaStream_t stream = nullptr;
     cudaGraphExec_t fwd1 = nullptr;  // one forward
     cudaGraphExec_t fwdN = nullptr;  // kGraphBatch forwards
+    cudaGraphExec_t fwd1s = nullptr; // one forward + the sampler (captured on first use)
+    cudaGraphExec_t fwdNs = nullptr; // kGraphBatch of them
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     std::string err;
 };
@@ -130,7 +133,7 @@ __global__ void init_state_kernel(L2State* st, int pos, int token, const int* d_
                                   const int* d_pos, int vocab, int seq_len, int n_prompt, int mode,
                                   const int* prompt, int* out, int reset_err) {
     int p = d_pos ? d_pos[0] : pos;
-    int t = d_token ? d_token[0] : (prompt && mode == 1 ? prompt[0] : token);
+    int t = d_token ? d_token[0] : (prompt && mode >= 1 ? prompt[0] : token);
     p = min(max(p, 0), seq_len - 1);
     t = min(max(t, 0), vocab - 1);
     st->pos = p;
@@ -229,11 +232,15 @@ cudaError_t enqueue_forward(l2_handle* h, cudaStream_t s) {
     return launch_kind(h, 5, 0, s);
 }
 
-int capture(l2_handle* h, int n_forwards, cudaGraphExec_t* out) {
+int capture(l2_handle* h, int n_forwards, cudaGraphExec_t* out, bool sample = false) {
     cudaGraph_t g = nullptr;
     L2_CUDA(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
     cudaError_t e = cudaSuccess;
-    for (int i = 0; i < n_forwards && e == cudaSuccess; ++i) e = enqueue_forward(h, h->stream);
+    for (int i = 0; i < n_forwards && e == cudaSuccess; ++i) {
+        e = enqueue_forward(h, h->stream);
+        if (e == cudaSuccess && sample)
+            e = launch_sample(SampleArgs{h->st, h->logits, h->cfg.vocab_size}, h->stream, true);
+    }
     cudaError_t e2 = cudaStreamEndCapture(h->stream, &g);
     if (e != cudaSuccess) {
         if (g) cudaGraphDestroy(g);
@@ -599,6 +606,9 @@ int upload(l2_handle* h, const float* blob, cudaMemcpyKind kind) {
 void free_all(l2_handle* h) {
     if (h->fwd1) cudaGraphExecDestroy(h->fwd1);
     if (h->fwdN) cudaGraphExecDestroy(h->fwdN);
+    if (h->fwd1s) cudaGraphExecDestroy(h->fwd1s);
+    if (h->fwdNs) cudaGraphExecDestroy(h->fwdNs);
+    h->fwd1s = h->fwdNs = nullptr;
     if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
     cudaFree(h->bw);
     cudaFree(h->bact);
@@ -749,7 +759,7 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     const size_t o_x = take(d), o_q = take(d), o_att = take(d), o_hb = take(F);
     const size_t o_lg = take(B * V);
     const size_t o_rope = take(S * h->hd);  // float2 [S][hd/2]
-    const size_t o_st = take((sizeof(L2State) + 3) / 4), o_ib = take(2 * S);
+    const size_t o_st = take((sizeof(L2State) + 3) / 4), o_ib = take(3 * S);
     e = cudaMalloc(&h->act, off * sizeof(float));
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMalloc(activations)"));
     h->x = h->act + o_x;
@@ -762,6 +772,7 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     h->ibuf = reinterpret_cast<int*>(h->act + o_ib);
     h->d_prompt = h->ibuf;
     h->d_out = h->ibuf + S;
+    h->d_uniforms = reinterpret_cast<float*>(h->ibuf + 2 * S);
 
     e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaStreamCreate"));
@@ -859,13 +870,82 @@ int l2_reset(l2_handle* h, int32_t seq) {
     return L2_OK;
 }
 
-static int run_forwards(l2_handle* h, int n, cudaStream_t s) {
+static int run_forwards(l2_handle* h, int n, cudaStream_t s, bool sample = false) {
+    cudaGraphExec_t gN = sample ? h->fwdNs : h->fwdN, g1 = sample ? h->fwd1s : h->fwd1;
     while (n >= kGraphBatch) {
-        L2_CUDA(h, cudaGraphLaunch(h->fwdN, s));
+        L2_CUDA(h, cudaGraphLaunch(gN, s));
         n -= kGraphBatch;
     }
-    for (; n > 0; --n) L2_CUDA(h, cudaGraphLaunch(h->fwd1, s));
+    for (; n > 0; --n) L2_CUDA(h, cudaGraphLaunch(g1, s));
     return L2_OK;
+}
+
+// Sampling parameters of a generation (the state already holds mode 2).
+__global__ void init_sample_kernel(L2State* st, float temperature, float topp,
+                                   const float* uniforms) {
+    st->temperature = temperature;
+    st->topp = topp;
+    st->uniforms = uniforms;
+}
+
+static int generate_sample_impl(l2_handle* h, const int32_t* prompt, int32_t n_prompt,
+                                int32_t steps, float temperature, float topp,
+                                const float* uniforms, int32_t* out, bool on_device,
+                                cudaStream_t stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!prompt || !out || !uniforms) return fail(h, L2_EINVAL, "NULL prompt, uniforms or output");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
+        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    if (!(temperature >= 0.0f) || !(topp > 0.0f && topp <= 1.0f))
+        return fail(h, L2_EINVAL, "need temperature >= 0 and 0 < topp <= 1");
+    if (!on_device) {
+        for (int i = 0; i < n_prompt; ++i)
+            if (prompt[i] < 0 || prompt[i] >= h->cfg.vocab_size)
+                return fail(h, L2_EINVAL, "prompt id out of range");
+        for (int i = 0; i < steps; ++i)
+            if (!(uniforms[i] >= 0.0f && uniforms[i] < 1.0f))
+                return fail(h, L2_EINVAL, "uniform numbers must lie in [0, 1)");
+    }
+    if (!h->fwd1s) {
+        int rc = capture(h, 1, &h->fwd1s, true);
+        if (rc == L2_OK) rc = capture(h, kGraphBatch, &h->fwdNs, true);
+        if (rc != L2_OK) return rc;
+    }
+    cudaStream_t s = on_device ? stream : h->stream;
+    const int32_t* d_prompt = prompt;
+    const float* d_u = uniforms;
+    int32_t* d_out = on_device ? out : h->d_out;
+    if (!on_device) {
+        L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, prompt, sizeof(int32_t) * n_prompt,
+                                   cudaMemcpyHostToDevice, s));
+        L2_CUDA(h, cudaMemcpyAsync(h->d_uniforms, uniforms, sizeof(float) * steps,
+                                   cudaMemcpyHostToDevice, s));
+        d_prompt = h->d_prompt;
+        d_u = h->d_uniforms;
+    }
+    init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
+                                      h->cfg.seq_len, n_prompt, 2, d_prompt, d_out, 1);
+    init_sample_kernel<<<1, 1, 0, s>>>(h->st, temperature, topp, d_u);
+    L2_CUDA(h, cudaGetLastError());
+    int rc = run_forwards(h, n_prompt + steps - 1, s, true);
+    if (rc != L2_OK || on_device) return rc;
+    L2_CUDA(h, cudaMemcpyAsync(out, h->d_out, sizeof(int32_t) * steps, cudaMemcpyDeviceToHost, s));
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return check_device_error(h);
+}
+
+int l2_generate_sample(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
+                       float temperature, float topp, const float* uniforms,
+                       int32_t* out_tokens) {
+    return generate_sample_impl(h, prompt, n_prompt, steps, temperature, topp, uniforms,
+                                out_tokens, false, nullptr);
+}
+
+int l2_generate_sample_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
+                              int32_t steps, float temperature, float topp,
+                              const float* d_uniforms, int32_t* d_out, void* stream) {
+    return generate_sample_impl(h, d_prompt, n_prompt, steps, temperature, topp, d_uniforms,
+                                d_out, true, static_cast<cudaStream_t>(stream));
 }
 
 int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_pos, int32_t B,

@@ -134,7 +134,10 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int STAGES = (BN == 128) ? 3 : 4;  // deepest ring that fits
-    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators (chunk drain)
+    // TMEM columns: one accumulator, or two when chunks are drained
+    __host__ __device__ static constexpr uint32_t tmem_cols(bool drain) {
+        return drain ? 2 * BN : BN;
+    }
     static constexpr int PS = BN + 4;  // row stride (floats) of a staged partial tile
     // split-K receive buffer: one slot per peer, ceil(128 / S) rows of PS floats
     __host__ __device__ static constexpr size_t recv_bytes(int ksplit) {
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         prefetch_map(&mB_lo);
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_alloc(tmem_slot, C::tmem_cols(DRAIN));
         tmem_relinquish();
     }
     tc_fence_before();
@@ -636,7 +639,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     // ---- teardown: every tcgen05 access of this CTA is complete
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, C::tmem_cols(DRAIN));
 }
 
 __global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restrict__ hi,

@@ -30,7 +30,7 @@ struct L2State {
     int pos;            // position the next forward consumes
     int token;          // token the next forward consumes
     int n_prompt;       // generate: prompt length
-    int mode;           // 0 = single forward, 1 = generate
+    int mode;           // 0 = single forward, 1 = generate, 2 = generate with sampling
     int last_argmax;    // greedy choice of the last forward
     int err;            // ERR_* bits
     const int* prompt;  // generate: device prompt [n_prompt]
@@ -38,6 +38,17 @@ struct L2State {
     unsigned long long argmax_key;  // packed (orderable value, ~index) max
     unsigned int cls_done;          // classifier CTAs finished this forward
     unsigned int pad;
+    // mode 2 (generate with sampling): the sampling kernel, not the classifier,
+    // chooses the token and advances the position
+    float temperature;
+    float topp;
+    const float* uniforms;  // one uniform number in [0, 1) per generated token
+};
+
+struct SampleArgs {
+    L2State* st;
+    const float* logits;    // [V] of the forward just computed
+    int vocab;
 };
 
 enum Epilogue : int { EPI_QKV_ROPE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_CLASSIFIER = 3 };
@@ -331,6 +342,9 @@ cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n,
 cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl);
 cudaError_t launch_battn(const BAttnArgs& a, int M, cudaStream_t s, bool pdl);
 cudaError_t launch_badvance(const BAdvanceArgs& a, cudaStream_t s, bool pdl);
+
+// sample.cu
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s, bool pdl);
 
 // layout.cu
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,

@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
                     if (pos >= np - 1) st->out_tokens[pos - (np - 1)] = idx;
                     st->token = (pos + 1 < np) ? st->prompt[pos + 1] : idx;
                 }
-                st->pos = pos + 1;
+                if (st->mode != 2) st->pos = pos + 1;  // mode 2: the sampler advances
                 __threadfence();
             }
         }
