@@ -24,7 +24,8 @@ class OracleConfig(ctypes.Structure):
                 ("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("vocab_size", ctypes.c_int32),
                 ("seq_len", ctypes.c_int32), ("rope_theta", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("shared_classifier", ctypes.c_int32)]
+                ("norm_eps", ctypes.c_float), ("shared_classifier", ctypes.c_int32),
+                ("rolling_cache", ctypes.c_int32)]
 
 
 def build() -> str:
@@ -93,7 +94,8 @@ def make_config(cfg: dict) -> OracleConfig:
     return OracleConfig(cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["n_heads"],
                         cfg.get("n_kv_heads") or cfg["n_heads"], cfg["vocab_size"],
                         cfg["seq_len"], cfg.get("rope_theta", 10000.0),
-                        cfg.get("norm_eps", 1e-5), cfg.get("shared_classifier", 0))
+                        cfg.get("norm_eps", 1e-5), cfg.get("shared_classifier", 0),
+                        cfg.get("rolling_cache", 0))
 
 
 def blob_floats(cfg: dict) -> int:

@@ -39,6 +39,8 @@ struct oracle_model {
     float *k_cache, *v_cache;
     /* run state */
     float *x, *xb, *q, *k, *v, *att, *y, *h1, *h3, *hb, *scores;
+    /* rolling cache: the attended window's K and V rows in position order [S][kvd] */
+    float *kwin, *vwin;
 };
 
 static int config_ok(const oracle_config* c) {
@@ -104,8 +106,10 @@ oracle_model* oracle_model_new(const oracle_config* c, const float* blob, size_t
     m->h3 = (float*)calloc(F, sizeof(float));
     m->hb = (float*)calloc(F, sizeof(float));
     m->scores = (float*)calloc((size_t)c->seq_len, sizeof(float));
+    m->kwin = (float*)calloc((size_t)c->seq_len * kvd, sizeof(float));
+    m->vwin = (float*)calloc((size_t)c->seq_len * kvd, sizeof(float));
     if (!m->k_cache || !m->v_cache || !m->x || !m->xb || !m->q || !m->k || !m->v || !m->att ||
-        !m->y || !m->h1 || !m->h3 || !m->hb || !m->scores) {
+        !m->y || !m->h1 || !m->h3 || !m->hb || !m->scores || !m->kwin || !m->vwin) {
         oracle_model_free(m);
         return NULL;
     }
@@ -117,6 +121,7 @@ void oracle_model_free(oracle_model* m) {
     free(m->k_cache); free(m->v_cache);
     free(m->x); free(m->xb); free(m->q); free(m->k); free(m->v); free(m->att); free(m->y);
     free(m->h1); free(m->h3); free(m->hb); free(m->scores);
+    free(m->kwin); free(m->vwin);
     free(m);
 }
 
@@ -307,7 +312,8 @@ int oracle_generate_sampled(oracle_model* m, const int32_t* prompt, int32_t n_pr
                             int32_t steps, float temperature, float topp, const float* uniforms,
                             int32_t* out_tokens, float* margins_out) {
     const oracle_config* c = &m->c;
-    if (n_prompt < 1 || steps < 1 || n_prompt + steps - 1 > c->seq_len) return -1;
+    if (n_prompt < 1 || steps < 1) return -1;
+    if (!c->rolling_cache && n_prompt + steps - 1 > c->seq_len) return -1;
     float* logits = (float*)malloc(sizeof(float) * (size_t)c->vocab_size);
     int32_t token = prompt[0];
     for (int32_t pos = 0; pos < n_prompt + steps - 1; ++pos) {
@@ -335,7 +341,8 @@ int oracle_generate_sampled(oracle_model* m, const int32_t* prompt, int32_t n_pr
 int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_out,
                    float* x_trace) {
     const oracle_config* c = &m->c;
-    if (token < 0 || token >= c->vocab_size || pos < 0 || pos >= c->seq_len) return -1;
+    if (token < 0 || token >= c->vocab_size || pos < 0) return -1;
+    if (!c->rolling_cache && pos >= c->seq_len) return -1;
     const int32_t d = c->dim, F = c->hidden_dim, hd = m->hd, kvd = m->kvd;
     const int32_t group = c->n_heads / c->n_kv_heads;
     const size_t S = (size_t)c->seq_len;
@@ -355,13 +362,28 @@ int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_ou
 
         float* kc = m->k_cache + (size_t)l * S * (size_t)kvd;
         float* vc = m->v_cache + (size_t)l * S * (size_t)kvd;
-        memcpy(kc + (size_t)pos * kvd, m->k, (size_t)kvd * sizeof(float));
-        memcpy(vc + (size_t)pos * kvd, m->v, (size_t)kvd * sizeof(float));
+        const size_t slot = (size_t)pos % S;  /* == pos unless the cache rolls */
+        memcpy(kc + slot * kvd, m->k, (size_t)kvd * sizeof(float));
+        memcpy(vc + slot * kvd, m->v, (size_t)kvd * sizeof(float));
 
+        /* the attended positions, oldest first */
+        const float* ka = kc;
+        const float* va = vc;
+        int32_t n_pos = pos + 1;
+        if ((size_t)pos >= S) {  /* rolling: the last S positions, gathered in order */
+            for (size_t j = 0; j < S; ++j) {
+                const size_t src = ((size_t)pos + 1 + j) % S;
+                memcpy(m->kwin + j * kvd, kc + src * kvd, (size_t)kvd * sizeof(float));
+                memcpy(m->vwin + j * kvd, vc + src * kvd, (size_t)kvd * sizeof(float));
+            }
+            ka = m->kwin;
+            va = m->vwin;
+            n_pos = (int32_t)S;
+        }
         for (int32_t h = 0; h < c->n_heads; ++h) {
             const int32_t kvh = h / group;
             oracle_attention_head(m->att + (size_t)h * hd, m->q + (size_t)h * hd,
-                                  kc + (size_t)kvh * hd, vc + (size_t)kvh * hd, kvd, hd, pos + 1);
+                                  ka + (size_t)kvh * hd, va + (size_t)kvh * hd, kvd, hd, n_pos);
         }
         oracle_matvec(m->y, m->wo + (size_t)l * d * d, m->att, d, d);
         for (int32_t i = 0; i < d; ++i) m->x[i] += m->y[i];
@@ -388,7 +410,8 @@ int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_ou
 int oracle_generate(oracle_model* m, const int32_t* prompt, int32_t n_prompt, int32_t steps,
                     int32_t* out_tokens, float* logits_trace) {
     const oracle_config* c = &m->c;
-    if (n_prompt < 1 || steps < 1 || n_prompt + steps - 1 > c->seq_len) return -1;
+    if (n_prompt < 1 || steps < 1) return -1;
+    if (!c->rolling_cache && n_prompt + steps - 1 > c->seq_len) return -1;
     float* logits = (float*)malloc((size_t)c->vocab_size * sizeof(float));
     if (!logits) return -1;
     int32_t token = prompt[0];

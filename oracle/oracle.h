@@ -37,6 +37,7 @@ typedef struct {
     int32_t dim, hidden_dim, n_layers, n_heads, n_kv_heads, vocab_size, seq_len;
     float rope_theta, norm_eps;
     int32_t shared_classifier; /* 1: the classifier is the embedding table */
+    int32_t rolling_cache;     /* 1: positions beyond seq_len keep the last seq_len */
 } oracle_config;
 
 typedef struct oracle_model oracle_model;
@@ -50,7 +51,10 @@ oracle_model* oracle_model_new(const oracle_config* cfg, const float* blob, size
 void oracle_model_free(oracle_model* m);
 
 /* One decode step: token at position pos, writes KV slot pos, reads slots
- * 0..pos. logits_out: [vocab]. x_trace (nullable): [n_layers + 1][dim], the
+ * 0..pos. With rolling_cache (decoding beyond seq_len, a to-do item of the
+ * openai.wiki page, "未排序的待办事项"): position pos (any pos >= 0) writes
+ * slot pos % seq_len and attends, in position order, over positions
+ * max(0, pos - seq_len + 1) .. pos; RoPE uses the absolute position. logits_out: [vocab]. x_trace (nullable): [n_layers + 1][dim], the
  * residual stream after the embedding and after each layer. Returns 0, or -1
  * on a token or position out of range. */
 int oracle_forward(oracle_model* m, int32_t token, int32_t pos, float* logits_out,

@@ -143,8 +143,9 @@ def test_zero_layer_weights_closed_form():
 
 # ---------------------------------------------------------------- brute-force recompute
 
-def _full_causal_forward(cfg, blob, tokens):
-    """All positions at once in float64 with a T x T causal mask; no KV cache."""
+def _full_causal_forward(cfg, blob, tokens, window=None):
+    """All positions at once in float64 with a T x T causal mask (position t
+    attends to t - window + 1 .. t when a window is given); no KV cache."""
     d, F, L, V = cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["vocab_size"]
     H, KVH = cfg["n_heads"], cfg["n_kv_heads"]
     hd = d // H
@@ -180,6 +181,8 @@ def _full_causal_forward(cfg, blob, tokens):
         return np.stack([a * c - bb * s, a * s + bb * c], -1).reshape(T, nh * hd)
 
     mask = np.tril(np.ones((T, T), bool))
+    if window is not None:
+        mask &= ~np.tril(np.ones((T, T), bool), -window)
     x = E[np.asarray(tokens)]
     for l in range(L):
         xb = rms(x, ga[l])
@@ -225,6 +228,42 @@ def test_incremental_decode_equals_full_causal_recompute(shape):
     ref = _full_causal_forward(cfg, blob, tokens)
     err = np.linalg.norm(inc - ref) / np.linalg.norm(ref)
     assert err < 2e-6, err
+
+
+@pytest.mark.parametrize("shape", [
+    dict(dim=16, hidden_dim=40, n_layers=2, n_heads=4, n_kv_heads=4, vocab_size=23, seq_len=4),
+    dict(dim=24, hidden_dim=36, n_layers=2, n_heads=4, n_kv_heads=2, vocab_size=31, seq_len=5),
+])
+def test_rolling_cache_equals_windowed_full_recompute(shape):
+    # decoding past seq_len with a rolling cache == every position attending to
+    # the last seq_len positions (itself included), RoPE at the absolute position
+    cfg = _cfg(rolling_cache=1, **shape)
+    blob = synth.make_blob(cfg, 7, std=0.3)
+    S = cfg["seq_len"]
+    T = 3 * S + 1
+    tokens = synth.prompt_ids(8, T, cfg["vocab_size"])
+    m = oracle.Model(cfg, blob)
+    inc = np.stack([m.forward(t, p) for p, t in enumerate(tokens)]).astype(np.float64)
+    ref = _full_causal_forward(cfg, blob, tokens, window=S)
+    err = np.linalg.norm(inc - ref) / np.linalg.norm(ref)
+    assert err < 2e-6, err
+    # the full causal recompute differs once the window has rolled
+    full = _full_causal_forward(cfg, blob, tokens)
+    assert np.linalg.norm(inc[S:] - full[S:]) / np.linalg.norm(full[S:]) > 1e-3
+
+
+def test_rolling_cache_before_the_wrap_is_the_plain_cache():
+    shape = dict(dim=16, hidden_dim=40, n_layers=2, n_heads=4, n_kv_heads=4, vocab_size=23,
+                 seq_len=6)
+    blob = synth.make_blob(_cfg(**shape), 12, std=0.3)
+    tokens = synth.prompt_ids(2, 6, shape["vocab_size"])
+    a = oracle.Model(_cfg(**shape), blob)
+    b = oracle.Model(_cfg(rolling_cache=1, **shape), blob)
+    for p, t in enumerate(tokens):
+        np.testing.assert_array_equal(a.forward(t, p), b.forward(t, p))
+    with pytest.raises(ValueError):
+        a.forward(1, 6)           # plain cache: position seq_len is out of range
+    b.forward(1, 6)               # rolling cache: fine
 
 
 # ---------------------------------------------------------------- loop semantics

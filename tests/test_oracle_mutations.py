@@ -27,9 +27,10 @@ MUTANTS = {
     "rope_on_q_only": [("oracle_rope(m->k, c->n_kv_heads, hd, pos, c->rope_theta);", "")],
     "softmax_no_max_shift": [("s[i] = expf(s[i] - mx);", "s[i] = expf(s[i]);")],
     "attention_unscaled": [("s[t] = dot / scale_div;", "s[t] = dot;")],
-    "attention_skips_current_position": [("kvd, hd, pos + 1);", "kvd, hd, pos > 0 ? pos : 1);")],
-    "kv_written_to_slot_zero": [("memcpy(kc + (size_t)pos * kvd", "memcpy(kc + (size_t)0 * kvd")],
-    "values_written_to_slot_zero": [("memcpy(vc + (size_t)pos * kvd", "memcpy(vc + (size_t)0 * kvd")],
+    "attention_skips_current_position": [("int32_t n_pos = pos + 1;",
+                                          "int32_t n_pos = pos > 0 ? pos : 1;")],
+    "kv_written_to_slot_zero": [("memcpy(kc + slot * kvd", "memcpy(kc + 0 * kvd")],
+    "values_written_to_slot_zero": [("memcpy(vc + slot * kvd", "memcpy(vc + 0 * kvd")],
     "gqa_head_map_modulo": [("const int32_t kvh = h / group;",
                              "const int32_t kvh = h % c->n_kv_heads;")],
     "gate_up_swapped": [("const float z = h1[i];\n        hb[i] = (z / (1.0f + expf(-z))) * h3[i];",
@@ -49,6 +50,12 @@ MUTANTS = {
     "argmax_last_tie": [("if (v[i] > v[best]) best = i;", "if (v[i] >= v[best]) best = i;")],
     "generate_feeds_prompt_late": [("token = (pos + 1 < n_prompt) ? prompt[pos + 1] : best;",
                                     "token = (pos < n_prompt) ? prompt[pos] : best;")],
+    "rolling_rope_at_slot": [("oracle_rope(m->q, c->n_heads, hd, pos, c->rope_theta);",
+                              "oracle_rope(m->q, c->n_heads, hd, pos % c->seq_len, c->rope_theta);"),
+                             ("oracle_rope(m->k, c->n_kv_heads, hd, pos, c->rope_theta);",
+                              "oracle_rope(m->k, c->n_kv_heads, hd, pos % c->seq_len, c->rope_theta);")],
+    "rolling_slot_not_wrapped": [("const size_t slot = (size_t)pos % S;",
+                                  "const size_t slot = (size_t)pos % S == 0 && pos > 0 ? S - 1 : (size_t)pos % S;")],
     "sample_temperature_multiplies": [("p[i] = expf((logits[i] - mx) / temperature);",
                                        "p[i] = expf((logits[i] - mx) * temperature);")],
     "sample_nucleus_drops_last": [("            if (cum >= target) {\n                v = s[k].p;",
@@ -70,6 +77,8 @@ def _pins():
     fns += [getattr(samp, n) for n in dir(samp) if n.startswith("test_")]
     for p in model.test_incremental_decode_equals_full_causal_recompute.pytestmark[0].args[1]:
         fns.append(lambda p=p: model.test_incremental_decode_equals_full_causal_recompute(p))
+    for p in model.test_rolling_cache_equals_windowed_full_recompute.pytestmark[0].args[1]:
+        fns.append(lambda p=p: model.test_rolling_cache_equals_windowed_full_recompute(p))
     return fns
 
 
