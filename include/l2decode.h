@@ -62,7 +62,13 @@ extern "C" {
  * hidden_dim % 4 == 0; 1 <= max_batch <= 1024; 0 <= max_prefill <= 1024.
  * max_batch sequences get a KV cache each; the tensor-core path (batched
  * decode, prefill) is set up when max_batch > 1 or max_prefill > 1, with
- * row buffers for max(max_batch, max_prefill) rows. */
+ * row buffers for max(max_batch, max_prefill) rows.
+ * rolling_positions: 0 (or <= seq_len) keeps every position below seq_len.
+ * N > seq_len lets a batch-1 sequence decode positions 0 .. N-1: position p
+ * writes cache slot p % seq_len and attends over the last seq_len positions
+ * (a rolling cache; the openai.wiki page lists decoding beyond max_seq_len as
+ * a to-do that has to handle the KV cache, "未排序的待办事项"); RoPE keeps
+ * the absolute position. Batched decode and prefill stay below seq_len. */
 typedef struct {
     int32_t dim;               /* d, width of the residual stream            */
     int32_t hidden_dim;        /* F, SwiGLU hidden width                     */
@@ -76,6 +82,7 @@ typedef struct {
     int32_t max_batch;         /* sequences one handle can decode at once    */
     int32_t shared_classifier; /* 1: classifier = embedding table (no Wcls)  */
     int32_t max_prefill;       /* prompt positions one prefill pass takes    */
+    int32_t rolling_positions; /* > seq_len: decode up to this many positions */
 } l2_config;
 
 typedef struct l2_handle l2_handle;

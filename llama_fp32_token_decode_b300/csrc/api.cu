@@ -23,6 +23,7 @@ struct l2_handle {
     l2_config cfg{};
     int dev = 0, num_sms = 0;
     int hd = 0, kvd = 0;
+    int pmax = 0;                    // batch-1 positions 0 .. pmax-1 (> seq_len: rolling cache)
 
     float* weights = nullptr;
     float *emb = nullptr, *g_att = nullptr, *g_ffn = nullptr, *g_final = nullptr;
@@ -124,6 +125,8 @@ bool config_valid(const l2_config* c, std::string* why) {
     if (c->seq_len > (1 << 20)) return bad("seq_len <= 2^20");
     if (c->max_batch > 1024) return bad("max_batch <= 1024");
     if (c->max_prefill < 0 || c->max_prefill > 1024) return bad("0 <= max_prefill <= 1024");
+    if (c->rolling_positions < 0 || c->rolling_positions > (1 << 24))
+        return bad("0 <= rolling_positions <= 2^24");
     if (!(c->norm_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("norm_eps >= 0 and rope_theta > 0");
     if (c->shared_classifier != 0 && c->shared_classifier != 1) return bad("shared_classifier is 0 or 1");
     return true;
@@ -704,6 +707,8 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     const size_t B = c.max_batch;
     h->hd = c.dim / c.n_heads;
     h->kvd = c.n_kv_heads * h->hd;
+    h->pmax = c.rolling_positions > c.seq_len ? c.rolling_positions : c.seq_len;
+    const size_t P = static_cast<size_t>(h->pmax);
     const size_t kvd = h->kvd;
 
     // plans
@@ -758,8 +763,8 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     off = 0;
     const size_t o_x = take(d), o_q = take(d), o_att = take(d), o_hb = take(F);
     const size_t o_lg = take(B * V);
-    const size_t o_rope = take(S * h->hd);  // float2 [S][hd/2]
-    const size_t o_st = take((sizeof(L2State) + 3) / 4), o_ib = take(3 * S);
+    const size_t o_rope = take(P * h->hd);  // float2 [positions][hd/2]
+    const size_t o_st = take((sizeof(L2State) + 3) / 4), o_ib = take(3 * P);
     e = cudaMalloc(&h->act, off * sizeof(float));
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMalloc(activations)"));
     h->x = h->act + o_x;
@@ -771,8 +776,8 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     h->st = reinterpret_cast<L2State*>(h->act + o_st);
     h->ibuf = reinterpret_cast<int*>(h->act + o_ib);
     h->d_prompt = h->ibuf;
-    h->d_out = h->ibuf + S;
-    h->d_uniforms = reinterpret_cast<float*>(h->ibuf + 2 * S);
+    h->d_out = h->ibuf + P;
+    h->d_uniforms = reinterpret_cast<float*>(h->ibuf + 2 * P);
 
     e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaStreamCreate"));
@@ -784,8 +789,8 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
 
     // RoPE table: angle pos * theta^(-2i/hd) in double, rounded to float
     {
-        std::vector<float2> tab(S * (h->hd / 2));
-        for (size_t p = 0; p < S; ++p)
+        std::vector<float2> tab(P * (h->hd / 2));
+        for (size_t p = 0; p < P; ++p)
             for (int i = 0; i < h->hd / 2; ++i) {
                 const double freq = pow(static_cast<double>(c.rope_theta), -2.0 * i / h->hd);
                 const double ang = static_cast<double>(p) * freq;
@@ -894,8 +899,10 @@ static int generate_sample_impl(l2_handle* h, const int32_t* prompt, int32_t n_p
                                 cudaStream_t stream) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!prompt || !out || !uniforms) return fail(h, L2_EINVAL, "NULL prompt, uniforms or output");
-    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
-        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->pmax)
+        return fail(h, L2_EINVAL,
+                    "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len (rolling: "
+                    "rolling_positions)");
     if (!(temperature >= 0.0f) || !(topp > 0.0f && topp <= 1.0f))
         return fail(h, L2_EINVAL, "need temperature >= 0 and 0 < topp <= 1");
     if (!on_device) {
@@ -924,7 +931,7 @@ static int generate_sample_impl(l2_handle* h, const int32_t* prompt, int32_t n_p
         d_u = h->d_uniforms;
     }
     init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
-                                      h->cfg.seq_len, n_prompt, 2, d_prompt, d_out, 1);
+                                      h->pmax, n_prompt, 2, d_prompt, d_out, 1);
     init_sample_kernel<<<1, 1, 0, s>>>(h->st, temperature, topp, d_u);
     L2_CUDA(h, cudaGetLastError());
     int rc = run_forwards(h, n_prompt + steps - 1, s, true);
@@ -968,7 +975,7 @@ int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_po
         return L2_OK;
     }
     init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, d_tokens, d_pos, h->cfg.vocab_size,
-                                      h->cfg.seq_len, 0, 0, nullptr, nullptr, 0);
+                                      h->pmax, 0, 0, nullptr, nullptr, 0);
     L2_CUDA(h, cudaGetLastError());
     int rc = run_forwards(h, 1, s);
     if (rc != L2_OK) return rc;
@@ -985,7 +992,8 @@ int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t 
     if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
     for (int b = 0; b < B; ++b) {
         if (tokens[b] < 0 || tokens[b] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
-        if (pos[b] < 0 || pos[b] >= h->cfg.seq_len) return fail(h, L2_EINVAL, "position out of range");
+        if (pos[b] < 0 || pos[b] >= (B == 1 ? h->pmax : h->cfg.seq_len))
+            return fail(h, L2_EINVAL, "position out of range");
     }
     if (B > 1) {
         L2_CUDA(h, cudaMemcpyAsync(h->b_token, tokens, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
@@ -1002,7 +1010,7 @@ int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t 
         return check_device_error(h);
     }
     init_state_kernel<<<1, 1, 0, h->stream>>>(h->st, pos[0], tokens[0], nullptr, nullptr,
-                                              h->cfg.vocab_size, h->cfg.seq_len, 0, 0, nullptr,
+                                              h->cfg.vocab_size, h->pmax, 0, 0, nullptr,
                                               nullptr, 1);
     L2_CUDA(h, cudaGetLastError());
     int rc = run_forwards(h, 1, h->stream);
@@ -1018,11 +1026,13 @@ int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt, 
                        int32_t* d_out, void* stream) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!d_prompt || !d_out) return fail(h, L2_EINVAL, "NULL prompt or output buffer");
-    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
-        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->pmax)
+        return fail(h, L2_EINVAL,
+                    "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len (rolling: "
+                    "rolling_positions)");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     init_state_kernel<<<1, 1, 0, s>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
-                                      h->cfg.seq_len, n_prompt, 1, d_prompt, d_out, 0);
+                                      h->pmax, n_prompt, 1, d_prompt, d_out, 0);
     L2_CUDA(h, cudaGetLastError());
     return run_forwards(h, n_prompt + steps - 1, s);
 }
@@ -1031,14 +1041,16 @@ int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t s
                 int32_t* out_tokens) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!prompt || !out_tokens) return fail(h, L2_EINVAL, "NULL prompt or output");
-    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
-        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->pmax)
+        return fail(h, L2_EINVAL,
+                    "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len (rolling: "
+                    "rolling_positions)");
     for (int i = 0; i < n_prompt; ++i)
         if (prompt[i] < 0 || prompt[i] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "prompt id out of range");
     L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, prompt, sizeof(int32_t) * n_prompt,
                                cudaMemcpyHostToDevice, h->stream));
     init_state_kernel<<<1, 1, 0, h->stream>>>(h->st, 0, 0, nullptr, nullptr, h->cfg.vocab_size,
-                                              h->cfg.seq_len, n_prompt, 1, h->d_prompt, h->d_out, 1);
+                                              h->pmax, n_prompt, 1, h->d_prompt, h->d_out, 1);
     L2_CUDA(h, cudaGetLastError());
     int rc = run_forwards(h, n_prompt + steps - 1, h->stream);
     if (rc != L2_OK) return rc;
@@ -1134,8 +1146,10 @@ static int generate_prefill_impl(l2_handle* h, const int32_t* prompt, int32_t n_
                                  int32_t steps, int32_t* out, bool on_device, cudaStream_t stream) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!prompt || !out) return fail(h, L2_EINVAL, "NULL prompt or output");
-    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->cfg.seq_len)
-        return fail(h, L2_EINVAL, "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len");
+    if (n_prompt < 1 || steps < 1 || static_cast<long long>(n_prompt) + steps - 1 > h->pmax)
+        return fail(h, L2_EINVAL,
+                    "need n_prompt >= 1, steps >= 1, n_prompt + steps - 1 <= seq_len (rolling: "
+                    "rolling_positions)");
     int rc = prefill_checks(h, n_prompt, 0);
     if (rc != L2_OK) return rc;
     cudaStream_t s = on_device ? stream : h->stream;

@@ -62,7 +62,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         const int e = lane + 32 * j;
         qr[j] = e < hd ? __ldcg(a.q + static_cast<size_t>(h) * hd + e) : 0.0f;
     }
-    const int n = __ldcg(&a.st->pos) + 1;
+    // slots 0..pos, or every slot once the cache rolls (attention does not
+    // depend on the order of the positions it sums over)
+    const int n = min(__ldcg(&a.st->pos) + 1, a.seq_len);
     const int t0 = static_cast<int>(static_cast<long long>(n) * rank / nsplit);
     const int t1 = static_cast<int>(static_cast<long long>(n) * (rank + 1) / nsplit);
     const float* Kh = a.k_cache + static_cast<size_t>(kvh) * a.seq_len * hd;

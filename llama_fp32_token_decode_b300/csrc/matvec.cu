@@ -317,8 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
         }
     } else if constexpr (EPI == EPI_QKV_ROPE) {
         const int pos = __ldcg(&st->pos);
+        const int slot = pos % a.seq_len;  // == pos unless the cache rolls
         const int hd = a.head_dim, half = hd >> 1;
-        const float2* rope = a.rope + static_cast<size_t>(pos) * half;
+        const float2* rope = a.rope + static_cast<size_t>(pos) * half;  // absolute position
         for (int i = tid; i < nrows / 2; i += kThreads) {
             const int gr = r0 + 2 * i;
             const float x0 = rowval(2 * i), x1 = rowval(2 * i + 1);
@@ -329,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
             } else if (gr < a.d + a.kvd) {
                 const int j = gr - a.d, kvh = j / hd, e = j % hd;
                 const float2 cs = rope[e >> 1];
-                float* dst = a.k_cache + (static_cast<size_t>(kvh) * a.seq_len + pos) * hd + e;
+                float* dst = a.k_cache + (static_cast<size_t>(kvh) * a.seq_len + slot) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
                 dst[1] = x0 * cs.y + x1 * cs.x;
             } else {
                 const int j = gr - a.d - a.kvd, kvh = j / hd, e = j % hd;
-                float* dst = a.v_cache + (static_cast<size_t>(kvh) * a.seq_len + pos) * hd + e;
+                float* dst = a.v_cache + (static_cast<size_t>(kvh) * a.seq_len + slot) * hd + e;
                 dst[0] = x0;
                 dst[1] = x1;
             }
