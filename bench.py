@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="7b", choices=["15m", "44m", "110m", "7b", "batched"])
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="7B run: skip the with-prefill measurement (and its tf32 weight copies)")
     ap.add_argument("--no-batched", action="store_true",
                     help="default run: skip the batch-256 measurement added to the 7B line")
     ap.add_argument("--cpu-forwards", type=int, default=0,
@@ -302,6 +304,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     w = synth.workload(args.workload)
     cfg = synth.model_config(w)
+    use_prefill = args.workload == "7b" and not args.no_prefill
+    if use_prefill:
+        cfg["max_prefill"] = w["n_prompt"]  # rows of the prefill pass (no extra KV caches)
     n_fwd = forwards_of(w)
     prompt = synth.prompt(w)
     steps = w["steps"]
@@ -377,6 +382,15 @@ def run_ours(args, world, rank, local):
                 "kernel": "matvec_kernel<EPI_SWIGLU> (W1/W3 + SwiGLU)",
                 "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
+    # every kernel kind of the forward, timed live at the same position
+    kinds = {}
+    for kind in range(6):
+        t = l2.l2_time_kernel(dec.h, kind, pos_mid, iters if kind < 5 else 8, stream)
+        b = l2.l2_kernel_bytes(dec.h, kind, pos_mid)
+        kinds[l2.KERNEL_KINDS[kind]] = {
+            "launch_ms": t, "GB/s": b / (t / 1e3) / 1e9, "frac": b / (t / 1e3) / 1e9 / peak,
+            "ms_per_forward": t * (cfg["n_layers"] if kind < 5 else 1)}
+    roofline["per_kernel_at_pos"] = {"pos": pos_mid, "kernels": kinds}
     # whole-step roofline: algorithmic bytes of every forward over the step time
     step_bytes = sum(workload_bytes_per_forward(cfg, p) for p in range(n_fwd))
     step_gbs = step_bytes * args.steps / (ms / 1e3) / 1e9
@@ -385,6 +399,54 @@ def run_ours(args, world, rank, local):
                      "roofline_tok_s": n_fwd / (step_bytes / (peak * 1e9))}
 
     # ---- CPU baseline: the oracle as it stands, on a bounded sample, 1 core
+    # ---- the same workload with the prompt taken by one prefill pass: the
+    # decode of the generated tokens is unchanged, the 64 prompt positions go
+    # through the tensor-core path at once (weights read once for the prompt)
+    prefill = None
+    if use_prefill:
+        d_out_p = torch.zeros(steps, dtype=torch.int32, device="cuda")
+
+        def pstep(k):
+            l2.l2_generate_prefill_device(dec.h, d_prompt, len(prompt), k, d_out_p, stream)
+
+        for _ in range(args.warmup):
+            pstep(steps)
+        stream.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            pstep(steps)
+        e1.record(stream)
+        e1.synchronize()
+        ms_p = e0.elapsed_time(e1) / args.steps
+        ptoks = d_out_p.cpu().numpy()
+        same = int(np.argmax(ptoks != ref_tokens)) if np.any(ptoks != ref_tokens) else steps
+        e0.record(stream)
+        for _ in range(args.steps):
+            pstep(1)  # the prefill pass alone (+ the hand-off of its argmax)
+        e1.record(stream)
+        e1.synchronize()
+        ms_pre = e0.elapsed_time(e1) / args.steps
+        d, F, L, V = cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["vocab_size"]
+        kvd = cfg["n_kv_heads"] * (d // cfg["n_heads"])
+        params = L * (2 * d * d + 2 * d * kvd + 3 * d * F) + V * d
+        n = len(prompt)
+        flops = 2.0 * n * params
+        bytes_fp32 = 4.0 * params
+        peaks, _ = measured_peaks()
+        bound_ms = max(bytes_fp32 / (float(peaks["hbm_gbs"]) * 1e6),
+                       flops / (tf32x3_peak(peaks) * 1e9))
+        prefill = {"value": n_fwd / (ms_p / 1e3), "unit": "tok/s", "ms_per_step": ms_p,
+                   "prefill_ms": ms_pre, "prefill_tok_s": n / (ms_pre / 1e3),
+                   "prefill_roofline": {
+                       "bound_ms": bound_ms, "frac": bound_ms / ms_pre,
+                       "flops": flops, "fp32_weight_bytes": bytes_fp32,
+                       "note": "bound = max(fp32 weights once / HBM peak, 2 n params FLOPs / "
+                               "3xTF32 peak); the pass reads the tf32 hi and lo weight "
+                               "copies (2x the fp32 bytes)"},
+                   "tokens_equal_to_decode_path": same,
+                   "note": "prompt through l2_generate_prefill_device (one causal "
+                           "tensor-core pass), then 255 decode forwards; not the headline"}
+
     cpu = None
     if keep_host_blob:
         nf = args.cpu_forwards or default_cpu_forwards(args.workload)
@@ -412,6 +474,8 @@ def run_ours(args, world, rank, local):
             "roofline": roofline, "step_roofline": step_roofline,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": launches_per_step * args.steps}
+    if prefill is not None:
+        line["with_prefill"] = prefill
     dec.close()
     del dec
     if blob is not None:
