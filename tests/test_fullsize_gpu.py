@@ -90,8 +90,11 @@ def test_batch1_workload_full_size(l2, name, n_check):
 def test_7b_shape_full_size(l2):
     # the bench's workload: 7B shape (27 GB of fp32 weights), 64-token prompt;
     # the oracle takes several seconds per forward, so two positions are checked
+    # against it; the prefill pass is checked at every prompt position against
+    # the decode path
     w = synth.workload("7b")
     cfg = synth.model_config(w)
+    cfg["max_prefill"] = w["n_prompt"]  # also the prefill pass over the 64-token prompt
     blob = synth.make_blob(cfg, w["seed"])
     prompt = synth.prompt(w)
     consumed, logits, greedy = _oracle_prefix(cfg, blob, prompt, 2)
@@ -99,12 +102,21 @@ def test_7b_shape_full_size(l2):
         del blob
         gen = _device_generate(l2, dec, prompt, w["steps"])
         assert gen.shape == (w["steps"],)
+        # decode path, teacher-forced over the prompt
+        dec_lg = np.stack([dec.forward([int(t)], [p])[0] for p, t in enumerate(prompt)])
         for p in range(2):
-            lg = dec.forward([consumed[p]], [p])[0]
-            e = rel_l2(lg, logits[p])
+            e = rel_l2(dec_lg[p], logits[p])
             assert e <= REL_L2_TOL, f"7b pos {p}: rel-L2 {e:.3e}"
             if top2_gap(logits[p]) > GAP_TOL:
-                assert int(np.argmax(lg)) == int(greedy[p])
+                assert int(np.argmax(dec_lg[p])) == int(greedy[p])
+        # prefill pass over the same prompt: oracle at positions 0-1, decode path at all 64
+        pre = dec.prefill(prompt)
+        for p in range(2):
+            assert rel_l2(pre[p], logits[p]) <= REL_L2_TOL, f"7b prefill pos {p}"
+        for p in range(len(prompt)):
+            assert rel_l2(pre[p], dec_lg[p]) <= REL_L2_TOL, f"7b prefill vs decode pos {p}"
+        if top2_gap(dec_lg[-1]) > GAP_TOL:
+            assert int(np.argmax(pre[-1])) == int(gen[0])
 
 
 def test_batched_workload_full_size(l2):
