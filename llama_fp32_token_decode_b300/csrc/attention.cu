@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 
     pdl_launch_dependents();
     pdl_wait();
+    cluster_arrive_relaxed();  // this CTA is running (waited for before the remote writes)
 
     float qr[EPL];
 #pragma unroll
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     __syncthreads();
     float M = -INFINITY;
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+    cluster_wait_all();  // every CTA of the cluster is running: rank 0's inbox exists
     float* inbox = cluster.map_shared_rank(&s_inbox[rank][0], 0);
     for (int e = tid; e < hd; e += kAttnThreads) {
         float acc = 0.0f;
@@ -208,6 +210,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
     }
 
     pdl_wait();  // q and the current position's row come from the QKV matvec
+    cluster_arrive_relaxed();  // this CTA is running (waited for before the remote writes)
 
     const int n = min(__ldcg(&a.st->pos) + 1, a.seq_len);
     int t0, t1;
@@ -293,6 +296,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+    cluster_wait_all();  // every CTA of the cluster is running: rank 0's inbox exists
     if (tid < hd4) {
         float4 acc = z;
 #pragma unroll

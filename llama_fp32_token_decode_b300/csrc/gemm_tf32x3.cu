@@ -124,8 +124,9 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Dynamic shared memory one CTA may use (227 KB opt-in, minus static use).
-constexpr size_t kMaxDynSmem = 227 * 1024 - 64;
+// Dynamic shared memory one CTA may use (227 KB opt-in, minus static use:
+// the row-state arrays and the error flag).
+constexpr size_t kMaxDynSmem = 227 * 1024 - 2048;
 
 template <int BN>
 struct Cfg {
@@ -188,12 +189,18 @@ __device__ __forceinline__ void bulk_commit_and_wait_read() {
     asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Per-row state the QKV epilogue needs: position, whether the row is active,
+// and the KV cache it appends to.
+struct RowState {
+    int pos, active, cache;
+};
+
 // Fused epilogue of four consecutive output columns gc..gc+3 (gc % 4 == 0) of
-// row r. pos / active: the row's position and state (QKV only). ARGMAX folds
-// the columns into `best`; the caller publishes it.
+// row r. rs: the row's state (QKV only). ARGMAX folds the columns into
+// `best`; the caller publishes it.
 template <int EPI>
-__device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const float (&a)[4], int pos,
-                                     int active, unsigned long long& best) {
+__device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const float (&a)[4],
+                                     const RowState& rs, unsigned long long& best) {
     if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
         float* o = g.out + static_cast<size_t>(r) * g.ldc + gc;
         if (gc + 4 <= g.N && (g.ldc & 3) == 0) {
@@ -213,19 +220,27 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
     } else if constexpr (EPI == GEPI_SWIGLU) {
         // interleaved rows: column 2j is the gate, 2j+1 the up projection
         const size_t F = static_cast<size_t>(g.N) >> 1;
+        const size_t idx = static_cast<size_t>(r) * F + (gc >> 1);
+        if (gc + 4 <= g.N && (F & 1) == 0) {  // both outputs of the group, 8-byte aligned
+            const float h0 = silu(a[0]) * a[1], h1 = silu(a[2]) * a[3];
+            const float2 hi = make_float2(tf32_round(h0), tf32_round(h1));
+            *reinterpret_cast<float2*>(g.out_hi + idx) = hi;
+            *reinterpret_cast<float2*>(g.out_lo + idx) =
+                make_float2(tf32_round(h0 - hi.x), tf32_round(h1 - hi.y));
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-            if (gc + j + 1 < g.N) {
-                const float h = silu(a[j]) * a[j + 1];
-                const float hi = tf32_round(h);
-                const size_t idx = static_cast<size_t>(r) * F + ((gc + j) >> 1);
-                g.out_hi[idx] = hi;
-                g.out_lo[idx] = tf32_round(h - hi);
+            for (int j = 0; j < 4; j += 2) {
+                if (gc + j + 1 < g.N) {
+                    const float h = silu(a[j]) * a[j + 1];
+                    const float hi = tf32_round(h);
+                    g.out_hi[idx + (j >> 1)] = hi;
+                    g.out_lo[idx + (j >> 1)] = tf32_round(h - hi);
+                }
             }
         }
     } else if constexpr (EPI == GEPI_QKV_ROPE) {
-        if (!active) return;
-        const int hd = g.head_dim;
+        if (!rs.active) return;
+        const int hd = g.head_dim, pos = rs.pos;
         const float2* rope = g.rope + static_cast<size_t>(pos) * (hd >> 1);
 #pragma unroll
         for (int j = 0; j < 4; j += 2) {
@@ -240,13 +255,13 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
             } else if (c < g.d + g.kvd) {
                 const int jj = c - g.d, kvh = jj / hd, e = jj % hd;
                 const float2 cs = rope[e >> 1];
-                float* dst = g.k_cache + static_cast<size_t>(g.seq ? __ldcg(g.seq + r) : r) * g.cache_seq +
+                float* dst = g.k_cache + static_cast<size_t>(rs.cache) * g.cache_seq +
                              (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
                 dst[1] = x0 * cs.y + x1 * cs.x;
             } else {
                 const int jj = c - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
-                float* dst = g.v_cache + static_cast<size_t>(g.seq ? __ldcg(g.seq + r) : r) * g.cache_seq +
+                float* dst = g.v_cache + static_cast<size_t>(rs.cache) * g.cache_seq +
                              (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
                 dst[0] = x0;
                 dst[1] = x1;
@@ -265,18 +280,24 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
     }
 }
 
-__device__ __forceinline__ void row_state(const GemmArgs& g, int r, int& pos, int& active) {
-    pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
-    active = g.active ? __ldcg(g.active + r) : 1;
+// Row r's state, read from the arrays the previous kernels wrote.
+__device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
+    RowState rs;
+    rs.pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
+    rs.active = g.active ? __ldcg(g.active + r) : 1;
+    rs.cache = g.seq ? __ldcg(g.seq + r) : r;
+    return rs;
 }
 
 // Grid (S, tiles): blockIdx.x is the K split (the CTA's rank in a cluster of S
 // CTAs that share one 128 x BN output tile), blockIdx.y the tile (M tiles of
-// one N tile adjacent). Warps 0-3 own TMEM lane quarters 0-3 (tile rows
-// 32w..32w+31) and run the epilogue. Without the chunk drain (four warps)
-// warp 0 lane 0 issues TMA and warp 1 lane 0 the MMAs before joining the
-// epilogue; with it (six warps) warps 0-3 drain chunks during the mainloop,
-// so TMA and MMA issue move to warps 4 and 5.
+// one N tile adjacent). Warp w reads TMEM lane quarter w % 4 (tile rows
+// 32(w % 4) .. + 31). Without the chunk drain (eight warps) warp 0 lane 0
+// issues TMA and warp 1 lane 0 the MMAs; afterwards warps w and w + 4 share
+// the accumulator's 32-column chunks, and all eight run the epilogue (the
+// epilogue is a chain of dependent loads and stores per output group, so it
+// wants many warps in flight). With the drain (six warps) warps 0-3 drain
+// chunks during the mainloop, so TMA and MMA issue move to warps 4 and 5.
 //
 // Accumulation precision: the tensor core adds into its fp32 accumulator
 // without round-to-nearest. Measured against float64 (M 64, N 512): letting
@@ -295,7 +316,7 @@ __device__ __forceinline__ void row_state(const GemmArgs& g, int r, int& pos, in
 // peer's mbarrier); CTA s adds rows [128 s / S, 128 (s+1) / S) of the S
 // partials in rank order (a fixed order: the result does not depend on
 // timing) and applies the epilogue to them.
-constexpr int gemm_threads(bool drain) { return drain ? 192 : 128; }
+constexpr int gemm_threads(bool drain) { return drain ? 192 : 256; }
 constexpr int kChunk = 2;         // K-blocks per TMEM accumulation chunk (DRAIN)
 constexpr int kDrainAbove = 16;   // a CTA with more K-blocks than this drains chunks
 
@@ -325,6 +346,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     uint64_t* recvb = accfree + 2;   // split-K: the peers' slices of this CTA's rows
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
     __shared__ int s_err;
+    // QKV epilogue: state of the tile's rows, loaded once during the mainloop
+    __shared__ RowState s_rows[EPI == GEPI_QKV_ROPE ? 128 : 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = (g.M + 127) / 128;
@@ -445,9 +468,19 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             }
         }
     } else if constexpr (!DRAIN) {
-        // the other lanes wait below for the single accumulator
+        // the other warps wait below for the single accumulator; warp 2 first
+        // fetches the QKV rows' state (written by earlier kernels)
+        if (EPI == GEPI_QKV_ROPE && warp == 2) {
+            pdl_wait();
+            for (int i = lane; i < 128; i += 32)
+                if (m0 + i < m_end) s_rows[i] = load_row_state(g, m0 + i);
+        }
     } else {
         // ---- warps 0-3: drain every chunk into registers (fp32 round-to-nearest adds)
+        if (EPI == GEPI_QKV_ROPE && m0 + threadIdx.x < m_end) {
+            pdl_wait();
+            s_rows[threadIdx.x] = load_row_state(g, m0 + threadIdx.x);
+        }
         const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
         for (int c = 0; c < NCH; ++c) {
             const int buf = c & 1;
@@ -471,23 +504,31 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     }
     __syncwarp();
     if constexpr (!DRAIN) {
-        // ---- all four warps: wait for the single accumulator (read in the epilogue)
+        // ---- all warps: wait for the single accumulator (read in the epilogue)
         if (NK > 0 && !mbar_wait_bounded(&accfull[0], 0u)) s_err = 1;
         tc_fence_after();
     }
-    __syncthreads();  // mainloop and drain done; s_err settled
-    const int row = 32 * warp + lane;  // warps 0-3: this thread's tile row
+    __syncthreads();  // mainloop and drain done; s_err settled; s_rows loaded
+    constexpr int NT = gemm_threads(DRAIN);
+    // TMEM readers: warps 0-3 with the drain (all columns, from R); without
+    // it all eight warps, warp w taking chunks w / 4, w / 4 + 2, ...
+    constexpr int kHalves = DRAIN ? 1 : 2;
+    const int half = DRAIN ? 0 : (warp >> 2);
+    const bool reader = DRAIN ? (warp < 4) : true;
+    const int row = 32 * (warp & 3) + lane;  // this reader's tile row
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    auto rstate = [&](int lr) {
+        if constexpr (EPI == GEPI_QKV_ROPE) return s_rows[lr];
+        return RowState{0, 1, 0};
+    };
 
     if (nsplit == 1) {
         if (s_err) {
             if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
-        } else if (warp < 4) {
+        } else if (reader) {
             const int r = m0 + row;
             const bool row_ok = r < m_end;
-            int pos = 0, active = 1;
-            if constexpr (EPI == GEPI_QKV_ROPE) {
-                if (row_ok) row_state(g, r, pos, active);
-            }
+            const RowState rs = row_ok ? rstate(row) : RowState{0, 0, 0};
             unsigned long long best = 0ull;
             if constexpr (DRAIN) {
                 if (row_ok) {
@@ -496,22 +537,22 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                         const int gc = n0 + j;
                         if (gc < g.N) {
                             const float a4[4] = {R[j], R[j + 1], R[j + 2], R[j + 3]};
-                            epi4<EPI>(g, r, gc, a4, pos, active, best);
+                            epi4<EPI>(g, r, gc, a4, rs, best);
                         }
                     }
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     float v[32];
                     __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+                    tmem_ld32(tmem + lane_addr + 32 * c, v);
                     const int gc0 = n0 + 32 * c;
                     if (!row_ok || gc0 >= g.N) continue;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
-                        if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, pos, active, best);
+                        if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, rs, best);
                     }
                 }
             }
@@ -522,7 +563,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     } else {
         // stage this CTA's partial tile (row-major, stride PS) in the ring
         float* P = reinterpret_cast<float*>(gbase);
-        if (warp < 4) {
+        if (reader) {
             if constexpr (DRAIN) {
 #pragma unroll
                 for (int j = 0; j < BN; j += 4)
@@ -530,10 +571,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                         make_float4(R[j], R[j + 1], R[j + 2], R[j + 3]);
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     float v[32];
                     __syncwarp();
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+                    tmem_ld32(tmem + lane_addr + 32 * c, v);
                     if (NK == 0) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = 0.0f;
@@ -563,7 +604,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                             static_cast<uint32_t>((q1 - q0) * PS * 4), map_peer(smem_u32(recvb), q));
             }
         }
-        if (warp < 4) {
+        {
             const int gpr = BN / 4;  // float4 groups per row
             // residual: this thread's first rows of x are loaded while the slices travel
             constexpr int kPre = 4;
@@ -572,7 +613,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             for (int u = 0; u < kPre; ++u) {
                 xpre[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if constexpr (EPI == GEPI_RESIDUAL) {
-                    const int t = threadIdx.x + 128 * u;
+                    const int t = threadIdx.x + NT * u;
                     const int lr = r0 + t / gpr, gc = n0 + 4 * (t % gpr);
                     const int r = m0 + lr;
                     if (t < (r1 - r0) * gpr && r < m_end && gc + 4 <= g.N && (g.ldc & 3) == 0)
@@ -609,25 +650,23 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                             make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
                         return;
                     }
-                    int pos = 0, active = 1;
-                    if constexpr (EPI == GEPI_QKV_ROPE) row_state(g, r, pos, active);
                     unsigned long long best = 0ull;
                     const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-                    epi4<EPI>(g, r, gc, a4, pos, active, best);
+                    epi4<EPI>(g, r, gc, a4, rstate(lr), best);
                     if constexpr (EPI == GEPI_ARGMAX) {
                         if (best != 0ull) atomicMax(g.argmax_keys + r, best);
                     }
                 };
 #pragma unroll
                 for (int u = 0; u < kPre; ++u) {
-                    const int t = threadIdx.x + 128 * u;
+                    const int t = threadIdx.x + NT * u;
                     if (t < ngroups) {
                         const int gc = n0 + 4 * (t % gpr);
                         const bool hx = (EPI == GEPI_RESIDUAL) && gc + 4 <= g.N && (g.ldc & 3) == 0;
                         group(t, hx, xpre[u]);
                     }
                 }
-                for (int t = threadIdx.x + 128 * kPre; t < ngroups; t += 128)
+                for (int t = threadIdx.x + NT * kPre; t < ngroups; t += NT)
                     group(t, false, make_float4(0.f, 0.f, 0.f, 0.f));
             } else if (threadIdx.x == 0) {
                 atomicOr(g.err, ERR_TIMEOUT_TMA);
