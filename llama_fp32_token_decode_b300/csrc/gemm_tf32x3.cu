@@ -195,18 +195,51 @@ struct RowState {
     int pos, active, cache;
 };
 
+// Global operands of one output group's epilogue, loaded ahead of the
+// partial sums so that their latency overlaps the reduction: the residual's
+// four values (RESIDUAL), the RoPE (cos, sin) pairs of the group's two
+// column pairs (QKV).
+struct EpiPre {
+    float4 x;
+    float2 cs[2];
+};
+
+template <int EPI>
+__device__ __forceinline__ EpiPre epi_pre(const GemmArgs& g, int r, int gc, const RowState& rs) {
+    EpiPre p;
+    p.x = make_float4(0.f, 0.f, 0.f, 0.f);
+    p.cs[0] = p.cs[1] = make_float2(1.f, 0.f);
+    if constexpr (EPI == GEPI_RESIDUAL) {
+        if (gc + 4 <= g.N && (g.ldc & 3) == 0)
+            p.x = __ldcg(reinterpret_cast<const float4*>(g.out + static_cast<size_t>(r) * g.ldc + gc));
+    } else if constexpr (EPI == GEPI_QKV_ROPE) {
+        if (rs.active) {
+            const int hd = g.head_dim;
+            const float2* rope = g.rope + static_cast<size_t>(rs.pos) * (hd >> 1);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = gc + 2 * j;
+                if (c + 1 < g.N && c < g.d + g.kvd)
+                    p.cs[j] = rope[((c < g.d ? c : c - g.d) % hd) >> 1];
+            }
+        }
+    }
+    return p;
+}
+
 // Fused epilogue of four consecutive output columns gc..gc+3 (gc % 4 == 0) of
-// row r. rs: the row's state (QKV only). ARGMAX folds the columns into
-// `best`; the caller publishes it.
+// row r. rs: the row's state (QKV only); pre: from epi_pre for the same group.
+// ARGMAX folds the columns into `best`; the caller publishes it.
 template <int EPI>
 __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const float (&a)[4],
-                                     const RowState& rs, unsigned long long& best) {
+                                     const RowState& rs, const EpiPre& pre,
+                                     unsigned long long& best) {
     if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
         float* o = g.out + static_cast<size_t>(r) * g.ldc + gc;
         if (gc + 4 <= g.N && (g.ldc & 3) == 0) {
             float4 w = make_float4(a[0], a[1], a[2], a[3]);
             if constexpr (EPI == GEPI_RESIDUAL) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
+                const float4 x = pre.x;
                 w.x += x.x;
                 w.y += x.y;
                 w.z += x.z;
@@ -241,20 +274,18 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
     } else if constexpr (EPI == GEPI_QKV_ROPE) {
         if (!rs.active) return;
         const int hd = g.head_dim, pos = rs.pos;
-        const float2* rope = g.rope + static_cast<size_t>(pos) * (hd >> 1);
 #pragma unroll
         for (int j = 0; j < 4; j += 2) {
             const int c = gc + j;
             if (c + 1 >= g.N) break;
             const float x0 = a[j], x1 = a[j + 1];
+            const float2 cs = pre.cs[j >> 1];
             if (c < g.d) {
-                const float2 cs = rope[(c % hd) >> 1];
                 float* q = g.q + static_cast<size_t>(r) * g.d + c;
                 q[0] = x0 * cs.x - x1 * cs.y;
                 q[1] = x0 * cs.y + x1 * cs.x;
             } else if (c < g.d + g.kvd) {
                 const int jj = c - g.d, kvh = jj / hd, e = jj % hd;
-                const float2 cs = rope[e >> 1];
                 float* dst = g.k_cache + static_cast<size_t>(rs.cache) * g.cache_seq +
                              (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
@@ -511,8 +542,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     __syncthreads();  // mainloop and drain done; s_err settled; s_rows loaded
     constexpr int NT = gemm_threads(DRAIN);
     // TMEM readers: warps 0-3 with the drain (all columns, from R); without
-    // it all eight warps, warp w taking chunks w / 4, w / 4 + 2, ...
-    constexpr int kHalves = DRAIN ? 1 : 2;
+    // it every warp, warp w taking chunks w / 4, w / 4 + NT / 128, ...
+    constexpr int kHalves = DRAIN ? 1 : NT / 128;
     const int half = DRAIN ? 0 : (warp >> 2);
     const bool reader = DRAIN ? (warp < 4) : true;
     const int row = 32 * (warp & 3) + lane;  // this reader's tile row
@@ -537,7 +568,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                         const int gc = n0 + j;
                         if (gc < g.N) {
                             const float a4[4] = {R[j], R[j + 1], R[j + 2], R[j + 3]};
-                            epi4<EPI>(g, r, gc, a4, rs, best);
+                            epi4<EPI>(g, r, gc, a4, rs, epi_pre<EPI>(g, r, gc, rs), best);
                         }
                     }
                 }
@@ -552,7 +583,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
-                        if (gc0 + j < g.N) epi4<EPI>(g, r, gc0 + j, a4, rs, best);
+                        if (gc0 + j < g.N)
+                            epi4<EPI>(g, r, gc0 + j, a4, rs, epi_pre<EPI>(g, r, gc0 + j, rs), best);
                     }
                 }
             }
@@ -606,68 +638,69 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         }
         {
             const int gpr = BN / 4;  // float4 groups per row
-            // residual: this thread's first rows of x are loaded while the slices travel
-            constexpr int kPre = 4;
-            float4 xpre[kPre];
+            const int ngroups = (r1 - r0) * gpr;
+            const float* recv =
+                reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
+            // Each thread takes its groups kU at a time: group t is row r0 + t / gpr,
+            // columns 4 (t % gpr) .. + 3 of the tile. The global operands of a batch
+            // are requested first (for the first batch, while the slices travel),
+            // then all its partial-sum loads, then the epilogue math and stores, so
+            // a batch has kU * S loads in flight rather than one chain per group.
+            constexpr int kU = 4;
+            int t0 = threadIdx.x;
+            bool ok[kU];
+            int lrs[kU];
+            EpiPre pre[kU];
+            auto fetch = [&](int tb) {
 #pragma unroll
-            for (int u = 0; u < kPre; ++u) {
-                xpre[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (EPI == GEPI_RESIDUAL) {
-                    const int t = threadIdx.x + NT * u;
-                    const int lr = r0 + t / gpr, gc = n0 + 4 * (t % gpr);
-                    const int r = m0 + lr;
-                    if (t < (r1 - r0) * gpr && r < m_end && gc + 4 <= g.N && (g.ldc & 3) == 0)
-                        xpre[u] = __ldcg(reinterpret_cast<const float4*>(
-                            g.out + static_cast<size_t>(r) * g.ldc + gc));
+                for (int u = 0; u < kU; ++u) {
+                    const int t = tb + NT * u;
+                    lrs[u] = r0 + t / gpr;
+                    const int r = m0 + lrs[u], gc = n0 + 4 * (t % gpr);
+                    ok[u] = t < ngroups && r < m_end && gc < g.N;
+                    pre[u] = ok[u] ? epi_pre<EPI>(g, r, gc, rstate(lrs[u])) : EpiPre{};
                 }
-            }
+            };
+            fetch(t0);
             const bool got = mbar_wait_bounded(recvb, 0u);
             if (!got) s_err = 1;
             if (!s_err) {
-                const float* recv =
-                    reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
-                const int ngroups = (r1 - r0) * gpr;
-                // group t: row r0 + t / gpr, columns 4 (t % gpr) .. + 3 of the tile; the
-                // partials are added in rank order (a fixed order, whoever arrived first)
-                auto group = [&](int t, bool have_x, float4 x) {
-                    const int lr = r0 + t / gpr, c4 = t % gpr;
-                    const int r = m0 + lr, gc = n0 + 4 * c4;
-                    if (r >= m_end || gc >= g.N) return;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int q = 0; q < nsplit; ++q) {
-                        const float* src =
-                            (q == split) ? P + lr * PS
-                                         : recv + static_cast<size_t>((q < split ? q : q - 1) * R_ +
-                                                                      (lr - r0)) * PS;
-                        const float4 v = *reinterpret_cast<const float4*>(src + 4 * c4);
-                        acc.x += v.x;
-                        acc.y += v.y;
-                        acc.z += v.z;
-                        acc.w += v.w;
-                    }
-                    if (have_x) {  // residual with its row already loaded
-                        *reinterpret_cast<float4*>(g.out + static_cast<size_t>(r) * g.ldc + gc) =
-                            make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
-                        return;
-                    }
-                    unsigned long long best = 0ull;
-                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-                    epi4<EPI>(g, r, gc, a4, rstate(lr), best);
-                    if constexpr (EPI == GEPI_ARGMAX) {
-                        if (best != 0ull) atomicMax(g.argmax_keys + r, best);
-                    }
-                };
+                for (; t0 < ngroups; t0 += kU * NT) {
+                    float4 acc[kU];
 #pragma unroll
-                for (int u = 0; u < kPre; ++u) {
-                    const int t = threadIdx.x + NT * u;
-                    if (t < ngroups) {
-                        const int gc = n0 + 4 * (t % gpr);
-                        const bool hx = (EPI == GEPI_RESIDUAL) && gc + 4 <= g.N && (g.ldc & 3) == 0;
-                        group(t, hx, xpre[u]);
+                    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    // the S partials in rank order (a fixed order, whoever arrived first)
+                    for (int q = 0; q < nsplit; ++q) {
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            if (!ok[u]) continue;
+                            const int c4 = (t0 + NT * u) % gpr;
+                            const float* src =
+                                (q == split)
+                                    ? P + lrs[u] * PS
+                                    : recv + static_cast<size_t>((q < split ? q : q - 1) * R_ +
+                                                                 (lrs[u] - r0)) * PS;
+                            const float4 v = *reinterpret_cast<const float4*>(src + 4 * c4);
+                            acc[u].x += v.x;
+                            acc[u].y += v.y;
+                            acc[u].z += v.z;
+                            acc[u].w += v.w;
+                        }
                     }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        if (!ok[u]) continue;
+                        const int t = t0 + NT * u;
+                        const int r = m0 + lrs[u], gc = n0 + 4 * (t % gpr);
+                        unsigned long long best = 0ull;
+                        const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+                        epi4<EPI>(g, r, gc, a4, rstate(lrs[u]), pre[u], best);
+                        if constexpr (EPI == GEPI_ARGMAX) {
+                            if (best != 0ull) atomicMax(g.argmax_keys + r, best);
+                        }
+                    }
+                    if (t0 + kU * NT < ngroups) fetch(t0 + kU * NT);
                 }
-                for (int t = threadIdx.x + NT * kPre; t < ngroups; t += NT)
-                    group(t, false, make_float4(0.f, 0.f, 0.f, 0.f));
             } else if (threadIdx.x == 0) {
                 atomicOr(g.err, ERR_TIMEOUT_TMA);
             }
