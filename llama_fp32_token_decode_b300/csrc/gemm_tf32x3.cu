@@ -134,7 +134,7 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 4;  // 16 KB
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
-    static constexpr int STAGES = (BN == 128) ? 3 : 4;  // deepest ring that fits
+    static constexpr int STAGES = (BN >= 256) ? 2 : (BN == 128) ? 3 : 4;  // deepest ring that fits
     // TMEM columns: one accumulator, or two when chunks are drained
     __host__ __device__ static constexpr uint32_t tmem_cols(bool drain) {
         return drain ? 2 * BN : BN;
@@ -776,15 +776,23 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
                               m.b_lo, g);
 }
 
+// Tiles wider than 128 columns have no drained variant (its register copy of
+// the tile row would not fit): they serve only K ranges of at most
+// kDrainAbove K-blocks per CTA.
+template <int BN>
+constexpr bool has_drain() { return BN <= 128; }
+
 template <int BN, int EPI>
 cudaError_t set_smem() {
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynSmem));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kMaxDynSmem));
+    if constexpr (has_drain<BN>())
+        e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kMaxDynSmem));
+    return e;
 }
 
 template <int BN>
@@ -816,7 +824,10 @@ cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cud
                       bool pdl) {
     const int KB = (g.K + 31) / 32;
     const int per_cta = (KB + ks - 1) / ks;
-    if (per_cta > kDrainAbove) return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
+    if (per_cta > kDrainAbove) {
+        if constexpr (has_drain<BN>()) return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
+        return cudaErrorInvalidValue;
+    }
     return launch_bd<BN, false>(epi, m, g, ks, s, pdl);
 }
 
@@ -856,7 +867,7 @@ template <int BN>
 int active_clusters(int ksplit, int stages) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ksplit, 1024);
-    cfg.blockDim = dim3(gemm_threads(true));
+    cfg.blockDim = dim3(gemm_threads(has_drain<BN>()));
     cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages, ksplit);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -866,8 +877,8 @@ int active_clusters(int ksplit, int stages) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE, true>, &cfg) !=
-        cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(
+            &n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE, has_drain<BN>()>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -880,6 +891,7 @@ int active_clusters(int ksplit, int stages) {
 cudaError_t prepare_gemm(GemmOccupancy* occ) {
     cudaError_t e = set_smem_bn<64>();
     if (e == cudaSuccess) e = set_smem_bn<128>();
+    if (e == cudaSuccess) e = set_smem_bn<256>();
     if (e != cudaSuccess || occ == nullptr) return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -890,6 +902,7 @@ cudaError_t prepare_gemm(GemmOccupancy* occ) {
         for (int st = 2; st <= 4; ++st) {
             occ->clusters[0][sp][st] = fits<64>(st, sp) ? active_clusters<64>(sp, st) : 0;
             occ->clusters[1][sp][st] = fits<128>(st, sp) ? active_clusters<128>(sp, st) : 0;
+            occ->clusters[2][sp][st] = fits<256>(st, sp) ? active_clusters<256>(sp, st) : 0;
         }
     return cudaSuccess;
 }
@@ -899,33 +912,53 @@ cudaError_t prepare_gemm(GemmOccupancy* occ) {
 // holds one CTA's K-blocks, at least 2 and at most what fits. (Measured on the
 // batched decode GEMMs: two co-resident CTAs per SM with 2-slot rings are no
 // faster than one CTA per SM with a deeper ring.)
+// The ring depth, whether a ring fits, and the occupancy table row of a tile width.
+int max_stages(int bn) {
+    return bn == 256 ? Cfg<256>::STAGES : bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+}
+bool fits_bn(int bn, int stages, int ksplit) {
+    return bn == 256 ? fits<256>(stages, ksplit)
+           : bn == 128 ? fits<128>(stages, ksplit)
+                       : fits<64>(stages, ksplit);
+}
+int bn_row(int bn) { return bn == 256 ? 2 : bn == 128 ? 1 : 0; }
+
+// ksplit == 0 in the result: no plan with this tile width (a 256-wide tile
+// needs a split that leaves each CTA at most kDrainAbove K-blocks and fits).
 GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
     const int KB = (K + 31) / 32, mt = (M + 127) / 128;
     const int tiles = mt * ((N + bn - 1) / bn);
-    const int max_st = bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+    const int max_st = max_stages(bn);
+    const bool drainable = bn <= 128;
     auto depth = [&](int sp) {
         const int per = (KB + sp - 1) / sp;
         int st = per < 2 ? 2 : per > max_st ? max_st : per;
-        while (st > 2 && !(bn == 128 ? fits<128>(st, sp) : fits<64>(st, sp))) --st;
+        while (st > 2 && !fits_bn(bn, st, sp)) --st;
         return st;
     };
+    auto ok = [&](int sp) { return drainable || (KB + sp - 1) / sp <= kDrainAbove; };
     for (int sp = 8; sp > 1; --sp) {
-        if (KB / sp < 2) continue;
+        if (KB / sp < 2 || !ok(sp)) continue;
         const int st = depth(sp);
-        if (tiles <= occ.clusters[bn == 128][sp][st]) return GemmPlan{bn, sp, st};
+        if (fits_bn(bn, st, sp) && tiles <= occ.clusters[bn_row(bn)][sp][st])
+            return GemmPlan{bn, sp, st};
     }
+    if (!ok(1) || !fits_bn(bn, depth(1), 1)) return GemmPlan{bn, 0, 2};
     return GemmPlan{bn, 1, depth(1)};
 }
 
 // Tile width and split of an M x N x K GEMM: the plan that keeps more SMs
 // busy in its first wave wins, ties going to the wider tile (fewer
-// activation re-reads).
+// activation re-reads, and fewer waves when the tiles outnumber the SMs: the
+// 256 x 32000 classifier runs 250 tiles of 256 columns in two rounds instead
+// of 500 of 128 in four).
 GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K) {
     GemmPlan best{128, 1, Cfg<128>::STAGES};
     long long best_ctas = -1;
     const int mt = (M + 127) / 128;
-    for (int bn : {128, 64}) {
+    for (int bn : {256, 128, 64}) {
         const GemmPlan p = plan_split(occ, bn, M, N, K);
+        if (p.ksplit < 1) continue;
         long long ctas = static_cast<long long>(mt) * ((N + bn - 1) / bn) * p.ksplit;
         if (ctas > occ.num_sms) ctas = occ.num_sms;
         if (ctas > best_ctas) {
@@ -938,12 +971,13 @@ GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K) {
 
 cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g0,
                         cudaStream_t s, bool pdl) {
-    const int max_st = p.bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+    const int max_st = max_stages(p.bn);
     if (g0.M < 1 || g0.N < 1 || g0.K < 4 || g0.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8 ||
         p.stages < 2 || p.stages > max_st)
         return cudaErrorInvalidValue;
     GemmArgs g = g0;
     g.stages = p.stages;
+    if (p.bn == 256) return launch_bn<256>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 128) return launch_bn<128>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 64) return launch_bn<64>(epi, m, g, p.ksplit, s, pdl);
     return cudaErrorInvalidValue;

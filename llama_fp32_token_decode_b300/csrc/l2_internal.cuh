@@ -337,7 +337,7 @@ struct GemmPlan {
 // Clusters of each (tile width, split, ring depth) that the device runs at
 // once, measured with cudaOccupancyMaxActiveClusters at set-up.
 struct GemmOccupancy {
-    int clusters[2][9][5];  // [bn == 128][ksplit][stages]
+    int clusters[3][9][5];  // [tile width 64 / 128 / 256][ksplit][stages]
     int num_sms;
 };
 cudaError_t prepare_gemm(GemmOccupancy* occ);
