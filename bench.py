@@ -115,6 +115,28 @@ def workload_bytes_per_forward(cfg, pos: float) -> float:
     return 4.0 * (weights + d + kv)
 
 
+def batched_run_bound(cfg, lens, steps: int, B: int, hbm_gbs: float, p3_tflops: float):
+    """Lower bound (seconds) of one batched generation run, phase by phase.
+
+    Lockstep step t runs every sequence at position t; sequence b is active
+    for t < lens[b] + steps - 1 (inactive rows stay in the GEMMs). A step's
+    GEMM phase cannot beat max(its fp32 weights once / HBM, its FLOPs on all
+    B rows / 3xTF32 peak); its attention phase cannot beat the KV bytes of the
+    active rows (read positions 0..t, write position t) / HBM. The phases are
+    dependent, so their bounds add; the embedding rows and norm vectors are
+    counted with the weights."""
+    d, F, L, V = cfg["dim"], cfg["hidden_dim"], cfg["n_layers"], cfg["vocab_size"]
+    kvd = cfg["n_kv_heads"] * (d // cfg["n_heads"])
+    weights = 4.0 * (L * (2 * d * d + 2 * d * kvd + 3 * d * F + 2 * d) + d + V * d + B * d)
+    flops = 2.0 * B * (L * (d * (d + 2 * kvd) + d * d + 3 * d * F) + V * d)
+    gemm_s = max(weights / (hbm_gbs * 1e9), flops / (p3_tflops * 1e12))
+    n_lock = int(lens.max()) + steps - 1
+    t = np.arange(n_lock)
+    active = (t[:, None] < (lens[None, :] + steps - 1)).sum(axis=1)
+    kv_bytes = 4.0 * L * 2 * kvd * active * (t + 2)  # read t + 1 rows, write 1
+    return n_lock * gemm_s + float(kv_bytes.sum()) / (hbm_gbs * 1e9), n_lock * gemm_s
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
@@ -603,6 +625,13 @@ def run_ours_batched(args, world, rank, local, compact=False):
                  "unit": "GB/s", "frac": attn["bytes"] / (attn["launch_ms"] / 1e3) / 1e9 / hbm,
                  "pos": pos_mid}
     kernels = {v["name"]: round(v["ms_per_step"] / total_ms, 4) for v in per.values()}
+    bound_s, gemm_bound_s = batched_run_bound(cfg, lens, steps, B, hbm, p3)
+    run_s = ms_max / args.steps / 1e3
+    step_roof = {"bound_ms": bound_s * 1e3, "gemm_phases_bound_ms": gemm_bound_s * 1e3,
+                 "measured_ms": run_s * 1e3, "frac": bound_s / run_s,
+                 "roofline_tok_s": n_fwd / bound_s,
+                 "note": "sum over lockstep steps of max(fp32 weights / HBM, GEMM FLOPs / "
+                         "3xTF32 peak) + active rows' KV bytes / HBM"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -635,6 +664,7 @@ def run_ours_batched(args, world, rank, local, compact=False):
                            B * 2 * L * cfg["seq_len"] * cfg["dim"] * 4 / 1e9)},
             "roofline": roofline, "gemm_phase_roofline": gemm_phase,
             "attention_roofline": attn_roof, "kernel_time_shares": kernels,
+            "step_roofline": step_roof,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * (1 + n_lock * (2 + 7 * L + 1))}
     if compact:
