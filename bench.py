@@ -514,7 +514,7 @@ def run_ours(args, world, rank, local):
 BATCHED_KINDS = {  # batched kernel kinds of l2_time_kernel and their launches per step
     6: "QKV GEMM (+RoPE, KV append)", 7: "attention", 8: "Wo GEMM (+residual)",
     9: "W1/W3 GEMM (+SwiGLU)", 10: "W2 GEMM (+residual)", 11: "classifier GEMM (+argmax)",
-    12: "RMSNorm"}
+    12: "embedding gather"}
 
 
 def batched_gemm_shape(cfg, kind):
@@ -594,7 +594,7 @@ def run_ours_batched(args, world, rank, local, compact=False):
     per = {}
     for kind, name in BATCHED_KINDS.items():
         t = l2.l2_time_kernel(dec.h, kind, pos_mid, 3 * L, stream)
-        launches = {11: 1, 12: 2 * L + 1}.get(kind, L)
+        launches = {11: 1, 12: 1}.get(kind, L)
         shp = batched_gemm_shape(cfg, kind)
         flops = 2.0 * B * shp[0] * shp[1] if shp else 0.0
         per[kind] = {"name": name, "launch_ms": t, "launches_per_step": launches,
@@ -666,7 +666,7 @@ def run_ours_batched(args, world, rank, local, compact=False):
             "attention_roofline": attn_roof, "kernel_time_shares": kernels,
             "step_roofline": step_roof,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps * (1 + n_lock * (2 + 7 * L + 1))}
+            "gpu_launches": args.steps * (1 + n_lock * (2 + 5 * L + 1))}
     if compact:
         for k in ("steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data",
                   "n_gpus"):

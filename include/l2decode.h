@@ -234,7 +234,9 @@ L2_API const char* l2_last_error(const l2_handle* h);
  * 1 attention, 2 Wo+residual, 3 W1/W3+SwiGLU, 4 W2+residual,
  * 5 classifier+argmax. Batched kinds (handles with max_batch > 1; all
  * max_batch rows at position pos): 6 QKV GEMM, 7 attention, 8 Wo GEMM,
- * 9 W1/W3 GEMM, 10 W2 GEMM, 11 classifier GEMM + argmax, 12 RMSNorm,
+ * 9 W1/W3 GEMM, 10 W2 GEMM, 11 classifier GEMM + argmax, 12 embedding gather
+ * (residual rows, their tf32 pair and sums of squares; the RMSNorms are folded
+ * into the GEMMs that consume them),
  * 13 advance. It reads and writes the handle's own run state (the KV cache
  * contents are left as they were, except slot `pos` of the caches used).
  * Errors: L2_EINVAL, L2_ECUDA. Synchronous. */

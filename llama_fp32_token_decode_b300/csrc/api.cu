@@ -64,6 +64,11 @@ struct l2_handle {
     int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
     int* b_seq = nullptr;              // KV cache of each row (prefill: all 0)
     unsigned long long* b_keys = nullptr;
+    // sums of squares of the rows entering a folded RMSNorm, [Mcap][ss_stride]:
+    // ss_att (from the embedding gather or W2, read by QKV and the classifier)
+    // and ss_ffn (from Wo, read by W1/W3)
+    float *ss_att = nullptr, *ss_ffn = nullptr;
+    int ss_stride = 0;
     GemmMaps m_qkv{}, m_wo{}, m_w13{}, m_w2{}, m_cls{};
     GemmPlan gp_qkv{64, 1, 2}, gp_wo{64, 1, 2}, gp_w13{64, 1, 2}, gp_w2{64, 1, 2}, gp_cls{128, 1, 2};
     GemmOccupancy gocc{};
@@ -269,15 +274,16 @@ int check_device_error(l2_handle* h) {
 // Kernel kinds of a batched step (l2_time_kernel numbers them 6 + kind).
 enum BKind : int {
     BK_QKV = 0, BK_ATTN = 1, BK_WO = 2, BK_W13 = 3, BK_W2 = 4, BK_CLS = 5,
-    BK_NORM = 6,      // RMSNorm of the residual rows with gain `gain_sel`
+    BK_EMB = 6,  // embedding gather: residual rows, their tf32 pair, sums of squares
     BK_ADVANCE = 7,
-    BK_NORM_EMB = 8,  // embedding gather + RMSNorm (step start)
 };
 
-// Launches one kernel of a batched step for layer l on M rows. For BK_NORM the
-// gain is g_ffn[l] (gain_next == false) or the next layer's g_att / g_final.
+// Partial sums of squares a residual GEMM with this plan writes per row.
+int ss_slots(const GemmPlan& p, int N) { return 2 * ((N + p.bn - 1) / p.bn); }
+
+// Launches one kernel of a batched step for layer l on M rows.
 cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mode, int steps,
-                         bool want_logits, bool gain_next, cudaStream_t s, bool prefill = false) {
+                         bool want_logits, cudaStream_t s, bool prefill = false) {
     const l2_config& c = h->cfg;
     const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
     GemmArgs g{};
@@ -288,22 +294,18 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
     // tile width fixed at create (it is the weight maps' box); K split for this M
     auto plan = [&](const GemmPlan& p, int N, int K) { return plan_split(h->gocc, p.bn, M, N, K); };
     switch (kind) {
-        case BK_NORM_EMB:
-        case BK_NORM: {
+        case BK_EMB: {
             BNormArgs n{};
             n.row0 = row0;
             n.x = h->bx;
-            n.emb = kind == BK_NORM_EMB ? h->emb : nullptr;
+            n.emb = h->emb;
             n.token = h->b_token;
-            n.gain = kind == BK_NORM_EMB ? h->g_att
-                     : !gain_next        ? h->g_ffn + static_cast<size_t>(l) * d
-                     : (l + 1 < L)       ? h->g_att + static_cast<size_t>(l + 1) * d
-                                         : h->g_final;
             n.xn_hi = h->xn_hi;
             n.xn_lo = h->xn_lo;
+            n.ss_out = h->ss_att;
+            n.ss_stride = h->ss_stride;
             n.d = d;
             n.vocab = V;
-            n.eps = c.norm_eps;
             return launch_brmsnorm(n, M, s, true);
         }
         case BK_QKV:
@@ -321,6 +323,10 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.head_dim = h->hd;
             g.seq_len = c.seq_len;
             g.cache_seq = h->cache_seq;
+            g.ss_in = h->ss_att;  // attention RMSNorm (gain in the weights)
+            g.ss_count = l == 0 ? 1 : ss_slots(h->gp_w2, d);
+            g.ss_stride = h->ss_stride;
+            g.eps = c.norm_eps;
             return launch_gemm(GEPI_QKV_ROPE, plan(h->gp_qkv, g.N, g.K), h->m_qkv, g, s, true);
         case BK_ATTN: {
             BAttnArgs t{};
@@ -346,18 +352,30 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.K = d;
             g.out = h->bx;
             g.ldc = d;
+            g.x_hi = h->xn_hi;  // the W1/W3 GEMM's rows and their sums of squares
+            g.x_lo = h->xn_lo;
+            g.ss_out = h->ss_ffn;
+            g.ss_stride = h->ss_stride;
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_wo, g.N, g.K), h->m_wo, g, s, true);
         case BK_W13:
             g.N = 2 * F;
             g.K = d;
             g.out_hi = h->hb_hi;
             g.out_lo = h->hb_lo;
+            g.ss_in = h->ss_ffn;  // FFN RMSNorm (gain in the weights)
+            g.ss_count = ss_slots(h->gp_wo, d);
+            g.ss_stride = h->ss_stride;
+            g.eps = c.norm_eps;
             return launch_gemm(GEPI_SWIGLU, plan(h->gp_w13, g.N, g.K), h->m_w13, g, s, true);
         case BK_W2:
             g.N = d;
             g.K = F;
             g.out = h->bx;
             g.ldc = d;
+            g.x_hi = h->xn_hi;  // the next QKV (or classifier) GEMM's rows and sums of squares
+            g.x_lo = h->xn_lo;
+            g.ss_out = h->ss_att;
+            g.ss_stride = h->ss_stride;
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_w2, g.N, g.K), h->m_w2, g, s, true);
         case BK_CLS:
             g.layer = 0;
@@ -366,6 +384,10 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.out = want_logits ? h->blogits : nullptr;
             g.ldc = V;
             g.argmax_keys = h->b_keys;
+            g.ss_in = h->ss_att;  // final RMSNorm (gain in the weights)
+            g.ss_count = ss_slots(h->gp_w2, d);
+            g.ss_stride = h->ss_stride;
+            g.eps = c.norm_eps;
             return launch_gemm(GEPI_ARGMAX, plan(h->gp_cls, g.N, g.K), h->m_cls, g, s, true);
         case BK_ADVANCE: {
             BAdvanceArgs a{};
@@ -389,25 +411,24 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
     }
 }
 
-// Kernels of one lockstep step of rows [row0, row0 + M), in order: embedding
-// + RMSNorm, then per layer the QKV GEMM (RoPE + KV append), attention, Wo
-// GEMM + residual, RMSNorm, W1/W3 GEMM + SwiGLU, W2 GEMM + residual, RMSNorm;
-// the classifier GEMM with the per-row argmax; and the per-sequence advance.
+// Kernels of one lockstep step of rows [row0, row0 + M), in order: the
+// embedding gather, then per layer the QKV GEMM (attention RMSNorm folded in;
+// RoPE + KV append), attention, Wo GEMM + residual, W1/W3 GEMM (FFN RMSNorm
+// folded in; SwiGLU), W2 GEMM + residual; the classifier GEMM (final RMSNorm
+// folded in) with the per-row argmax; and the per-sequence advance.
 // `prefill`: every row is a position of sequence 0 (cache 0, row positions
 // in b_pos) instead of a sequence of its own.
 cudaError_t enqueue_rows(l2_handle* h, int row0, int M, int mode, int steps, bool want_logits,
                          cudaStream_t s, bool prefill = false) {
-    cudaError_t e =
-        launch_bkind(h, BK_NORM_EMB, 0, row0, M, mode, steps, want_logits, false, s, prefill);
+    cudaError_t e = launch_bkind(h, BK_EMB, 0, row0, M, mode, steps, want_logits, s, prefill);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
-        const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_NORM, BK_W13, BK_W2, BK_NORM};
-        for (int i = 0; i < 7 && e == cudaSuccess; ++i)
-            e = launch_bkind(h, seq[i], l, row0, M, mode, steps, want_logits, i == 6, s, prefill);
+        const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_W13, BK_W2};
+        for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+            e = launch_bkind(h, seq[i], l, row0, M, mode, steps, want_logits, s, prefill);
     }
+    if (e == cudaSuccess) e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, s, prefill);
     if (e == cudaSuccess)
-        e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, false, s, prefill);
-    if (e == cudaSuccess)
-        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, false, s, prefill);
+        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, s, prefill);
     return e;
 }
 
@@ -503,21 +524,26 @@ int setup_batched(l2_handle* h) {
     h->cls_hi = h->bw + o_ch; h->cls_lo = h->bw + o_cl;
     cudaStream_t s = h->stream;
     L2_CUDA(h, prepare_gemm(&h->gocc));
-    L2_CUDA(h, launch_split_tf32(h->wqkv, h->qkv_hi, h->qkv_lo, n_qkv, s));
+    // the GEMMs that consume a normalised row carry the RMSNorm gain in their
+    // weights (W[n][k] * g[k]); the row scale is applied in their epilogue
+    L2_CUDA(h, launch_split_tf32_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, h->qkv_lo, s));
     L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
-    L2_CUDA(h, launch_split_tf32(h->w13, h->w13_hi, h->w13_lo, n_w13, s));
+    L2_CUDA(h, launch_split_tf32_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, h->w13_lo, s));
     L2_CUDA(h, launch_split_tf32(h->w2, h->w2_hi, h->w2_lo, n_w2, s));
-    L2_CUDA(h, launch_split_tf32(h->wcls, h->cls_hi, h->cls_lo, n_cls, s));
+    L2_CUDA(h, launch_split_tf32_gain(h->wcls, h->g_final, d, V, 1, h->cls_hi, h->cls_lo, s));
 
     off = 0;
     const size_t o_x = take(Mc * d), o_nh = take(Mc * d), o_nl = take(Mc * d), o_q = take(Mc * d);
     const size_t o_ah = take(Mc * d), o_al = take(Mc * d), o_hh = take(Mc * F), o_hl = take(Mc * F);
     const size_t o_lg = take(RW * V);
+    h->ss_stride = static_cast<int>(2 * ((d + 63) / 64));  // two slots per N tile of >= 64
+    const size_t o_ssa = take(Mc * h->ss_stride), o_ssf = take(Mc * h->ss_stride);
     L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
     L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));
     h->bx = h->bact + o_x; h->xn_hi = h->bact + o_nh; h->xn_lo = h->bact + o_nl;
     h->bq = h->bact + o_q; h->att_hi = h->bact + o_ah; h->att_lo = h->bact + o_al;
     h->hb_hi = h->bact + o_hh; h->hb_lo = h->bact + o_hl; h->blogits = h->bact + o_lg;
+    h->ss_att = h->bact + o_ssa; h->ss_ffn = h->bact + o_ssf;
 
     off = 0;
     const size_t o_pos = take(Mc), o_tok = take(Mc), o_act = take(Mc), o_len = take(Mc);
@@ -533,9 +559,10 @@ int setup_batched(l2_handle* h) {
 
     const int Mb = static_cast<int>(RW);
     h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
-    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d));
+    // Wo and W2 write the per-row sums of squares of the next norm: tiles <= 128
+    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d), 128);
     h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d));
-    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F));
+    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128);
     h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d));
     const long long D = d, FF = F, LL = L, MC = Mc;
     struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
@@ -1208,10 +1235,10 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
         bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
                                                     h->b_keys, h->st);
         L2_CUDA(h, cudaGetLastError());
-        L2_CUDA(h, launch_bkind(h, bk, 0, 0, M, 0, 0, false, false, s));
+        L2_CUDA(h, launch_bkind(h, bk, 0, 0, M, 0, 0, false, s));
         L2_CUDA(h, cudaEventRecord(h->ev0, s));
         for (int i = 0; i < iters; ++i)
-            L2_CUDA(h, launch_bkind(h, bk, i % h->cfg.n_layers, 0, M, 0, 0, false, false, s));
+            L2_CUDA(h, launch_bkind(h, bk, i % h->cfg.n_layers, 0, M, 0, 0, false, s));
         L2_CUDA(h, cudaEventRecord(h->ev1, s));
         L2_CUDA(h, cudaEventSynchronize(h->ev1));
         float t = 0.0f;
@@ -1256,7 +1283,7 @@ double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
         case 9: return 4.0 * (2 * F * d + M * d + M * F);
         case 10: return 4.0 * (d * F + M * F + 2 * M * d);
         case 11: return 4.0 * (V * d + M * d);
-        case 12: return 4.0 * (2 * M * d + d);
+        case 12: return 4.0 * (4 * M * d + M);  // embedding rows in; x, its pair, sums out
         case 13: return 4.0 * 6 * M;
         default: return 0.0;
     }

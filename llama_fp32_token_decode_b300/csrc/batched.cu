@@ -3,8 +3,11 @@
 // position, token and KV cache (the decode step of the llama2.c pages' fp32
 // engine, applied to B sequences at once). The projections of the step run in
 // the 3xTF32 tensor-core GEMM (gemm_tf32x3.cu); this file holds
-//   brmsnorm_kernel   optional embedding gather + RMSNorm, writing the
-//                     normalised rows as tf32 (hi, lo) pairs for the next GEMM
+//   brmsnorm_kernel   embedding gather at the start of a step: the residual
+//                     rows, their tf32 (hi, lo) pairs and sums of squares for
+//                     the first QKV GEMM (every RMSNorm of the step is folded
+//                     into the GEMM that consumes it: gains into the weights,
+//                     the row scale into its epilogue)
 //   battn_kernel      causal attention of every (row, head) over the row's KV
 //                     cache (its own sequence's; in a prefill every row is a
 //                     position of one sequence), ragged lengths pos + 1,
@@ -29,37 +32,29 @@ __global__ void __launch_bounds__(kNormThreads) brmsnorm_kernel(const BNormArgs 
     const int b = a.row0 + blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, d4 = d >> 2;
     float4* x4 = reinterpret_cast<float4*>(a.x + static_cast<size_t>(b) * d);
-    const float4* src4 = x4;
-    if (a.emb != nullptr) {
-        const int tok = min(max(__ldcg(a.token + b), 0), a.vocab - 1);
-        src4 = reinterpret_cast<const float4*>(a.emb + static_cast<size_t>(tok) * d);
-    }
+    const int tok = min(max(__ldcg(a.token + b), 0), a.vocab - 1);
+    const float4* src4 = reinterpret_cast<const float4*>(a.emb + static_cast<size_t>(tok) * d);
+    float4* hi4 = reinterpret_cast<float4*>(a.xn_hi + static_cast<size_t>(b) * d);
+    float4* lo4 = reinterpret_cast<float4*>(a.xn_lo + static_cast<size_t>(b) * d);
     __shared__ float s_part[kNormThreads / 32];
     float ss = 0.0f;
     for (int i = tid; i < d4; i += kNormThreads) {
         const float4 v = __ldcg(src4 + i);
+        x4[i] = v;
+        const float4 h = make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z), tf32_round(v.w));
+        hi4[i] = h;
+        lo4[i] = make_float4(tf32_round(v.x - h.x), tf32_round(v.y - h.y), tf32_round(v.z - h.z),
+                             tf32_round(v.w - h.w));
         ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
     ss = warp_sum(ss);
     if (lane == 0) s_part[warp] = ss;
     __syncthreads();
-    float tot = 0.0f;
+    if (tid == 0) {
+        float tot = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(d) + a.eps);
-    const float4* g4 = reinterpret_cast<const float4*>(a.gain);
-    float4* hi4 = reinterpret_cast<float4*>(a.xn_hi + static_cast<size_t>(b) * d);
-    float4* lo4 = reinterpret_cast<float4*>(a.xn_lo + static_cast<size_t>(b) * d);
-    for (int i = tid; i < d4; i += kNormThreads) {
-        const float4 v = __ldcg(src4 + i);
-        if (a.emb != nullptr) x4[i] = v;
-        const float4 g = __ldg(g4 + i);
-        const float n0 = g.x * (inv * v.x), n1 = g.y * (inv * v.y);
-        const float n2 = g.z * (inv * v.z), n3 = g.w * (inv * v.w);
-        const float4 h = make_float4(tf32_round(n0), tf32_round(n1), tf32_round(n2), tf32_round(n3));
-        hi4[i] = h;
-        lo4[i] = make_float4(tf32_round(n0 - h.x), tf32_round(n1 - h.y), tf32_round(n2 - h.z),
-                             tf32_round(n3 - h.w));
+        for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
+        a.ss_out[static_cast<size_t>(b) * a.ss_stride] = tot;
     }
 }
 
@@ -333,7 +328,8 @@ cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, const Args& a, cudaStrea
 }  // namespace
 
 cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl) {
-    if (M < 1 || a.d % 4 != 0) return cudaErrorInvalidValue;
+    if (M < 1 || a.d % 4 != 0 || a.emb == nullptr || a.ss_out == nullptr || a.ss_stride < 1)
+        return cudaErrorInvalidValue;
     return launch_pdl(brmsnorm_kernel, dim3(M), dim3(kNormThreads), a, s, pdl);
 }
 

@@ -125,8 +125,8 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 }
 
 // Dynamic shared memory one CTA may use (227 KB opt-in, minus static use:
-// the row-state arrays and the error flag).
-constexpr size_t kMaxDynSmem = 227 * 1024 - 2048;
+// the row-state and row-scale arrays and the error flag).
+constexpr size_t kMaxDynSmem = 227 * 1024 - 3072;
 
 template <int BN>
 struct Cfg {
@@ -229,26 +229,54 @@ __device__ __forceinline__ EpiPre epi_pre(const GemmArgs& g, int r, int gc, cons
 
 // Fused epilogue of four consecutive output columns gc..gc+3 (gc % 4 == 0) of
 // row r. rs: the row's state (QKV only); pre: from epi_pre for the same group.
-// ARGMAX folds the columns into `best`; the caller publishes it.
+// ARGMAX folds the columns into `best`; the caller publishes it. Returns the
+// sum of squares of the residual values written (RESIDUAL with x_hi set),
+// else 0.
 template <int EPI>
-__device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const float (&a)[4],
-                                     const RowState& rs, const EpiPre& pre,
-                                     unsigned long long& best) {
+__device__ __forceinline__ float epi4(const GemmArgs& g, int r, int gc, const float (&a)[4],
+                                      const RowState& rs, const EpiPre& pre,
+                                      unsigned long long& best) {
     if constexpr (EPI == GEPI_STORE || EPI == GEPI_RESIDUAL) {
         float* o = g.out + static_cast<size_t>(r) * g.ldc + gc;
+        float w4[4] = {a[0], a[1], a[2], a[3]};
+        int nw = 4;
         if (gc + 4 <= g.N && (g.ldc & 3) == 0) {
-            float4 w = make_float4(a[0], a[1], a[2], a[3]);
             if constexpr (EPI == GEPI_RESIDUAL) {
-                const float4 x = pre.x;
-                w.x += x.x;
-                w.y += x.y;
-                w.z += x.z;
-                w.w += x.w;
+                w4[0] += pre.x.x;
+                w4[1] += pre.x.y;
+                w4[2] += pre.x.z;
+                w4[3] += pre.x.w;
             }
-            *reinterpret_cast<float4*>(o) = w;
+            *reinterpret_cast<float4*>(o) = make_float4(w4[0], w4[1], w4[2], w4[3]);
         } else {
-            for (int j = 0; j < 4 && gc + j < g.N; ++j)
-                o[j] = (EPI == GEPI_RESIDUAL) ? __ldcg(o + j) + a[j] : a[j];
+            nw = 0;
+            for (int j = 0; j < 4 && gc + j < g.N; ++j, ++nw) {
+                w4[j] = (EPI == GEPI_RESIDUAL) ? __ldcg(o + j) + a[j] : a[j];
+                o[j] = w4[j];
+            }
+        }
+        if constexpr (EPI == GEPI_RESIDUAL) {
+            if (g.x_hi != nullptr) {  // the rows the next (norm-folded) GEMM reads
+                float ss = 0.0f;
+                float* xh = g.x_hi + static_cast<size_t>(r) * g.ldc + gc;
+                float* xl = g.x_lo + static_cast<size_t>(r) * g.ldc + gc;
+                if (nw == 4 && (g.ldc & 3) == 0) {
+                    const float4 h = make_float4(tf32_round(w4[0]), tf32_round(w4[1]),
+                                                 tf32_round(w4[2]), tf32_round(w4[3]));
+                    *reinterpret_cast<float4*>(xh) = h;
+                    *reinterpret_cast<float4*>(xl) =
+                        make_float4(tf32_round(w4[0] - h.x), tf32_round(w4[1] - h.y),
+                                    tf32_round(w4[2] - h.z), tf32_round(w4[3] - h.w));
+                } else {
+                    for (int j = 0; j < nw; ++j) {
+                        const float h = tf32_round(w4[j]);
+                        xh[j] = h;
+                        xl[j] = tf32_round(w4[j] - h);
+                    }
+                }
+                for (int j = 0; j < nw; ++j) ss = fmaf(w4[j], w4[j], ss);
+                return ss;
+            }
         }
     } else if constexpr (EPI == GEPI_SWIGLU) {
         // interleaved rows: column 2j is the gate, 2j+1 the up projection
@@ -272,7 +300,7 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
             }
         }
     } else if constexpr (EPI == GEPI_QKV_ROPE) {
-        if (!rs.active) return;
+        if (!rs.active) return 0.0f;
         const int hd = g.head_dim, pos = rs.pos;
 #pragma unroll
         for (int j = 0; j < 4; j += 2) {
@@ -309,6 +337,16 @@ __device__ __forceinline__ void epi4(const GemmArgs& g, int r, int gc, const flo
             }
         }
     }
+    return 0.0f;
+}
+
+// Scale of row r of a norm-folded GEMM: 1 / sqrt(mean of x[r]^2 + eps), the
+// sum of squares being the producer's partials added in slot order.
+__device__ __forceinline__ float row_scale(const GemmArgs& g, int r) {
+    const float* p = g.ss_in + static_cast<size_t>(r) * g.ss_stride;
+    float ss = 0.0f;
+    for (int j = 0; j < g.ss_count; ++j) ss += __ldcg(p + j);
+    return 1.0f / sqrtf(ss / static_cast<float>(g.K) + g.eps);
 }
 
 // Row r's state, read from the arrays the previous kernels wrote.
@@ -379,6 +417,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     __shared__ int s_err;
     // QKV epilogue: state of the tile's rows, loaded once during the mainloop
     __shared__ RowState s_rows[EPI == GEPI_QKV_ROPE ? 128 : 1];
+    // norm-folded consumers (g.ss_in set): the tile's row scales, likewise
+    __shared__ float s_scale[EPI == GEPI_RESIDUAL || EPI == GEPI_STORE ? 1 : 128];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = (g.M + 127) / 128;
@@ -506,11 +546,24 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             for (int i = lane; i < 128; i += 32)
                 if (m0 + i < m_end) s_rows[i] = load_row_state(g, m0 + i);
         }
+        if constexpr (EPI != GEPI_RESIDUAL && EPI != GEPI_STORE) {
+            if (warp == 3 && g.ss_in != nullptr) {  // ... and warp 3 the row scales
+                pdl_wait();
+                for (int i = lane; i < 128; i += 32)
+                    if (m0 + i < m_end) s_scale[i] = row_scale(g, m0 + i);
+            }
+        }
     } else {
         // ---- warps 0-3: drain every chunk into registers (fp32 round-to-nearest adds)
         if (EPI == GEPI_QKV_ROPE && m0 + threadIdx.x < m_end) {
             pdl_wait();
             s_rows[threadIdx.x] = load_row_state(g, m0 + threadIdx.x);
+        }
+        if constexpr (EPI != GEPI_RESIDUAL && EPI != GEPI_STORE) {
+            if (g.ss_in != nullptr && m0 + threadIdx.x < m_end) {
+                pdl_wait();
+                s_scale[threadIdx.x] = row_scale(g, m0 + threadIdx.x);
+            }
         }
         const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
         for (int c = 0; c < NCH; ++c) {
@@ -552,6 +605,11 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         if constexpr (EPI == GEPI_QKV_ROPE) return s_rows[lr];
         return RowState{0, 1, 0};
     };
+    auto rscale = [&](int lr) {
+        if constexpr (EPI == GEPI_RESIDUAL || EPI == GEPI_STORE) return 1.0f;
+        return g.ss_in != nullptr ? s_scale[lr] : 1.0f;
+    };
+    const int ss_slot = 2 * (n0 / BN);  // this tile's sum-of-squares slots
 
     if (nsplit == 1) {
         if (s_err) {
@@ -560,15 +618,18 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             const int r = m0 + row;
             const bool row_ok = r < m_end;
             const RowState rs = row_ok ? rstate(row) : RowState{0, 0, 0};
+            const float sc = row_ok ? rscale(row) : 1.0f;
             unsigned long long best = 0ull;
+            float ssq = 0.0f;  // RESIDUAL producer: sum of squares of this thread's values
             if constexpr (DRAIN) {
                 if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < BN; j += 4) {
                         const int gc = n0 + j;
                         if (gc < g.N) {
-                            const float a4[4] = {R[j], R[j + 1], R[j + 2], R[j + 3]};
-                            epi4<EPI>(g, r, gc, a4, rs, epi_pre<EPI>(g, r, gc, rs), best);
+                            const float a4[4] = {R[j] * sc, R[j + 1] * sc, R[j + 2] * sc,
+                                                 R[j + 3] * sc};
+                            ssq += epi4<EPI>(g, r, gc, a4, rs, epi_pre<EPI>(g, r, gc, rs), best);
                         }
                     }
                 }
@@ -582,14 +643,27 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                     if (!row_ok || gc0 >= g.N) continue;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        const float a4[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
+                        const float a4[4] = {v[j] * sc, v[j + 1] * sc, v[j + 2] * sc,
+                                             v[j + 3] * sc};
                         if (gc0 + j < g.N)
-                            epi4<EPI>(g, r, gc0 + j, a4, rs, epi_pre<EPI>(g, r, gc0 + j, rs), best);
+                            ssq += epi4<EPI>(g, r, gc0 + j, a4, rs,
+                                             epi_pre<EPI>(g, r, gc0 + j, rs), best);
                     }
                 }
             }
             if constexpr (EPI == GEPI_ARGMAX) {
                 if (row_ok && best != 0ull) atomicMax(g.argmax_keys + r, best);
+            }
+            if constexpr (EPI == GEPI_RESIDUAL) {
+                if (g.ss_out != nullptr && row_ok) {
+                    float* so = g.ss_out + static_cast<size_t>(r) * g.ss_stride + ss_slot;
+                    if constexpr (DRAIN) {
+                        so[0] = ssq;
+                        so[1] = 0.0f;
+                    } else {
+                        so[half] = ssq;  // kHalves == 2: both slots written
+                    }
+                }
             }
         }
     } else {
@@ -665,7 +739,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             const bool got = mbar_wait_bounded(recvb, 0u);
             if (!got) s_err = 1;
             if (!s_err) {
-                for (; t0 < ngroups; t0 += kU * NT) {
+                // warp-uniform trip count (the sum-of-squares reduction shuffles)
+                for (; t0 - lane < ngroups; t0 += kU * NT) {
                     float4 acc[kU];
 #pragma unroll
                     for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -689,14 +764,32 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                     }
 #pragma unroll
                     for (int u = 0; u < kU; ++u) {
-                        if (!ok[u]) continue;
                         const int t = t0 + NT * u;
                         const int r = m0 + lrs[u], gc = n0 + 4 * (t % gpr);
-                        unsigned long long best = 0ull;
-                        const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-                        epi4<EPI>(g, r, gc, a4, rstate(lrs[u]), pre[u], best);
-                        if constexpr (EPI == GEPI_ARGMAX) {
-                            if (best != 0ull) atomicMax(g.argmax_keys + r, best);
+                        float sq = 0.0f;
+                        if (ok[u]) {
+                            unsigned long long best = 0ull;
+                            const float sc = rscale(lrs[u]);
+                            const float a4[4] = {acc[u].x * sc, acc[u].y * sc, acc[u].z * sc,
+                                                 acc[u].w * sc};
+                            sq = epi4<EPI>(g, r, gc, a4, rstate(lrs[u]), pre[u], best);
+                            if constexpr (EPI == GEPI_ARGMAX) {
+                                if (best != 0ull) atomicMax(g.argmax_keys + r, best);
+                            }
+                        }
+                        if constexpr (EPI == GEPI_RESIDUAL) {
+                            if (g.ss_out != nullptr) {
+                                // the gpr lanes of a row (gpr divides 32) add their
+                                // squares in a fixed shuffle tree
+                                for (int o = gpr / 2; o > 0; o >>= 1)
+                                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                                if (ok[u] && t % gpr == 0) {
+                                    float* so = g.ss_out + static_cast<size_t>(r) * g.ss_stride +
+                                                ss_slot;
+                                    so[0] = sq;
+                                    so[1] = 0.0f;
+                                }
+                            }
                         }
                     }
                     if (t0 + kU * NT < ngroups) fetch(t0 + kU * NT);
@@ -728,6 +821,19 @@ __global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restri
         // lo rounded to tf32 as well: the tensor core would otherwise truncate it
         lo[i] = make_float4(tf32_round(v.x - h.x), tf32_round(v.y - h.y), tf32_round(v.z - h.z),
                             tf32_round(v.w - h.w));
+    }
+}
+
+__global__ void split_tf32_gain_kernel(const float* __restrict__ x, const float* __restrict__ gain,
+                                       long long K, long long rows, long long n,
+                                       float* __restrict__ hi, float* __restrict__ lo) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long k = i % K, layer = i / (K * rows);
+        const float v = x[i] * gain[layer * K + k];
+        const float h = tf32_round(v);
+        hi[i] = h;
+        lo[i] = tf32_round(v - h);
     }
 }
 
@@ -951,12 +1057,14 @@ GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
 // busy in its first wave wins, ties going to the wider tile (fewer
 // activation re-reads, and fewer waves when the tiles outnumber the SMs: the
 // 256 x 32000 classifier runs 250 tiles of 256 columns in two rounds instead
-// of 500 of 128 in four).
-GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K) {
-    GemmPlan best{128, 1, Cfg<128>::STAGES};
+// of 500 of 128 in four). max_bn caps the width (a GEMM whose epilogue
+// produces per-row sums of squares needs a tile row within one warp: 128).
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn) {
+    GemmPlan best{64, 1, Cfg<64>::STAGES};
     long long best_ctas = -1;
     const int mt = (M + 127) / 128;
     for (int bn : {256, 128, 64}) {
+        if (bn > max_bn || (bn > 64 && bn > N)) continue;  // a tile wider than N is waste
         const GemmPlan p = plan_split(occ, bn, M, N, K);
         if (p.ksplit < 1) continue;
         long long ctas = static_cast<long long>(mt) * ((N + bn - 1) / bn) * p.ksplit;
@@ -975,12 +1083,26 @@ cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const Gem
     if (g0.M < 1 || g0.N < 1 || g0.K < 4 || g0.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8 ||
         p.stages < 2 || p.stages > max_st)
         return cudaErrorInvalidValue;
+    // a sum-of-squares producer needs a tile row within one warp (gpr <= 32)
+    // and room for two slots per N tile
+    if (g0.ss_out != nullptr &&
+        (p.bn > 128 || 2 * ((g0.N + p.bn - 1) / p.bn) > g0.ss_stride || epi != GEPI_RESIDUAL))
+        return cudaErrorInvalidValue;
     GemmArgs g = g0;
     g.stages = p.stages;
     if (p.bn == 256) return launch_bn<256>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 128) return launch_bn<128>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 64) return launch_bn<64>(epi, m, g, p.ksplit, s, pdl);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_split_tf32_gain(const float* x, const float* gain, long long K, long long rows,
+                                   long long layers, float* hi, float* lo, cudaStream_t s) {
+    if (K < 1 || rows < 1 || layers < 1) return cudaErrorInvalidValue;
+    const long long n = K * rows * layers;
+    const int blocks = static_cast<int>(n / 256 + 1 < 8192 ? n / 256 + 1 : 8192);
+    split_tf32_gain_kernel<<<blocks, 256, 0, s>>>(x, gain, K, rows, n, hi, lo);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s) {

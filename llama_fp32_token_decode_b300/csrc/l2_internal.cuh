@@ -137,19 +137,37 @@ struct GemmArgs {
     unsigned long long* argmax_keys;  // ARGMAX: [M]
     int* err;             // ERR_* bits
     int stages;           // ring depth (set by launch_gemm from the plan)
+    // RMSNorm folded into the GEMM that consumes the normalised rows. The
+    // weights carry the norm gain (W[n][k] * g[k]) and A holds the raw rows x
+    // (tf32 pair), so the consumer scales row r of its result by
+    // 1 / sqrt(ss_r / K + eps), ss_r = the sum of squares of x[r] as the sum of
+    // ss_count partials at ss_in[r * ss_stride] (fixed order). Null: no norm.
+    const float* ss_in;
+    int ss_count, ss_stride;
+    float eps;
+    // RESIDUAL producer of such rows: also writes the new rows as a tf32 pair
+    // (x_hi, x_lo) and its partial sums of squares (two slots per N tile, at
+    // ss_out[r * ss_stride + 2 * tile], the second 0 unless warps split the
+    // tile's columns). Null: not produced.
+    float* x_hi;
+    float* x_lo;
+    float* ss_out;
 };
 
 // Batched decode (batched.cu). Row b of every [M][...] array is sequence b.
+// Start of a batched step: the embedding rows of the tokens become the
+// residual rows x, their tf32 pair (the first QKV GEMM's A operand, the norm
+// being folded into that GEMM) and their sums of squares.
 struct BNormArgs {
     int row0;              // rows row0 .. row0 + gridDim.x - 1
-    float* x;              // [rows][d] residual rows (set to emb[token] when emb != null)
-    const float* emb;      // embedding table [V][d] or null
-    const int* token;      // [M] (used when emb != null)
-    const float* gain;     // [d]
-    float* xn_hi;          // [M][d] normalised rows, tf32 pair
+    float* x;              // [rows][d] residual rows, set to emb[token]
+    const float* emb;      // embedding table [V][d]
+    const int* token;      // [M]
+    float* xn_hi;          // [M][d] x as a tf32 pair
     float* xn_lo;
+    float* ss_out;         // [M][ss_stride]: slot 0 = sum of squares of x[r]
+    int ss_stride;
     int d, vocab;
-    float eps;
 };
 
 struct BAttnArgs {
@@ -341,11 +359,15 @@ struct GemmOccupancy {
     int num_sms;
 };
 cudaError_t prepare_gemm(GemmOccupancy* occ);
-GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K);
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn = 256);
 GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K);
 cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
+// The same split of gain-scaled weights: element k of every row of layer l
+// is multiplied by gain[l * K + k] first ([layers][rows][K] weights).
+cudaError_t launch_split_tf32_gain(const float* x, const float* gain, long long K, long long rows,
+                                   long long layers, float* hi, float* lo, cudaStream_t s);
 
 // batched.cu
 cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl);
