@@ -536,7 +536,8 @@ int setup_batched(l2_handle* h) {
     const size_t o_x = take(Mc * d), o_nh = take(Mc * d), o_nl = take(Mc * d), o_q = take(Mc * d);
     const size_t o_ah = take(Mc * d), o_al = take(Mc * d), o_hh = take(Mc * F), o_hl = take(Mc * F);
     const size_t o_lg = take(RW * V);
-    h->ss_stride = static_cast<int>(2 * ((d + 63) / 64));  // two slots per N tile of >= 64
+    // two slots per N tile of >= 64 columns, rounded up to whole 16-byte groups
+    h->ss_stride = static_cast<int>((2 * ((d + 63) / 64) + 3) / 4 * 4);
     const size_t o_ssa = take(Mc * h->ss_stride), o_ssf = take(Mc * h->ss_stride);
     L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
     L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));

@@ -343,9 +343,19 @@ __device__ __forceinline__ float epi4(const GemmArgs& g, int r, int gc, const fl
 // Scale of row r of a norm-folded GEMM: 1 / sqrt(mean of x[r]^2 + eps), the
 // sum of squares being the producer's partials added in slot order.
 __device__ __forceinline__ float row_scale(const GemmArgs& g, int r) {
-    const float* p = g.ss_in + static_cast<size_t>(r) * g.ss_stride;
+    // ss_stride is a multiple of 4: the slots are read as independent 16-byte loads
+    const float4* p = reinterpret_cast<const float4*>(g.ss_in + static_cast<size_t>(r) * g.ss_stride);
+    const int n = g.ss_count, n4 = (n + 3) >> 2;
     float ss = 0.0f;
-    for (int j = 0; j < g.ss_count; ++j) ss += __ldcg(p + j);
+#pragma unroll 4
+    for (int j = 0; j < n4; ++j) {
+        const float4 v = __ldcg(p + j);
+        const int k = 4 * j;
+        ss += v.x;
+        ss += k + 1 < n ? v.y : 0.0f;
+        ss += k + 2 < n ? v.z : 0.0f;
+        ss += k + 3 < n ? v.w : 0.0f;
+    }
     return 1.0f / sqrtf(ss / static_cast<float>(g.K) + g.eps);
 }
 
@@ -547,10 +557,11 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                 if (m0 + i < m_end) s_rows[i] = load_row_state(g, m0 + i);
         }
         if constexpr (EPI != GEPI_RESIDUAL && EPI != GEPI_STORE) {
-            if (warp == 3 && g.ss_in != nullptr) {  // ... and warp 3 the row scales
+            static_assert(gemm_threads(false) == 256, "warps 4-7 load the 128 row scales");
+            if (warp >= 4 && g.ss_in != nullptr) {  // ... and warps 4-7 the row scales
                 pdl_wait();
-                for (int i = lane; i < 128; i += 32)
-                    if (m0 + i < m_end) s_scale[i] = row_scale(g, m0 + i);
+                const int i = threadIdx.x - 128;
+                if (m0 + i < m_end) s_scale[i] = row_scale(g, m0 + i);
             }
         }
     } else {

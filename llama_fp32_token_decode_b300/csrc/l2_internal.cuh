@@ -141,7 +141,8 @@ struct GemmArgs {
     // weights carry the norm gain (W[n][k] * g[k]) and A holds the raw rows x
     // (tf32 pair), so the consumer scales row r of its result by
     // 1 / sqrt(ss_r / K + eps), ss_r = the sum of squares of x[r] as the sum of
-    // ss_count partials at ss_in[r * ss_stride] (fixed order). Null: no norm.
+    // ss_count partials at ss_in[r * ss_stride] (fixed order; ss_stride a
+    // multiple of 4). Null: no norm.
     const float* ss_in;
     int ss_count, ss_stride;
     float eps;
