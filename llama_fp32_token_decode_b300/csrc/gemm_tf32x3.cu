@@ -8,17 +8,21 @@
 //     C = Xhi*Whi + Xhi*Wlo + Xlo*Whi
 // drops only the Xlo*Wlo term (relative size 2^-22), with fp32 accumulation.
 //
-// Kernel (sm_103a, one 128 x BN output tile per CTA, 128 threads):
+// Kernel (sm_103a, one 128 x BN output tile per CTA, 256 threads; BN 64,
+// 128 or 256; details at the kernel):
 //   * warp 0 lane 0 streams K-blocks of 32 floats (128 bytes, one 128-byte
 //     swizzle row) of Xhi, Xlo, Whi, Wlo into a ring of shared-memory stages
 //     with 3-D TMA tile loads (completion on mbarriers); weight tiles of the
 //     first stages are requested before griddepcontrol.wait, since weights
 //     never depend on the previous kernel;
 //   * warp 1 lane 0 issues tcgen05.mma kind::tf32 (M 128, N BN, K 8) from the
-//     stages into one TMEM accumulator (128 lanes x BN fp32 columns) and frees
-//     each stage with tcgen05.commit;
-//   * all four warps then read the accumulator with tcgen05.ld (warp w owns
-//     TMEM lanes 32w..32w+31 = output rows) and apply the fused epilogue.
+//     stages into a TMEM accumulator (128 lanes x BN fp32 columns) and frees
+//     each stage with tcgen05.commit; idle warps meanwhile stage per-row data
+//     the epilogue needs (row positions, RMSNorm row scales);
+//   * every warp then reads the accumulator with tcgen05.ld (warp w: TMEM
+//     lanes 32 (w mod 4) .. + 31 = output rows) and applies the fused
+//     epilogue; a K split over a thread-block cluster first adds the CTAs'
+//     partial tiles through distributed shared memory.
 // Every wait is bounded; on a timeout the kernel records ERR_TIMEOUT_TMA,
 // drains its own copies, frees its TMEM and returns.
 #include <math.h>
