@@ -285,7 +285,7 @@ int ss_slots(const GemmPlan& p, int N) { return 2 * ((N + p.bn - 1) / p.bn); }
 cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mode, int steps,
                          bool want_logits, cudaStream_t s, bool prefill = false) {
     const l2_config& c = h->cfg;
-    const int d = c.dim, F = c.hidden_dim, L = c.n_layers, V = c.vocab_size;
+    const int d = c.dim, F = c.hidden_dim, V = c.vocab_size;
     GemmArgs g{};
     g.row0 = row0;
     g.M = M;
