@@ -56,6 +56,8 @@ struct l2_handle {
     float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
     float *cls_hi = nullptr, *cls_lo = nullptr;
     float* bact = nullptr;
+    // bx: residual rows; xn_hi / xn_lo: the same rows as a tf32 pair, the A
+    // operand of the norm-folded QKV, W1/W3 and classifier GEMMs
     float *bx = nullptr, *xn_hi = nullptr, *xn_lo = nullptr, *bq = nullptr;
     float *att_hi = nullptr, *att_lo = nullptr, *hb_hi = nullptr, *hb_lo = nullptr;
     float* blogits = nullptr;
