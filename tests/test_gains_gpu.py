@@ -1,0 +1,80 @@
+"""GPU parity with RMSNorm gains other than 1.
+
+Every workload blob has unit norm gains (the configs say so), which would let
+a gain that is dropped, misplaced or applied to the wrong layer go unseen.
+Here the gain segments of the blob hold seeded values in [0.5, 1.5], and the
+batch-1 forward, the batched forward (gains folded into the GEMM weights) and
+the prefill pass are each compared with the oracle on the same blob.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity_util import REL_L2_TOL, config, rel_l2
+
+
+@pytest.fixture(scope="module")
+def l2():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import llama_fp32_token_decode_b300 as m
+    return m
+
+
+def _blob_with_gains(cfg, seed):
+    blob = synth.make_blob(cfg, seed, std=0.05)
+    rng = np.random.default_rng(seed + 1000)
+    off = 0
+    n_gain = 0
+    for _, cnt, is_gain in synth.blob_segments(cfg):
+        if is_gain:
+            blob[off:off + cnt] = rng.uniform(0.5, 1.5, cnt).astype(np.float32)
+            n_gain += cnt
+        off += cnt
+    assert n_gain == cfg["n_layers"] * 2 * cfg["dim"] + cfg["dim"]
+    return blob
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_kv_heads", [8, 2])
+def test_nonunit_gains_all_paths(l2, n_kv_heads):
+    cfg = config(dim=128, hidden_dim=344, n_layers=3, n_heads=8, n_kv_heads=n_kv_heads,
+                 vocab_size=1000, seq_len=16, max_batch=3, max_prefill=4)
+    blob = _blob_with_gains(cfg, 31)
+    toks = np.array([[5, 17, 99], [7, 3, 11], [42, 8, 600], [1, 2, 3]], np.int32)  # [pos][seq]
+    refs = []
+    for b in range(3):
+        m = oracle.Model(cfg, blob)
+        refs.append([m.forward(int(toks[p][b]), p) for p in range(4)])
+        m.close()
+    with l2.Decoder(cfg, blob) as dec:
+        for p in range(4):  # batched forward: three sequences in lockstep
+            lg = dec.forward(toks[p], [p] * 3)
+            for b in range(3):
+                e = rel_l2(lg[b], refs[b][p])
+                assert e <= REL_L2_TOL, f"batched seq {b} pos {p}: rel-L2 {e:.3e}"
+        dec.reset()
+        for p in range(4):  # batch-1 forward of sequence 0
+            lg = dec.forward([int(toks[p][0])], [p])[0]
+            e = rel_l2(lg, refs[0][p])
+            assert e <= REL_L2_TOL, f"batch-1 pos {p}: rel-L2 {e:.3e}"
+        dec.reset()
+        pre = dec.prefill(toks[:, 0])  # prefill pass of sequence 0
+        for p in range(4):
+            e = rel_l2(pre[p], refs[0][p])
+            assert e <= REL_L2_TOL, f"prefill pos {p}: rel-L2 {e:.3e}"
+
+
+def test_gain_segments_reach_the_oracle():
+    # CPU: the modified gains change the oracle's logits (the test above would
+    # otherwise compare unit-gain models)
+    cfg = config(dim=64, hidden_dim=160, n_layers=2, n_heads=4, vocab_size=300, seq_len=8)
+    unit = synth.make_blob(cfg, 31, std=0.05)
+    gained = _blob_with_gains(cfg, 31)
+    ma, mb = oracle.Model(cfg, unit), oracle.Model(cfg, gained)
+    a, b = ma.forward(5, 0), mb.forward(5, 0)
+    ma.close()
+    mb.close()
+    assert rel_l2(b, a) > 1e-2
