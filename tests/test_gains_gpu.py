@@ -4,7 +4,8 @@ Every workload blob has unit norm gains (the configs say so), which would let
 a gain that is dropped, misplaced or applied to the wrong layer go unseen.
 Here the gain segments of the blob hold seeded values in [0.5, 1.5], and the
 batch-1 forward, the batched forward (gains folded into the GEMM weights) and
-the prefill pass are each compared with the oracle on the same blob.
+the prefill pass are each compared with the oracle on the same blob (one
+case with a RoPE theta and a norm epsilon other than the workloads').
 """
 import numpy as np
 import pytest
@@ -38,10 +39,13 @@ def _blob_with_gains(cfg, seed):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("n_kv_heads", [8, 2])
-def test_nonunit_gains_all_paths(l2, n_kv_heads):
+@pytest.mark.parametrize("n_kv_heads,theta,eps", [(8, 10000.0, 1e-5), (2, 500000.0, 1e-6)])
+def test_nonunit_gains_all_paths(l2, n_kv_heads, theta, eps):
+    # the second case also moves RoPE theta and the norm epsilon off the
+    # workloads' values, so neither can be a constant on any path
     cfg = config(dim=128, hidden_dim=344, n_layers=3, n_heads=8, n_kv_heads=n_kv_heads,
-                 vocab_size=1000, seq_len=16, max_batch=3, max_prefill=4)
+                 vocab_size=1000, seq_len=16, max_batch=3, max_prefill=4, rope_theta=theta,
+                 norm_eps=eps)
     blob = _blob_with_gains(cfg, 31)
     toks = np.array([[5, 17, 99], [7, 3, 11], [42, 8, 600], [1, 2, 3]], np.int32)  # [pos][seq]
     refs = []
