@@ -218,6 +218,28 @@ L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t
 L2_API int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
                                     int32_t B, int32_t steps, int32_t* d_out, void* stream);
 
+/* l2_generate_batch with temperature / top-p sampling of the generated tokens
+ * (the rule of l2_generate_sample, applied to each sequence's logits row).
+ * uniforms: host fp32 [B][steps], each in [0, 1): uniforms[b * steps + k]
+ * draws sequence b's k-th generated token; temperature <= 0 is the greedy
+ * choice. Needs a handle with max_batch > 1.
+ * Errors: as l2_generate_batch, plus L2_EINVAL for a NULL uniforms array,
+ * temperature < 0, topp outside (0, 1], a uniform outside [0, 1), or
+ * max_batch == 1. Synchronous. */
+L2_API int l2_generate_batch_sample(l2_handle* h, const int32_t* prompts, const int32_t* lens,
+                                    int32_t B, int32_t steps, float temperature, float topp,
+                                    const float* uniforms, int32_t* out_tokens);
+
+/* l2_generate_batch_sample with device buffers: d_prompts int32 [sum of
+ * lens], d_uniforms fp32 [B][steps], d_out int32 [B][steps]; lens a HOST
+ * array [B]. Queued on `stream`, returns without waiting; device values are
+ * not range-checked. */
+L2_API int l2_generate_batch_sample_device(l2_handle* h, const int32_t* d_prompts,
+                                           const int32_t* lens, int32_t B, int32_t steps,
+                                           float temperature, float topp,
+                                           const float* d_uniforms, int32_t* d_out,
+                                           void* stream);
+
 /* Clears KV cache `seq` (-1: all caches) to zero. Errors: L2_EINVAL. */
 L2_API int l2_reset(l2_handle* h, int32_t seq);
 

@@ -30,7 +30,8 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
                 "b_w2_gemm", "b_classifier_gemm", "b_rmsnorm", "b_advance")
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
-           "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device", "l2_prefill",
+           "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device",
+           "l2_generate_batch_sample", "l2_generate_batch_sample_device", "l2_prefill",
            "l2_generate_prefill", "l2_generate_prefill_device", "l2_generate_sample",
            "l2_generate_sample_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
@@ -73,6 +74,10 @@ _SIG = {
     "l2_generate_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_generate_batch": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
     "l2_generate_batch_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
+    "l2_generate_batch_sample": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float,
+                                                ctypes.c_float, _P, _P]),
+    "l2_generate_batch_sample_device": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float,
+                                                       ctypes.c_float, _P, _P, _P]),
     "l2_prefill": (ctypes.c_int, [_P, _P, _I, _I, _P]),
     "l2_generate_sample": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, ctypes.c_float, _P, _P]),
     "l2_generate_sample_device": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, ctypes.c_float,
@@ -235,6 +240,29 @@ def l2_generate_batch_device(h, d_prompts, lens, steps: int, d_out, stream=None)
                                          _ptr(d_out), _stream(stream)), h)
 
 
+def l2_generate_batch_sample(h, prompts, lens, steps: int, temperature: float, topp: float,
+                             uniforms) -> np.ndarray:
+    """uniforms: [B][steps] (sequence b's k-th draw at [b][k])."""
+    prompts, lens = _i32(prompts).ravel(), _i32(lens).ravel()
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).ravel()
+    if u.size < lens.size * steps:
+        raise ValueError("need one uniform number per sequence and generated token")
+    out = np.empty((lens.size, steps), np.int32)
+    _check(_lib.l2_generate_batch_sample(h, prompts.ctypes.data, lens.ctypes.data, lens.size,
+                                         steps, temperature, topp, u.ctypes.data,
+                                         out.ctypes.data), h)
+    return out
+
+
+def l2_generate_batch_sample_device(h, d_prompts, lens, steps: int, temperature: float,
+                                    topp: float, d_uniforms, d_out, stream=None) -> None:
+    """d_prompts, d_uniforms, d_out: device buffers; lens: host lengths."""
+    lens = _i32(lens).ravel()
+    _check(_lib.l2_generate_batch_sample_device(h, _ptr(d_prompts), lens.ctypes.data, lens.size,
+                                                steps, temperature, topp, _ptr(d_uniforms),
+                                                _ptr(d_out), _stream(stream)), h)
+
+
 def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:
     ms = ctypes.c_float()
     _check(_lib.l2_time_kernel(h, kind, pos, iters, _stream(stream), ctypes.byref(ms)), h)
@@ -315,6 +343,10 @@ class Decoder:
 
     def generate_batch(self, prompts, lens, steps: int) -> np.ndarray:
         return l2_generate_batch(self.h, prompts, lens, steps)
+
+    def generate_batch_sample(self, prompts, lens, steps: int, temperature: float, topp: float,
+                              uniforms) -> np.ndarray:
+        return l2_generate_batch_sample(self.h, prompts, lens, steps, temperature, topp, uniforms)
 
     def reset(self, seq: int = -1) -> None:
         l2_reset(self.h, seq)

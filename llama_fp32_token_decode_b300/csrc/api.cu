@@ -76,6 +76,10 @@ struct l2_handle {
     GemmOccupancy gocc{};
     cudaGraphExec_t bgraph = nullptr;  // one batched generation step
     int bgraph_M = 0, bgraph_steps = 0;
+    cudaGraphExec_t bgraph_s = nullptr;  // the same with sampling
+    int bgraph_s_M = 0, bgraph_s_steps = 0;
+    SampleParams* d_sparams = nullptr;   // batched sampling parameters
+    float* b_uniforms = nullptr;         // [max_batch][seq_len] host-path uniforms
 
     cudaStream_t stream = nullptr;
     cudaGraphExec_t fwd1 = nullptr;  // one forward
@@ -278,6 +282,7 @@ enum BKind : int {
     BK_QKV = 0, BK_ATTN = 1, BK_WO = 2, BK_W13 = 3, BK_W2 = 4, BK_CLS = 5,
     BK_EMB = 6,  // embedding gather: residual rows, their tf32 pair, sums of squares
     BK_ADVANCE = 7,
+    BK_SAMPLE_ADVANCE = 8,  // the advance of a generation with sampling
 };
 
 // Partial sums of squares a residual GEMM with this plan writes per row.
@@ -391,6 +396,24 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.ss_stride = h->ss_stride;
             g.eps = c.norm_eps;
             return launch_gemm(GEPI_ARGMAX, plan(h->gp_cls, g.N, g.K), h->m_cls, g, s, true);
+        case BK_SAMPLE_ADVANCE: {
+            BSampleArgs a{};
+            a.row0 = row0;
+            a.steps = steps;
+            a.vocab = V;
+            a.params = h->d_sparams;
+            a.logits = h->blogits;
+            a.keys = h->b_keys;
+            a.last = h->b_last;
+            a.pos = h->b_pos;
+            a.token = h->b_token;
+            a.active = h->b_active;
+            a.len = h->b_len;
+            a.poff = h->b_poff;
+            a.prompts = h->b_prompts;
+            a.out = h->b_out;
+            return launch_bsample(a, M, s, true);
+        }
         case BK_ADVANCE: {
             BAdvanceArgs a{};
             a.row0 = row0;
@@ -421,7 +444,8 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
 // `prefill`: every row is a position of sequence 0 (cache 0, row positions
 // in b_pos) instead of a sequence of its own.
 cudaError_t enqueue_rows(l2_handle* h, int row0, int M, int mode, int steps, bool want_logits,
-                         cudaStream_t s, bool prefill = false) {
+                         cudaStream_t s, bool prefill = false, bool sample = false) {
+    if (sample) want_logits = true;  // the sampler reads every row's logits
     cudaError_t e = launch_bkind(h, BK_EMB, 0, row0, M, mode, steps, want_logits, s, prefill);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
         const int seq[] = {BK_QKV, BK_ATTN, BK_WO, BK_W13, BK_W2};
@@ -430,7 +454,8 @@ cudaError_t enqueue_rows(l2_handle* h, int row0, int M, int mode, int steps, boo
     }
     if (e == cudaSuccess) e = launch_bkind(h, BK_CLS, 0, row0, M, mode, steps, want_logits, s, prefill);
     if (e == cudaSuccess)
-        e = launch_bkind(h, BK_ADVANCE, 0, row0, M, mode, steps, want_logits, s, prefill);
+        e = launch_bkind(h, sample ? BK_SAMPLE_ADVANCE : BK_ADVANCE, 0, row0, M, mode, steps,
+                         want_logits, s, prefill);
     return e;
 }
 
@@ -541,17 +566,20 @@ int setup_batched(l2_handle* h) {
     // two slots per N tile of >= 64 columns, rounded up to whole 16-byte groups
     h->ss_stride = static_cast<int>((2 * ((d + 63) / 64) + 3) / 4 * 4);
     const size_t o_ssa = take(Mc * h->ss_stride), o_ssf = take(Mc * h->ss_stride);
+    const size_t o_bu = take(B * S);
     L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
     L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));
     h->bx = h->bact + o_x; h->xn_hi = h->bact + o_nh; h->xn_lo = h->bact + o_nl;
     h->bq = h->bact + o_q; h->att_hi = h->bact + o_ah; h->att_lo = h->bact + o_al;
     h->hb_hi = h->bact + o_hh; h->hb_lo = h->bact + o_hl; h->blogits = h->bact + o_lg;
     h->ss_att = h->bact + o_ssa; h->ss_ffn = h->bact + o_ssf;
+    h->b_uniforms = h->bact + o_bu;
 
     off = 0;
     const size_t o_pos = take(Mc), o_tok = take(Mc), o_act = take(Mc), o_len = take(Mc);
     const size_t o_poff = take(Mc), o_last = take(Mc), o_pr = take(B * S), o_out = take(B * S);
     const size_t o_seq = take(Mc), o_keys = take(2 * Mc);
+    const size_t o_sp = take((sizeof(SampleParams) + 3) / 4);
     L2_CUDA(h, cudaMalloc(&h->bst, off * sizeof(int)));
     L2_CUDA(h, cudaMemsetAsync(h->bst, 0, off * sizeof(int), s));
     h->b_pos = h->bst + o_pos; h->b_token = h->bst + o_tok; h->b_active = h->bst + o_act;
@@ -559,6 +587,7 @@ int setup_batched(l2_handle* h) {
     h->b_prompts = h->bst + o_pr; h->b_out = h->bst + o_out;
     h->b_seq = h->bst + o_seq;
     h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
+    h->d_sparams = reinterpret_cast<SampleParams*>(h->bst + o_sp);
 
     const int Mb = static_cast<int>(RW);
     h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
@@ -643,6 +672,8 @@ void free_all(l2_handle* h) {
     if (h->fwdNs) cudaGraphExecDestroy(h->fwdNs);
     h->fwd1s = h->fwdNs = nullptr;
     if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+    if (h->bgraph_s) cudaGraphExecDestroy(h->bgraph_s);
+    h->bgraph_s = nullptr;
     cudaFree(h->bw);
     cudaFree(h->bact);
     cudaFree(h->bst);
@@ -672,24 +703,27 @@ int bforward(l2_handle* h, int M, bool want_logits, cudaStream_t s) {
     return L2_OK;
 }
 
-int capture_bstep(l2_handle* h, int M, int steps) {
-    if (h->bgraph && h->bgraph_M == M && h->bgraph_steps == steps) return L2_OK;
-    if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
-    h->bgraph = nullptr;
+int capture_bstep(l2_handle* h, int M, int steps, bool sample = false) {
+    cudaGraphExec_t& gx = sample ? h->bgraph_s : h->bgraph;
+    int& gM = sample ? h->bgraph_s_M : h->bgraph_M;
+    int& gS = sample ? h->bgraph_s_steps : h->bgraph_steps;
+    if (gx && gM == M && gS == steps) return L2_OK;
+    if (gx) cudaGraphExecDestroy(gx);
+    gx = nullptr;
     cudaGraph_t g = nullptr;
     L2_CUDA(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = enqueue_bstep(h, M, 1, steps, false, h->stream);
+    cudaError_t e = enqueue_rows(h, 0, M, 1, steps, false, h->stream, false, sample);
     cudaError_t e2 = cudaStreamEndCapture(h->stream, &g);
     if (e != cudaSuccess) {
         if (g) cudaGraphDestroy(g);
         return cuda_fail(h, e, "batched step launch during capture");
     }
     if (e2 != cudaSuccess) return cuda_fail(h, e2, "cudaStreamEndCapture");
-    e = cudaGraphInstantiate(&h->bgraph, g, 0);
+    e = cudaGraphInstantiate(&gx, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphInstantiate");
-    h->bgraph_M = M;
-    h->bgraph_steps = steps;
+    gM = M;
+    gS = steps;
     return L2_OK;
 }
 
@@ -1090,9 +1124,20 @@ int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t s
     return check_device_error(h);
 }
 
+__global__ void bparams_kernel(SampleParams* p, float temperature, float topp,
+                               const float* uniforms) {
+    p->temperature = temperature;
+    p->topp = topp;
+    p->uniforms = uniforms;
+}
+
+// sample: draw generated tokens (temperature, topp, uniforms [B][steps]) instead
+// of the greedy choice.
 static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32_t* lens,
                                int32_t B, int32_t steps, int32_t* out_tokens, bool on_device,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool sample = false,
+                               float temperature = 0.0f, float topp = 1.0f,
+                               const float* uniforms = nullptr) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (!prompts || !lens || !out_tokens) return fail(h, L2_EINVAL, "NULL prompts, lens or output");
     if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
@@ -1111,10 +1156,33 @@ static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32
     if (!on_device)
         for (long long i = 0; i < total; ++i)
             if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    if (sample) {
+        if (!uniforms) return fail(h, L2_EINVAL, "NULL uniforms");
+        if (!(temperature >= 0.0f) || !(topp > 0.0f && topp <= 1.0f))
+            return fail(h, L2_EINVAL, "need temperature >= 0 and 0 < topp <= 1");
+        if (!on_device)
+            for (long long i = 0; i < static_cast<long long>(B) * steps; ++i)
+                if (!(uniforms[i] >= 0.0f && uniforms[i] < 1.0f))
+                    return fail(h, L2_EINVAL, "uniform numbers must lie in [0, 1)");
+        if (h->cfg.max_batch == 1)
+            return fail(h, L2_EINVAL,
+                        "batched sampling needs max_batch > 1 (batch 1: l2_generate_sample)");
+    }
     if (h->cfg.max_batch == 1)
         return on_device ? l2_generate_device(h, prompts, lens[0], steps, out_tokens, stream)
                          : l2_generate(h, prompts, lens[0], steps, out_tokens);
     cudaStream_t s = on_device ? stream : h->stream;
+    if (sample) {
+        const float* d_u = uniforms;
+        if (!on_device) {
+            L2_CUDA(h, cudaMemcpyAsync(h->b_uniforms, uniforms,
+                                       sizeof(float) * static_cast<size_t>(B) * steps,
+                                       cudaMemcpyHostToDevice, s));
+            d_u = h->b_uniforms;
+        }
+        bparams_kernel<<<1, 1, 0, s>>>(h->d_sparams, temperature, topp, d_u);
+        L2_CUDA(h, cudaGetLastError());
+    }
     L2_CUDA(h, cudaMemcpyAsync(h->b_prompts, prompts, sizeof(int32_t) * total,
                                on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
     L2_CUDA(h, cudaMemcpyAsync(h->b_len, lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
@@ -1124,10 +1192,11 @@ static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32
                                                  h->b_len, h->b_poff, h->b_prompts, h->b_keys,
                                                  h->st);
     L2_CUDA(h, cudaGetLastError());
-    int rc = capture_bstep(h, B, steps);
+    int rc = capture_bstep(h, B, steps, sample);
     if (rc != L2_OK) return rc;
     const int n = max_len + steps - 1;
-    for (int i = 0; i < n; ++i) L2_CUDA(h, cudaGraphLaunch(h->bgraph, s));
+    cudaGraphExec_t gx = sample ? h->bgraph_s : h->bgraph;
+    for (int i = 0; i < n; ++i) L2_CUDA(h, cudaGraphLaunch(gx, s));
     L2_CUDA(h, cudaMemcpyAsync(out_tokens, h->b_out, sizeof(int32_t) * B * static_cast<size_t>(steps),
                                on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
     if (on_device) return L2_OK;
@@ -1223,6 +1292,21 @@ int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32
                              int32_t B, int32_t steps, int32_t* d_out, void* stream) {
     return generate_batch_impl(h, d_prompts, lens, B, steps, d_out, true,
                                static_cast<cudaStream_t>(stream));
+}
+
+int l2_generate_batch_sample(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
+                             int32_t steps, float temperature, float topp, const float* uniforms,
+                             int32_t* out_tokens) {
+    return generate_batch_impl(h, prompts, lens, B, steps, out_tokens, false, nullptr, true,
+                               temperature, topp, uniforms);
+}
+
+int l2_generate_batch_sample_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
+                                    int32_t B, int32_t steps, float temperature, float topp,
+                                    const float* d_uniforms, int32_t* d_out, void* stream) {
+    return generate_batch_impl(h, d_prompts, lens, B, steps, d_out, true,
+                               static_cast<cudaStream_t>(stream), true, temperature, topp,
+                               d_uniforms);
 }
 
 int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,

@@ -185,6 +185,30 @@ struct BAttnArgs {
     size_t cache_seq;
 };
 
+// Sampling parameters of a batched generation, device-resident (written
+// before the step graph replays, so the graph does not depend on them).
+struct SampleParams {
+    float temperature, topp;
+    const float* uniforms;  // [B][steps]: sequence b's uniform for its k-th token
+};
+
+// The per-sequence advance of a batched generation with sampling (sample.cu).
+struct BSampleArgs {
+    int row0;
+    int steps, vocab;
+    const SampleParams* params;
+    const float* logits;         // [M][V] of this step
+    unsigned long long* keys;    // [M] packed argmax keys (reset to 0 here)
+    int* last;
+    int* pos;
+    int* token;
+    int* active;
+    const int* len;
+    const int* poff;
+    const int* prompts;
+    int* out;                    // [M][steps]
+};
+
 struct BAdvanceArgs {
     int row0;                    // rows row0 .. row0 + M - 1
     int M;
@@ -377,6 +401,7 @@ cudaError_t launch_badvance(const BAdvanceArgs& a, cudaStream_t s, bool pdl);
 
 // sample.cu
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_bsample(const BSampleArgs& a, int M, cudaStream_t s, bool pdl);
 
 // layout.cu
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
