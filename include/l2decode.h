@@ -64,11 +64,12 @@ extern "C" {
  * decode, prefill) is set up when max_batch > 1 or max_prefill > 1, with
  * row buffers for max(max_batch, max_prefill) rows.
  * rolling_positions: 0 (or <= seq_len) keeps every position below seq_len.
- * N > seq_len lets a batch-1 sequence decode positions 0 .. N-1: position p
- * writes cache slot p % seq_len and attends over the last seq_len positions
- * (a rolling cache; the openai.wiki page lists decoding beyond max_seq_len as
- * a to-do that has to handle the KV cache, "未排序的待办事项"); RoPE keeps
- * the absolute position. Batched decode and prefill stay below seq_len. */
+ * N > seq_len lets a sequence decode positions 0 .. N-1 (batch 1 and
+ * batched decode): position p writes cache slot p % seq_len and attends over
+ * the last seq_len positions (a rolling cache; the openai.wiki page lists
+ * decoding beyond max_seq_len as a to-do that has to handle the KV cache,
+ * "未排序的待办事项"); RoPE keeps the absolute position. Prompts (and the
+ * prefill pass) stay below seq_len. */
 typedef struct {
     int32_t dim;               /* d, width of the residual stream            */
     int32_t hidden_dim;        /* F, SwiGLU hidden width                     */
@@ -117,8 +118,11 @@ L2_API int l2_create_from_device(const l2_config* cfg, const float* d_blob, size
  * 0..pos[b] (slots below pos[b] must hold that sequence's earlier steps;
  * re-running a lower pos overwrites its slot). Sequence b uses cache b.
  * tokens, pos: host arrays [B]. logits_out: host [B][V] floats or NULL.
+ * With a rolling cache (rolling_positions > S) positions run up to
+ * rolling_positions - 1, position p using slot p % S and the last min(p+1, S)
+ * positions being attended.
  * Errors: L2_EINVAL for B < 1, B > max_batch, a token outside [0, V) or a
- * position outside [0, S). Synchronous. */
+ * position outside [0, S) (rolling: [0, rolling_positions)). Synchronous. */
 L2_API int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t B,
                float* logits_out);
 
@@ -205,8 +209,11 @@ L2_API int l2_generate_sample_device(l2_handle* h, const int32_t* d_prompt, int3
  * >= 1; out_tokens: host [B][steps]. Sequence b runs forwards at positions
  * 0 .. lens[b]+steps-2 of its own cache; a sequence that has produced its
  * `steps` tokens idles while the others finish.
- * Errors: L2_EINVAL for B < 1 or > max_batch, a length < 1,
- * lens[b]+steps-1 > S, or an id outside [0, V). Synchronous. */
+ * With a rolling cache (rolling_positions > S) a sequence runs up to
+ * rolling_positions positions.
+ * Errors: L2_EINVAL for B < 1 or > max_batch, a length < 1 or > S,
+ * lens[b]+steps-1 > S (rolling: > rolling_positions), or an id outside
+ * [0, V). Synchronous. */
 L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
                       int32_t steps, int32_t* out_tokens);
 

@@ -329,6 +329,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.kvd = h->kvd;
             g.head_dim = h->hd;
             g.seq_len = c.seq_len;
+            g.rope_positions = h->pmax;
             g.cache_seq = h->cache_seq;
             g.ss_in = h->ss_att;  // attention RMSNorm (gain in the weights)
             g.ss_count = l == 0 ? 1 : ss_slots(h->gp_w2, d);
@@ -566,7 +567,7 @@ int setup_batched(l2_handle* h) {
     // two slots per N tile of >= 64 columns, rounded up to whole 16-byte groups
     h->ss_stride = static_cast<int>((2 * ((d + 63) / 64) + 3) / 4 * 4);
     const size_t o_ssa = take(Mc * h->ss_stride), o_ssf = take(Mc * h->ss_stride);
-    const size_t o_bu = take(B * S);
+    const size_t o_bu = take(B * static_cast<size_t>(h->pmax));
     L2_CUDA(h, cudaMalloc(&h->bact, off * sizeof(float)));
     L2_CUDA(h, cudaMemsetAsync(h->bact, 0, off * sizeof(float), s));
     h->bx = h->bact + o_x; h->xn_hi = h->bact + o_nh; h->xn_lo = h->bact + o_nl;
@@ -577,7 +578,8 @@ int setup_batched(l2_handle* h) {
 
     off = 0;
     const size_t o_pos = take(Mc), o_tok = take(Mc), o_act = take(Mc), o_len = take(Mc);
-    const size_t o_poff = take(Mc), o_last = take(Mc), o_pr = take(B * S), o_out = take(B * S);
+    const size_t o_poff = take(Mc), o_last = take(Mc), o_pr = take(B * S);
+    const size_t o_out = take(B * static_cast<size_t>(h->pmax));
     const size_t o_seq = take(Mc), o_keys = take(2 * Mc);
     const size_t o_sp = take((sizeof(SampleParams) + 3) / 4);
     L2_CUDA(h, cudaMalloc(&h->bst, off * sizeof(int)));
@@ -1056,7 +1058,7 @@ int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t 
     if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
     for (int b = 0; b < B; ++b) {
         if (tokens[b] < 0 || tokens[b] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
-        if (pos[b] < 0 || pos[b] >= (B == 1 ? h->pmax : h->cfg.seq_len))
+        if (pos[b] < 0 || pos[b] >= h->pmax)
             return fail(h, L2_EINVAL, "position out of range");
     }
     if (B > 1) {
@@ -1147,8 +1149,10 @@ static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32
     long long total = 0;
     int max_len = 0;
     for (int b = 0; b < B; ++b) {
-        if (lens[b] < 1 || static_cast<long long>(lens[b]) + steps - 1 > S)
-            return fail(h, L2_EINVAL, "need lens[b] >= 1 and lens[b] + steps - 1 <= seq_len");
+        if (lens[b] < 1 || lens[b] > S || static_cast<long long>(lens[b]) + steps - 1 > h->pmax)
+            return fail(h, L2_EINVAL,
+                        "need 1 <= lens[b] <= seq_len and lens[b] + steps - 1 <= seq_len "
+                        "(rolling: rolling_positions)");
         poff[b] = static_cast<int32_t>(total);
         total += lens[b];
         max_len = lens[b] > max_len ? lens[b] : max_len;

@@ -319,13 +319,13 @@ __device__ __forceinline__ float epi4(const GemmArgs& g, int r, int gc, const fl
             } else if (c < g.d + g.kvd) {
                 const int jj = c - g.d, kvh = jj / hd, e = jj % hd;
                 float* dst = g.k_cache + static_cast<size_t>(rs.cache) * g.cache_seq +
-                             (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                             (static_cast<size_t>(kvh) * g.seq_len + pos % g.seq_len) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
                 dst[1] = x0 * cs.y + x1 * cs.x;
             } else {
                 const int jj = c - g.d - g.kvd, kvh = jj / hd, e = jj % hd;
                 float* dst = g.v_cache + static_cast<size_t>(rs.cache) * g.cache_seq +
-                             (static_cast<size_t>(kvh) * g.seq_len + pos) * hd + e;
+                             (static_cast<size_t>(kvh) * g.seq_len + pos % g.seq_len) * hd + e;
                 dst[0] = x0;
                 dst[1] = x1;
             }
@@ -366,7 +366,10 @@ __device__ __forceinline__ float row_scale(const GemmArgs& g, int r) {
 // Row r's state, read from the arrays the previous kernels wrote.
 __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
     RowState rs;
-    rs.pos = min(max(__ldcg(g.pos + r), 0), g.seq_len - 1);
+    // positions run past seq_len when the cache rolls: RoPE at the absolute
+    // position (the table covers rope_positions), the KV slot pos % seq_len
+    rs.pos = min(max(__ldcg(g.pos + r), 0),
+                 (g.rope_positions > g.seq_len ? g.rope_positions : g.seq_len) - 1);
     rs.active = g.active ? __ldcg(g.active + r) : 1;
     rs.cache = g.seq ? __ldcg(g.seq + r) : r;
     return rs;

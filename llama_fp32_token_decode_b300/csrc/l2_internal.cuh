@@ -133,6 +133,7 @@ struct GemmArgs {
     const int* active;    // [M] 0 = finished sequence (no KV write) or null
     const int* seq;       // [M] KV cache of each row, or null (row r uses cache r)
     int d, kvd, head_dim, seq_len;
+    int rope_positions;   // positions of the RoPE table (> seq_len: the cache rolls)
     size_t cache_seq;     // floats of one sequence's cache (all layers)
     unsigned long long* argmax_keys;  // ARGMAX: [M]
     int* err;             // ERR_* bits

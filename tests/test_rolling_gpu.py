@@ -82,3 +82,31 @@ def test_rolling_cache_limits_and_sampling(l2):
     with l2.Decoder(plain, blob) as dec:
         with pytest.raises(l2.L2Error):
             dec.forward([1], [cfg["seq_len"]])             # no rolling: S is the limit
+
+
+def test_rolling_cache_batched(l2):
+    # three sequences in lockstep on the tensor-core path, each running past
+    # the window (3 S positions): teacher-forced logits at every position, then
+    # free-running generation compared per sequence up to its first near-tie
+    cfg = dict(SHAPES["s16_gqa"], max_batch=3, rolling_positions=48)
+    blob = synth.make_blob(cfg, 19, std=0.05)
+    S, N = cfg["seq_len"], cfg["rolling_positions"]
+    lens = np.array([1, 4, 6], np.int32)
+    prompts = [synth.prompt_ids(30 + b, int(lens[b]), cfg["vocab_size"]) for b in range(3)]
+    steps = N - int(lens.max()) + 1
+    runs = [oracle_run(cfg, blob, prompts[b], steps) for b in range(3)]
+    with l2.Decoder(cfg, blob) as dec:
+        n_common = int(lens.min()) + steps - 1  # positions every sequence runs
+        assert n_common > 2 * S
+        for p in range(n_common):  # every sequence at position p (consumed tokens of its run)
+            toks = [int(runs[b][1][p]) for b in range(3)]
+            lg = dec.forward(toks, [p] * 3)
+            for b in range(3):
+                e = rel_l2(lg[b], runs[b][2][p])
+                assert e <= REL_L2_TOL, f"seq {b} pos {p} (slot {p % S}): rel-L2 {e:.3e}"
+        gen = dec.generate_batch(np.concatenate(prompts), lens, steps)
+    for b in range(3):
+        toks, _, trace = runs[b]
+        k = first_near_tie(trace, int(lens[b]))
+        n = min(k + 1, steps)
+        np.testing.assert_array_equal(gen[b][:n], toks[:n])
