@@ -225,6 +225,23 @@ L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t
 L2_API int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
                                     int32_t B, int32_t steps, int32_t* d_out, void* stream);
 
+/* l2_generate_batch with every prompt taken by prefill passes: the prompt
+ * positions of all B sequences become rows of the tensor-core path (passes of
+ * up to max(max_batch, max_prefill) rows, in order), each row writing its own
+ * sequence's cache; the argmax of a sequence's last prompt position is its
+ * first token, and the sequences then advance in lockstep for the remaining
+ * steps - 1 tokens. Same arguments, output and errors as l2_generate_batch
+ * (plus L2_EINVAL when max_batch == 1). Synchronous. */
+L2_API int l2_generate_batch_prefill(l2_handle* h, const int32_t* prompts, const int32_t* lens,
+                                     int32_t B, int32_t steps, int32_t* out_tokens);
+
+/* l2_generate_batch_prefill with device prompts and output (as
+ * l2_generate_batch_device; lens a HOST array [B]). Queued on `stream`,
+ * returns without waiting. */
+L2_API int l2_generate_batch_prefill_device(l2_handle* h, const int32_t* d_prompts,
+                                            const int32_t* lens, int32_t B, int32_t steps,
+                                            int32_t* d_out, void* stream);
+
 /* l2_generate_batch with temperature / top-p sampling of the generated tokens
  * (the rule of l2_generate_sample, applied to each sequence's logits row).
  * uniforms: host fp32 [B][steps], each in [0, 1): uniforms[b * steps + k]

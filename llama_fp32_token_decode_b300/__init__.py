@@ -31,7 +31,8 @@ KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residu
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device",
-           "l2_generate_batch_sample", "l2_generate_batch_sample_device", "l2_prefill",
+           "l2_generate_batch_sample", "l2_generate_batch_sample_device",
+           "l2_generate_batch_prefill", "l2_generate_batch_prefill_device", "l2_prefill",
            "l2_generate_prefill", "l2_generate_prefill_device", "l2_generate_sample",
            "l2_generate_sample_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
@@ -74,6 +75,8 @@ _SIG = {
     "l2_generate_device": (ctypes.c_int, [_P, _P, _I, _I, _P, _P]),
     "l2_generate_batch": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
     "l2_generate_batch_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
+    "l2_generate_batch_prefill": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
+    "l2_generate_batch_prefill_device": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _P]),
     "l2_generate_batch_sample": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float,
                                                 ctypes.c_float, _P, _P]),
     "l2_generate_batch_sample_device": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float,
@@ -240,6 +243,22 @@ def l2_generate_batch_device(h, d_prompts, lens, steps: int, d_out, stream=None)
                                          _ptr(d_out), _stream(stream)), h)
 
 
+def l2_generate_batch_prefill(h, prompts, lens, steps: int) -> np.ndarray:
+    prompts, lens = _i32(prompts).ravel(), _i32(lens).ravel()
+    out = np.empty((lens.size, steps), np.int32)
+    _check(_lib.l2_generate_batch_prefill(h, prompts.ctypes.data, lens.ctypes.data, lens.size,
+                                          steps, out.ctypes.data), h)
+    return out
+
+
+def l2_generate_batch_prefill_device(h, d_prompts, lens, steps: int, d_out, stream=None) -> None:
+    """d_prompts, d_out: device buffers; lens: host lengths."""
+    lens = _i32(lens).ravel()
+    _check(_lib.l2_generate_batch_prefill_device(h, _ptr(d_prompts), lens.ctypes.data,
+                                                 lens.size, steps, _ptr(d_out),
+                                                 _stream(stream)), h)
+
+
 def l2_generate_batch_sample(h, prompts, lens, steps: int, temperature: float, topp: float,
                              uniforms) -> np.ndarray:
     """uniforms: [B][steps] (sequence b's k-th draw at [b][k])."""
@@ -343,6 +362,9 @@ class Decoder:
 
     def generate_batch(self, prompts, lens, steps: int) -> np.ndarray:
         return l2_generate_batch(self.h, prompts, lens, steps)
+
+    def generate_batch_prefill(self, prompts, lens, steps: int) -> np.ndarray:
+        return l2_generate_batch_prefill(self.h, prompts, lens, steps)
 
     def generate_batch_sample(self, prompts, lens, steps: int, temperature: float, topp: float,
                               uniforms) -> np.ndarray:

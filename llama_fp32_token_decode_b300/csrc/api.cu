@@ -65,6 +65,7 @@ struct l2_handle {
     int *b_pos = nullptr, *b_token = nullptr, *b_active = nullptr, *b_len = nullptr;
     int *b_poff = nullptr, *b_last = nullptr, *b_prompts = nullptr, *b_out = nullptr;
     int* b_seq = nullptr;              // KV cache of each row (prefill: all 0)
+    int* b_rmap = nullptr;             // batched prefill: (sequence, position) of each prompt row
     unsigned long long* b_keys = nullptr;
     // sums of squares of the rows entering a folded RMSNorm, [Mcap][ss_stride]:
     // ss_att (from the embedding gather or W2, read by QKV and the classifier)
@@ -582,6 +583,7 @@ int setup_batched(l2_handle* h) {
     const size_t o_out = take(B * static_cast<size_t>(h->pmax));
     const size_t o_seq = take(Mc), o_keys = take(2 * Mc);
     const size_t o_sp = take((sizeof(SampleParams) + 3) / 4);
+    const size_t o_rmap = take(2 * B * S);
     L2_CUDA(h, cudaMalloc(&h->bst, off * sizeof(int)));
     L2_CUDA(h, cudaMemsetAsync(h->bst, 0, off * sizeof(int), s));
     h->b_pos = h->bst + o_pos; h->b_token = h->bst + o_tok; h->b_active = h->bst + o_act;
@@ -590,6 +592,7 @@ int setup_batched(l2_handle* h) {
     h->b_seq = h->bst + o_seq;
     h->b_keys = reinterpret_cast<unsigned long long*>(h->bst + o_keys);
     h->d_sparams = reinterpret_cast<SampleParams*>(h->bst + o_sp);
+    h->b_rmap = h->bst + o_rmap;
 
     const int Mb = static_cast<int>(RW);
     h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
@@ -1274,6 +1277,124 @@ static int generate_prefill_impl(l2_handle* h, const int32_t* prompt, int32_t n_
     L2_CUDA(h, cudaMemcpyAsync(out, h->d_out, sizeof(int32_t) * steps, cudaMemcpyDeviceToHost, s));
     L2_CUDA(h, cudaStreamSynchronize(s));
     return check_device_error(h);
+}
+
+// Batched prefill: rows [0, n) of a pass are prompt rows start .. start+n-1
+// of the concatenated prompts; row r is sequence rmap[2 i] at position
+// rmap[2 i + 1] (i = start + r) and writes that sequence's cache.
+__global__ void bprefill_setup_kernel(int n, int start, const int* rmap, const int* prompts,
+                                      const int* poff, int vocab, int* b_token, int* b_pos,
+                                      int* b_seq, int* b_active, unsigned long long* keys,
+                                      L2State* st) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r == 0 && start == 0) st->err = 0;
+    if (r >= n) return;
+    const int b = rmap[2 * (start + r)], p = rmap[2 * (start + r) + 1];
+    b_token[r] = min(max(prompts[poff[b] + p], 0), vocab - 1);
+    b_pos[r] = p;
+    b_seq[r] = b;
+    b_active[r] = 1;
+    keys[r] = 0ull;
+}
+
+// After a pass: the argmax of a sequence's last prompt position is its first
+// generated token.
+__global__ void bprefill_handoff_kernel(int n, int start, const int* rmap, const int* lens,
+                                        const int* last, int steps, int* out) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= n) return;
+    const int b = rmap[2 * (start + r)], p = rmap[2 * (start + r) + 1];
+    if (p == lens[b] - 1) out[static_cast<size_t>(b) * steps] = last[r];
+}
+
+// Sequences continue in lockstep from their first generated token.
+__global__ void bprefill_continue_kernel(int B, int steps, const int* lens, const int* out,
+                                         int* pos, int* token, int* active,
+                                         unsigned long long* keys) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    pos[b] = lens[b];
+    token[b] = out[static_cast<size_t>(b) * steps];
+    active[b] = steps > 1 ? 1 : 0;
+    keys[b] = 0ull;
+}
+
+static int generate_batch_prefill_impl(l2_handle* h, const int32_t* prompts, const int32_t* lens,
+                                       int32_t B, int32_t steps, int32_t* out_tokens,
+                                       bool on_device, cudaStream_t stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (!prompts || !lens || !out_tokens) return fail(h, L2_EINVAL, "NULL prompts, lens or output");
+    if (h->cfg.max_batch < 2) return fail(h, L2_EINVAL, "batched prefill needs max_batch > 1");
+    if (B < 1 || B > h->cfg.max_batch) return fail(h, L2_EINVAL, "B out of range");
+    if (steps < 1) return fail(h, L2_EINVAL, "steps must be >= 1");
+    const int S = h->cfg.seq_len, V = h->cfg.vocab_size;
+    std::vector<int32_t> poff(B), rmap;
+    long long total = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 1 || lens[b] > S || static_cast<long long>(lens[b]) + steps - 1 > h->pmax)
+            return fail(h, L2_EINVAL,
+                        "need 1 <= lens[b] <= seq_len and lens[b] + steps - 1 <= seq_len "
+                        "(rolling: rolling_positions)");
+        poff[b] = static_cast<int32_t>(total);
+        total += lens[b];
+    }
+    if (!on_device)
+        for (long long i = 0; i < total; ++i)
+            if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    rmap.reserve(2 * total);
+    for (int b = 0; b < B; ++b)
+        for (int p = 0; p < lens[b]; ++p) {
+            rmap.push_back(b);
+            rmap.push_back(p);
+        }
+    cudaStream_t s = on_device ? stream : h->stream;
+    L2_CUDA(h, cudaMemcpyAsync(h->b_prompts, prompts, sizeof(int32_t) * total,
+                               on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
+    L2_CUDA(h, cudaMemcpyAsync(h->b_len, lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
+    L2_CUDA(h, cudaMemcpyAsync(h->b_poff, poff.data(), sizeof(int32_t) * B, cudaMemcpyHostToDevice,
+                               s));
+    L2_CUDA(h, cudaMemcpyAsync(h->b_rmap, rmap.data(), sizeof(int32_t) * rmap.size(),
+                               cudaMemcpyHostToDevice, s));
+    // passes of up to `rows` prompt rows, in order: a sequence's earlier
+    // positions are in its cache before its later ones attend to them
+    for (long long start = 0; start < total; start += h->rows) {
+        const int n = static_cast<int>(total - start < h->rows ? total - start : h->rows);
+        const int st0 = static_cast<int>(start);
+        bprefill_setup_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, st0, h->b_rmap, h->b_prompts,
+                                                              h->b_poff, V, h->b_token, h->b_pos,
+                                                              h->b_seq, h->b_active, h->b_keys,
+                                                              h->st);
+        L2_CUDA(h, cudaGetLastError());
+        L2_CUDA(h, enqueue_rows(h, 0, n, 0, 0, false, s, true));
+        bprefill_handoff_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, st0, h->b_rmap, h->b_len,
+                                                                h->b_last, steps, h->b_out);
+        L2_CUDA(h, cudaGetLastError());
+    }
+    bprefill_continue_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, steps, h->b_len, h->b_out,
+                                                             h->b_pos, h->b_token, h->b_active,
+                                                             h->b_keys);
+    L2_CUDA(h, cudaGetLastError());
+    if (steps > 1) {
+        int rc = capture_bstep(h, B, steps);
+        if (rc != L2_OK) return rc;
+        for (int i = 0; i < steps - 1; ++i) L2_CUDA(h, cudaGraphLaunch(h->bgraph, s));
+    }
+    L2_CUDA(h, cudaMemcpyAsync(out_tokens, h->b_out, sizeof(int32_t) * B * static_cast<size_t>(steps),
+                               on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
+    if (on_device) return L2_OK;
+    L2_CUDA(h, cudaStreamSynchronize(s));
+    return check_device_error(h);
+}
+
+int l2_generate_batch_prefill(l2_handle* h, const int32_t* prompts, const int32_t* lens, int32_t B,
+                              int32_t steps, int32_t* out_tokens) {
+    return generate_batch_prefill_impl(h, prompts, lens, B, steps, out_tokens, false, nullptr);
+}
+
+int l2_generate_batch_prefill_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
+                                     int32_t B, int32_t steps, int32_t* d_out, void* stream) {
+    return generate_batch_prefill_impl(h, d_prompts, lens, B, steps, d_out, true,
+                                       static_cast<cudaStream_t>(stream));
 }
 
 int l2_generate_prefill(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,

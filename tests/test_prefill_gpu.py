@@ -117,3 +117,38 @@ def test_prefill_errors(l2):
     with l2.Decoder(plain, blob) as dec:
         with pytest.raises(l2.L2Error):
             dec.prefill([1, 2])                                            # no prefill path
+
+
+@pytest.mark.parametrize("max_prefill", [0, 7])
+def test_batched_generation_with_prefill(l2, max_prefill):
+    # five ragged prompts taken by prefill passes (max_prefill 7 with
+    # max_batch 5: passes of 7 rows, so sequences straddle passes), then
+    # lockstep generation; each sequence against the oracle up to its first
+    # near-tie, and against the lockstep generation without prefill
+    import torch
+    cfg = config(dim=128, hidden_dim=344, n_layers=2, n_heads=8, n_kv_heads=2, vocab_size=3001,
+                 seq_len=40, max_batch=5, max_prefill=max_prefill)
+    blob = synth.make_blob(cfg, 21, std=0.05)
+    lens = np.array([3, 1, 9, 5, 6], np.int32)
+    prompts = [synth.prompt_ids(60 + b, int(lens[b]), cfg["vocab_size"]) for b in range(5)]
+    flat = np.concatenate(prompts).astype(np.int32)
+    steps = 20
+    with l2.Decoder(cfg, blob) as dec:
+        gen = dec.generate_batch_prefill(flat, lens, steps)
+        lock = dec.generate_batch(flat, lens, steps)
+        one = dec.generate_batch_prefill(flat, lens, 1)
+        s = torch.cuda.Stream()
+        d_p = torch.tensor(flat, device="cuda")
+        d_o = torch.zeros((5, steps), dtype=torch.int32, device="cuda")
+        l2.l2_generate_batch_prefill_device(dec.h, d_p, lens, steps, d_o, s)
+        s.synchronize()
+        np.testing.assert_array_equal(d_o.cpu().numpy(), gen)
+        with pytest.raises(l2.L2Error):
+            dec.generate_batch_prefill(flat, np.array([3, 1, 41, 5, 6], np.int32), steps)
+    for b in range(5):
+        toks, _, trace = oracle_run(cfg, blob, prompts[b], steps)
+        k = first_near_tie(trace, int(lens[b]))
+        n = min(k + 1, steps)
+        np.testing.assert_array_equal(gen[b][:n], toks[:n])
+        np.testing.assert_array_equal(lock[b][:n], toks[:n])
+        assert one[b][0] == gen[b][0]
