@@ -42,6 +42,9 @@ METRIC_BATCHED = "decode tok/s (fp32, batch 256)"
 DOMINANT_KIND = 3  # W1/W3 + SwiGLU: 44% of the streamed bytes of a 7B-shape step
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "w13_swiglu_7b_shape.md")
 KERNEL_SOURCE = os.path.join(ROOT, "llama_fp32_token_decode_b300", "csrc", "matvec.cu")
+BATTN_PROFILE = os.path.join(ROOT, "profiles", "battn_batched_44m.md")
+BATTN_SOURCE = os.path.join(ROOT, "llama_fp32_token_decode_b300", "csrc", "batched.cu")
+BATTN_HEAD = "template <int LPR, int G, int MINB>\n__global__ void"
 
 
 def parse_args():
@@ -212,11 +215,10 @@ def tf32x3_peak(peaks):
     return bf16 * (1.1 / 2.25) / 3.0
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
-    or None when the summary is missing or the kernel source changed since."""
+def summary_values(path):
+    """The `- key: value` lines of a committed ncu summary, or None."""
     try:
-        txt = open(PROFILE_TRAFFIC).read()
+        txt = open(path).read()
     except OSError:
         return None
     vals = {}
@@ -224,6 +226,28 @@ def profiled_traffic():
         if ":" in ln and ln.strip().startswith("- "):
             k, v = ln.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
+    return vals
+
+
+def kernel_text_sha256(path, head):
+    """sha256 of one kernel's source text: from the line that starts with
+    `head` to the first closing brace in column 0 after it (None if absent)."""
+    src = open(path).read()
+    i = src.find(head)
+    if i < 0:
+        return None
+    j = src.find("\n}\n", i)
+    if j < 0:
+        return None
+    return hashlib.sha256(src[i:j + 3].encode()).hexdigest()
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    vals = summary_values(PROFILE_TRAFFIC)
+    if vals is None:
+        return None
     src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
     if vals.get("matvec.cu sha256") != src:
         return None
@@ -231,6 +255,24 @@ def profiled_traffic():
         return float(vals["dram bytes per 7B-shape launch (read + write)"])
     except (KeyError, ValueError):
         return None
+
+
+def profiled_battn_traffic(alg_bytes):
+    """Per-launch DRAM bytes of the batched attention at the timed position:
+    the captured launch's DRAM bytes over its algorithmic bytes (K and V rows
+    read once per position, so both grow with the positions) times this
+    launch's algorithmic bytes. None when the summary is missing or the
+    kernel's source text changed since the capture."""
+    vals = summary_values(BATTN_PROFILE)
+    if vals is None or vals.get("battn4_kernel source sha256") != kernel_text_sha256(
+            BATTN_SOURCE, BATTN_HEAD):
+        return None
+    try:
+        dram = float(vals["dram bytes per launch (read + write)"])
+        alg = float(vals["algorithmic bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+    return dram / alg * alg_bytes
 
 
 def oracle_sample(cfg, blob, prompt, n_fwd: int):
@@ -628,7 +670,8 @@ def run_ours_batched(args, world, rank, local, compact=False):
     else:
         ach = dk["bytes"] / (dk["launch_ms"] / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                    "frac": ach / hbm, "traffic": None}
+                    "frac": ach / hbm,
+                    "traffic": profiled_battn_traffic(dk["bytes"]) if dom == 7 else None}
     roofline.update({"kernel": dk["name"], "launch_ms": dk["launch_ms"],
                      "share_of_kernel_time": dk["ms_per_step"] / total_ms,
                      "peak_source": (f"{peak_kind} bf16_tflops x 1.1/2.25 / 3 (3xTF32)"

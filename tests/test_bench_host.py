@@ -22,3 +22,31 @@ def test_batched_run_bound_matches_explicit_count():
     got, gemm = bench.batched_run_bound(cfg, lens, steps, B, hbm, p3)
     assert np.isclose(got, total, rtol=1e-12)
     assert np.isclose(gemm, n_lock * max(weights / (hbm * 1e9), flops / (p3 * 1e12)))
+
+
+def test_batched_attention_traffic_scales_and_follows_the_kernel(monkeypatch):
+    # the committed capture's DRAM bytes were taken at 301 positions; at any
+    # other position they scale with the algorithmic bytes, and they are
+    # withdrawn (None) when the kernel's source text no longer matches
+    vals = bench.summary_values(bench.BATTN_PROFILE)
+    ratio = float(vals["dram bytes per launch (read + write)"]) / float(
+        vals["algorithmic bytes per launch"])
+    assert 1.0 <= ratio < 1.05  # every K and V row read once
+    if vals["battn4_kernel source sha256"] == bench.kernel_text_sha256(bench.BATTN_SOURCE,
+                                                                       bench.BATTN_HEAD):
+        alg = 4.0 * 256 * (2 * 321 * 512 + 2 * 512)
+        assert np.isclose(bench.profiled_battn_traffic(alg), ratio * alg)
+    monkeypatch.setattr(bench, "BATTN_HEAD", "no such kernel head")
+    assert bench.profiled_battn_traffic(1e8) is None
+
+
+def test_kernel_text_hash_ignores_the_rest_of_the_file(tmp_path):
+    head = "template <int A>\n__global__ void"
+    body = head + " k() {\n    x();\n}\n"
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text("// one\n" + body + "void other() {}\n")
+    b.write_text("// two\nint y;\n" + body)
+    c.write_text("// one\n" + body.replace("x()", "z()"))
+    ha = bench.kernel_text_sha256(str(a), head)
+    assert ha is not None and ha == bench.kernel_text_sha256(str(b), head)
+    assert ha != bench.kernel_text_sha256(str(c), head)
