@@ -354,7 +354,13 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             t.head_dim = h->hd;
             t.seq_len = c.seq_len;
             t.cache_seq = h->cache_seq;
-            return launch_battn(t, M, s, true);
+            // Launched after the QKV GEMM has drained, not overlapped with it:
+            // with programmatic dependent launch its CTAs took SM slots while
+            // the GEMM's CTAs still held them, landed unevenly and ran beside
+            // the GEMM's shared-memory configuration (measured: the 256-row
+            // step 0.53 -> 0.50 s without the overlap; the Wo GEMM after it
+            // keeps the overlap, which measured better).
+            return launch_battn(t, M, s, false);
         }
         case BK_WO:
             g.N = d;
