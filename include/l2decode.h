@@ -130,7 +130,8 @@ L2_API int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, i
  * PyTorch tensors): d_tokens, d_pos int32 [B], d_logits fp32 [B][V] or NULL.
  * Queued on `stream` (a cudaStream_t, NULL = legacy default stream); returns
  * without waiting. Device values are not range-checked: tokens are clamped to
- * [0, V) and positions to [0, S) on the device. */
+ * [0, V) and positions to [0, S) (rolling: [0, rolling_positions)) on the
+ * device. */
 L2_API int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_pos, int32_t B,
                       float* d_logits, void* stream);
 
@@ -140,8 +141,8 @@ L2_API int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_
  * while p < n_prompt, afterwards the previous argmax; no stop token.
  * out_tokens[k] (host, [steps]) is the argmax at position n_prompt-1+k.
  * The token stays on the device between steps; one copy in, one copy out.
- * Errors: L2_EINVAL for n_prompt < 1, steps < 1, n_prompt+steps-1 > S, or a
- * prompt id outside [0, V). Synchronous. */
+ * Errors: L2_EINVAL for n_prompt < 1, steps < 1, n_prompt+steps-1 > S
+ * (rolling: > rolling_positions), or a prompt id outside [0, V). Synchronous. */
 L2_API int l2_generate(l2_handle* h, const int32_t* prompt, int32_t n_prompt, int32_t steps,
                 int32_t* out_tokens);
 
