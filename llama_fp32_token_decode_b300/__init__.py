@@ -5,7 +5,8 @@ CUDA kernels. There is no CPU fallback; importing this package fails loudly when
 the library has not been built (``python llama_fp32_token_decode_b300/build.py``).
 Functions keep the C names: l2_create, l2_create_from_device, l2_forward, l2_forward_device,
 l2_generate, l2_generate_device, l2_generate_batch, l2_generate_batch_device,
-l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_generate_sample,
+l2_generate_batch_sample, l2_generate_batch_sample_device, l2_generate_batch_prefill,
+l2_generate_batch_prefill_device, l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_generate_sample,
 l2_generate_sample_device, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
 l2_classify_greedy_noalloc, l2_gemm_tf32x3.
@@ -27,7 +28,7 @@ ERROR_NAMES = {L2_EINVAL: "L2_EINVAL", L2_ENOMEM: "L2_ENOMEM", L2_ECUDA: "L2_ECU
 # kinds of l2_time_kernel / l2_kernel_bytes
 KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residual",
                 "classifier_argmax", "b_qkv_gemm", "b_attention", "b_wo_gemm", "b_w13_gemm",
-                "b_w2_gemm", "b_classifier_gemm", "b_rmsnorm", "b_advance")
+                "b_w2_gemm", "b_classifier_gemm", "b_embedding", "b_advance")
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device",
