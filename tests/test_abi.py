@@ -101,3 +101,52 @@ def test_create_without_device_reports_cuda_error(l2):
     with pytest.raises(l2.L2Error) as e:
         l2.l2_create(cfg, np.zeros(l2.l2_blob_floats(cfg), np.float32))
     assert e.value.code in (l2.L2_ECUDA, l2.L2_ENOMEM)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "l2decode.h"
+
+int main(void) {
+    /* the 15M workload shape, untied classifier */
+    l2_config c;
+    memset(&c, 0, sizeof c);
+    c.dim = 288; c.hidden_dim = 768; c.n_layers = 6; c.n_heads = 6; c.n_kv_heads = 6;
+    c.vocab_size = 32000; c.seq_len = 256; c.rope_theta = 10000.0f; c.norm_eps = 1e-5f;
+    c.max_batch = 1;
+    printf("%zu\n", l2_blob_floats(&c));
+    l2_handle* h = (l2_handle*)&c;  /* must be overwritten with NULL on failure */
+    c.dim = 65;                       /* not a multiple of n_heads */
+    int rc = l2_create(&c, NULL, 0, &h);
+    printf("%d %d\n", rc, h == NULL);
+    printf("%s\n", l2_last_error(NULL));
+    printf("%d\n", l2_reset(NULL, -1));
+    l2_destroy(NULL);
+    return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_is_plain_c_and_links_from_c(l2, tmp_path, lang):
+    # a C (and a C++) consumer compiles against the header alone with strict
+    # warnings, links the in-tree library and calls its host-only paths
+    import subprocess
+    src = tmp_path / ("main.c" if lang == "c" else "main.cpp")
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "main"
+    lib_dir = os.path.dirname(l2.LIB_PATH)
+    cc = ["gcc", "-std=c99"] if lang == "c" else ["g++", "-std=c++17"]
+    cmd = cc + ["-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                str(src), "-o", str(exe), "-L", lib_dir, "-l:libl2decode.so",
+                "-Wl,-rpath," + lib_dir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.splitlines()
+    assert int(lines[0]) == 24407712
+    assert lines[1] == f"{l2.L2_EINVAL} 1"
+    assert "invalid config" in lines[2]
+    assert int(lines[3]) == l2.L2_EINVAL
