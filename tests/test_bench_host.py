@@ -50,3 +50,14 @@ def test_kernel_text_hash_ignores_the_rest_of_the_file(tmp_path):
     ha = bench.kernel_text_sha256(str(a), head)
     assert ha is not None and ha == bench.kernel_text_sha256(str(b), head)
     assert ha != bench.kernel_text_sha256(str(c), head)
+
+
+def test_clock_records_that_reject_a_timed_region():
+    ok = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(None)  # no sampler: nothing to judge
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=1500.0, reasons=["sw_power_cap"]))
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(ok, reasons=[r]))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))  # held low with no reason
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=1900.0))
