@@ -365,7 +365,13 @@ def run_reference(args, world, rank):
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload, "global_batch": 1,
-                       "forwards_per_step": per_step},
+                       "dim": cfg["dim"], "n_layers": cfg["n_layers"], "n_heads": cfg["n_heads"],
+                       "n_kv_heads": cfg["n_kv_heads"], "hidden_dim": cfg["hidden_dim"],
+                       "vocab_size": cfg["vocab_size"], "seq_len": cfg["seq_len"],
+                       "forwards_per_step": per_step, "parallelism": "replicas1",
+                       "sample_of": ("sequence 0 of the 256-sequence batched workload"
+                                     if w["prompt"] == "batch" else
+                                     f"the {args.workload} generation")},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
