@@ -271,8 +271,9 @@ L2_API int l2_reset(l2_handle* h, int32_t seq);
 /* Frees every device and host resource of h. NULL is accepted. */
 L2_API void l2_destroy(l2_handle* h);
 
-/* Text of the last error on h (or of the last failed l2_create when h is
- * NULL). The pointer stays valid until the next call on h. */
+/* Text of the last error on h (or, when h is NULL, of the last failed
+ * l2_create / l2_create_from_device on the calling thread). The pointer stays
+ * valid until the next call on h (or the next failed create on that thread). */
 L2_API const char* l2_last_error(const l2_handle* h);
 
 /* Measurement hook: launches one kernel kind of the step `iters` times on
