@@ -129,9 +129,10 @@ L2_API int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, i
 /* Same as l2_forward with device buffers owned by the caller (for example
  * PyTorch tensors): d_tokens, d_pos int32 [B], d_logits fp32 [B][V] or NULL.
  * Queued on `stream` (a cudaStream_t, NULL = legacy default stream); returns
- * without waiting. Device values are not range-checked: tokens are clamped to
- * [0, V) and positions to [0, S) (rolling: [0, rolling_positions)) on the
- * device. */
+ * without waiting. Device values are checked on the device: a token outside
+ * [0, V) or a position outside [0, S) (rolling: [0, rolling_positions)) is
+ * clamped, so that every access stays in bounds, and reported as L2_EINVAL by
+ * l2_status (see there). */
 L2_API int l2_forward_device(l2_handle* h, const int32_t* d_tokens, const int32_t* d_pos, int32_t B,
                       float* d_logits, void* stream);
 
@@ -171,14 +172,15 @@ L2_API int l2_generate_prefill(l2_handle* h, const int32_t* prompt, int32_t n_pr
                                int32_t steps, int32_t* out_tokens);
 
 /* l2_generate_prefill with device buffers (d_prompt int32 [n_prompt], d_out
- * int32 [steps]), queued on `stream`; returns without waiting. Device prompt
- * ids are not range-checked (clamped). */
+ * int32 [steps]), queued on `stream`; returns without waiting. A device prompt
+ * id outside [0, V) is clamped and reported by l2_status. */
 L2_API int l2_generate_prefill_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
                                       int32_t steps, int32_t* d_out, void* stream);
 
 /* l2_generate with device buffers: d_prompt int32 [n_prompt], d_out int32
  * [steps]; queued on `stream`, returns without waiting. Host-side checks as
- * l2_generate; device prompt ids are not range-checked (clamped). */
+ * l2_generate; a device prompt id outside [0, V) is clamped and reported by
+ * l2_status. */
 L2_API int l2_generate_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt, int32_t steps,
                        int32_t* d_out, void* stream);
 
@@ -200,7 +202,8 @@ L2_API int l2_generate_sample(l2_handle* h, const int32_t* prompt, int32_t n_pro
 
 /* l2_generate_sample with device buffers: d_prompt int32 [n_prompt],
  * d_uniforms fp32 [steps], d_out int32 [steps]; queued on `stream`, returns
- * without waiting. Device values are not range-checked. */
+ * without waiting. A device prompt id outside [0, V) is clamped and reported
+ * by l2_status; uniform numbers are not checked. */
 L2_API int l2_generate_sample_device(l2_handle* h, const int32_t* d_prompt, int32_t n_prompt,
                                      int32_t steps, float temperature, float topp,
                                      const float* d_uniforms, int32_t* d_out, void* stream);
@@ -222,7 +225,7 @@ L2_API int l2_generate_batch(l2_handle* h, const int32_t* prompts, const int32_t
  * d_prompts int32 [sum of lens], d_out int32 [B][steps]; `lens` stays a HOST
  * array [B] (the lockstep schedule is planned on the host). Queued on
  * `stream`, returns without waiting. Host-side checks as l2_generate_batch;
- * device prompt ids are not range-checked (clamped to [0, V)). */
+ * a device prompt id outside [0, V) is clamped and reported by l2_status. */
 L2_API int l2_generate_batch_device(l2_handle* h, const int32_t* d_prompts, const int32_t* lens,
                                     int32_t B, int32_t steps, int32_t* d_out, void* stream);
 
@@ -257,13 +260,37 @@ L2_API int l2_generate_batch_sample(l2_handle* h, const int32_t* prompts, const 
 
 /* l2_generate_batch_sample with device buffers: d_prompts int32 [sum of
  * lens], d_uniforms fp32 [B][steps], d_out int32 [B][steps]; lens a HOST
- * array [B]. Queued on `stream`, returns without waiting; device values are
- * not range-checked. */
+ * array [B]. Queued on `stream`, returns without waiting; a device prompt id
+ * outside [0, V) is clamped and reported by l2_status, uniform numbers are not
+ * checked. */
 L2_API int l2_generate_batch_sample_device(l2_handle* h, const int32_t* d_prompts,
                                            const int32_t* lens, int32_t B, int32_t steps,
                                            float temperature, float topp,
                                            const float* d_uniforms, int32_t* d_out,
                                            void* stream);
+
+/* Status of the device-side work queued by the *_device calls, which return
+ * before it runs: waits for `stream` (a cudaStream_t, NULL = legacy default
+ * stream) and the handle's own stream, reads the handle's device error word,
+ * clears it and returns what it holds: L2_OK; L2_EINVAL when a device token
+ * id or position was out of range (the kernels clamped it, so the results are
+ * not those of the input); L2_ETIMEOUT when a bounded device wait gave up.
+ * The word accumulates over *_device calls until l2_status reads it; every
+ * synchronous call clears it when it starts and reports its own work itself,
+ * so call l2_status before the next synchronous call on the handle.
+ * Errors: as listed, plus L2_ECUDA. */
+L2_API int l2_status(l2_handle* h, void* stream);
+
+/* Test hook of the failure-detection path. Every wait of a decode kernel on a
+ * bulk-copy completion is bounded: when it gives up, the kernel sets the
+ * handle's device error word, drains its own copies and returns, and the call
+ * reports L2_ETIMEOUT. This hook runs that bounded wait, the same device
+ * routine, on an mbarrier that nothing arrives at (no copy in flight), limited
+ * to spin_cycles SM clock cycles, so that it gives up; the error word is then
+ * read, cleared and reported as by a synchronous call. Returns L2_ETIMEOUT
+ * when the wait gave up as designed; the handle stays usable.
+ * Errors: L2_EINVAL for spin_cycles outside [1, 2e9], L2_ECUDA. Synchronous. */
+L2_API int l2_watchdog_check(l2_handle* h, int64_t spin_cycles);
 
 /* Clears KV cache `seq` (-1: all caches) to zero. Errors: L2_EINVAL. */
 L2_API int l2_reset(l2_handle* h, int32_t seq);

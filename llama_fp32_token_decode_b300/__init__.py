@@ -9,7 +9,7 @@ l2_generate_batch_sample, l2_generate_batch_sample_device, l2_generate_batch_pre
 l2_generate_batch_prefill_device, l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_generate_sample,
 l2_generate_sample_device, l2_reset, l2_destroy,
 l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
-l2_classify_greedy_noalloc, l2_gemm_tf32x3.
+l2_classify_greedy_noalloc, l2_gemm_tf32x3, l2_status, l2_watchdog_check.
 """
 from __future__ import annotations
 
@@ -37,7 +37,7 @@ EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward",
            "l2_generate_prefill", "l2_generate_prefill_device", "l2_generate_sample",
            "l2_generate_sample_device", "l2_reset", "l2_destroy",
            "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
-           "l2_gemm_tf32x3")
+           "l2_gemm_tf32x3", "l2_status", "l2_watchdog_check")
 
 L2_NOALLOC_MAX_VOCAB = 262144
 
@@ -97,6 +97,8 @@ _SIG = {
                                       _P]),
     "l2_classify_greedy_noalloc": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P, _P,
                                                   _P]),
+    "l2_status": (ctypes.c_int, [_P, _P]),
+    "l2_watchdog_check": (ctypes.c_int, [_P, ctypes.c_int64]),
 }
 for _name, (_res, _args) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -281,6 +283,18 @@ def l2_generate_batch_sample_device(h, d_prompts, lens, steps: int, temperature:
     _check(_lib.l2_generate_batch_sample_device(h, _ptr(d_prompts), lens.ctypes.data, lens.size,
                                                 steps, temperature, topp, _ptr(d_uniforms),
                                                 _ptr(d_out), _stream(stream)), h)
+
+
+def l2_status(h, stream=None) -> int:
+    """Return code of the device work queued by the *_device calls (waits for
+    `stream`); no exception, so that tests can compare codes."""
+    return int(_lib.l2_status(h, _stream(stream)))
+
+
+def l2_watchdog_check(h, spin_cycles: int) -> int:
+    """Runs one bounded device wait that nothing completes; returns the C code
+    (L2_ETIMEOUT when the wait gave up as designed)."""
+    return int(_lib.l2_watchdog_check(h, int(spin_cycles)))
 
 
 def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:

@@ -147,10 +147,14 @@ bool config_valid(const l2_config* c, std::string* why) {
 __global__ void init_state_kernel(L2State* st, int pos, int token, const int* d_token,
                                   const int* d_pos, int vocab, int seq_len, int n_prompt, int mode,
                                   const int* prompt, int* out, int reset_err) {
-    int p = d_pos ? d_pos[0] : pos;
-    int t = d_token ? d_token[0] : (prompt && mode >= 1 ? prompt[0] : token);
-    p = min(max(p, 0), seq_len - 1);
-    t = min(max(t, 0), vocab - 1);
+    const int p_in = d_pos ? d_pos[0] : pos;
+    // the token is checked (and clamped) where it is consumed, by the layer-0
+    // QKV kernel's embedding read; a device position outside [0, seq_len) is
+    // reported here and clamped, since the RoPE table and the cache slot
+    // index depend on it
+    const int t = d_token ? d_token[0] : (prompt && mode >= 1 ? prompt[0] : token);
+    const int p = min(max(p_in, 0), seq_len - 1);
+    (void)vocab;
     st->pos = p;
     st->token = t;
     st->n_prompt = n_prompt;
@@ -160,6 +164,7 @@ __global__ void init_state_kernel(L2State* st, int pos, int token, const int* d_
     st->argmax_key = 0ull;
     st->cls_done = 0u;
     if (reset_err) st->err = 0;
+    if (p != p_in) atomicOr(&st->err, ERR_BAD_INPUT);
 }
 
 MatvecArgs base_args(l2_handle* h) {
@@ -268,12 +273,27 @@ int capture(l2_handle* h, int n_forwards, cudaGraphExec_t* out, bool sample = fa
     return L2_OK;
 }
 
+// Synchronous calls clear the device error word before their work and report
+// it after; the *_device calls leave it accumulating for l2_status.
+cudaError_t clear_device_error(l2_handle* h, cudaStream_t s) {
+    return cudaMemsetAsync(&h->st->err, 0, sizeof(int), s);
+}
+
+// Return code for the bits of the device error word.
+int status_of(l2_handle* h, int err) {
+    if (err & (ERR_TIMEOUT_TMA | ERR_BAD_PLAN))
+        return fail(h, L2_ETIMEOUT, "a bounded device wait gave up (bulk-copy completion)");
+    if (err & ERR_BAD_INPUT)
+        return fail(h, L2_EINVAL,
+                    "a device token id outside [0, vocab_size) or position outside its range "
+                    "(it was clamped, so the results are not those of the input)");
+    return L2_OK;
+}
+
 int check_device_error(l2_handle* h) {
     int err = 0;
     L2_CUDA(h, cudaMemcpy(&err, &h->st->err, sizeof(int), cudaMemcpyDeviceToHost));
-    if (err & (ERR_TIMEOUT_TMA | ERR_BAD_PLAN))
-        return fail(h, L2_ETIMEOUT, "a bounded device wait gave up (bulk-copy completion)");
-    return L2_OK;
+    return status_of(h, err);
 }
 
 // ---------------------------------------------------------------- batched path
@@ -314,6 +334,9 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             n.ss_stride = h->ss_stride;
             n.d = d;
             n.vocab = V;
+            n.pos = h->b_pos;
+            n.pmax = h->pmax;
+            n.err = &h->st->err;
             return launch_brmsnorm(n, M, s, true);
         }
         case BK_QKV:
@@ -472,9 +495,8 @@ __global__ void prefill_setup_kernel(int n, int pos0, const int* tokens, int voc
                                      int* b_pos, int* b_seq, int* b_active,
                                      unsigned long long* keys, L2State* st) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r == 0) st->err = 0;
     if (r >= n) return;
-    b_token[r] = min(max(tokens[r], 0), vocab - 1);
+    b_token[r] = tokens[r];  // checked and clamped by the embedding gather
     b_pos[r] = pos0 + r;
     b_seq[r] = 0;
     b_active[r] = 1;
@@ -509,7 +531,6 @@ __global__ void binit_kernel(int M, int mode, int* pos, int* token, int* active,
                              const int* len, const int* poff, const int* prompts,
                              unsigned long long* keys, L2State* st) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b == 0) st->err = 0;
     if (b >= M) return;
     active[b] = 1;
     keys[b] = 0ull;
@@ -523,7 +544,6 @@ __global__ void binit_kernel(int M, int mode, int* pos, int* token, int* active,
 __global__ void bset_kernel(int M, int pos, int* b_pos, int* token, int* active,
                             unsigned long long* keys, L2State* st) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b == 0) st->err = 0;
     if (b >= M) return;
     b_pos[b] = pos;
     token[b] = 1;
@@ -736,6 +756,18 @@ int capture_bstep(l2_handle* h, int M, int steps, bool sample = false) {
     gM = M;
     gS = steps;
     return L2_OK;
+}
+
+// One bounded wait that nothing completes: an mbarrier expecting one arrival
+// that is never made, with no copy in flight. The wait gives up after `limit`
+// SM clock cycles and records the timeout in the error word, exactly as the
+// decode kernels' waits on bulk-copy completions do.
+__global__ void watchdog_kernel(L2State* st, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0u, limit)) atomicOr(&st->err, ERR_TIMEOUT_TMA);
 }
 
 }  // namespace
@@ -1071,6 +1103,7 @@ int l2_forward(l2_handle* h, const int32_t* tokens, const int32_t* pos, int32_t 
             return fail(h, L2_EINVAL, "position out of range");
     }
     if (B > 1) {
+        L2_CUDA(h, clear_device_error(h, h->stream));
         L2_CUDA(h, cudaMemcpyAsync(h->b_token, tokens, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
                                    h->stream));
         L2_CUDA(h, cudaMemcpyAsync(h->b_pos, pos, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
@@ -1169,6 +1202,7 @@ static int generate_batch_impl(l2_handle* h, const int32_t* prompts, const int32
     if (!on_device)
         for (long long i = 0; i < total; ++i)
             if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    if (!on_device) L2_CUDA(h, clear_device_error(h, h->stream));
     if (sample) {
         if (!uniforms) return fail(h, L2_EINVAL, "NULL uniforms");
         if (!(temperature >= 0.0f) || !(topp > 0.0f && topp <= 1.0f))
@@ -1244,6 +1278,7 @@ int l2_prefill(l2_handle* h, const int32_t* tokens, int32_t n, int32_t pos0, flo
     for (int i = 0; i < n; ++i)
         if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab_size) return fail(h, L2_EINVAL, "token out of range");
     cudaStream_t s = h->stream;
+    L2_CUDA(h, clear_device_error(h, s));
     L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, tokens, sizeof(int32_t) * n, cudaMemcpyHostToDevice, s));
     if ((rc = enqueue_prefill(h, h->d_prompt, n, pos0, logits_out != nullptr, s)) != L2_OK) return rc;
     if (logits_out)
@@ -1271,6 +1306,7 @@ static int generate_prefill_impl(l2_handle* h, const int32_t* prompt, int32_t n_
         for (int i = 0; i < n_prompt; ++i)
             if (prompt[i] < 0 || prompt[i] >= h->cfg.vocab_size)
                 return fail(h, L2_EINVAL, "prompt id out of range");
+        L2_CUDA(h, clear_device_error(h, s));
         L2_CUDA(h, cudaMemcpyAsync(h->d_prompt, prompt, sizeof(int32_t) * n_prompt,
                                    cudaMemcpyHostToDevice, s));
         d_prompt = h->d_prompt;
@@ -1293,10 +1329,9 @@ __global__ void bprefill_setup_kernel(int n, int start, const int* rmap, const i
                                       int* b_seq, int* b_active, unsigned long long* keys,
                                       L2State* st) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r == 0 && start == 0) st->err = 0;
     if (r >= n) return;
     const int b = rmap[2 * (start + r)], p = rmap[2 * (start + r) + 1];
-    b_token[r] = min(max(prompts[poff[b] + p], 0), vocab - 1);
+    b_token[r] = prompts[poff[b] + p];  // checked and clamped by the embedding gather
     b_pos[r] = p;
     b_seq[r] = b;
     b_active[r] = 1;
@@ -1347,6 +1382,7 @@ static int generate_batch_prefill_impl(l2_handle* h, const int32_t* prompts, con
     if (!on_device)
         for (long long i = 0; i < total; ++i)
             if (prompts[i] < 0 || prompts[i] >= V) return fail(h, L2_EINVAL, "prompt id out of range");
+    if (!on_device) L2_CUDA(h, clear_device_error(h, h->stream));
     rmap.reserve(2 * total);
     for (int b = 0; b < B; ++b)
         for (int p = 0; p < lens[b]; ++p) {
@@ -1450,6 +1486,7 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kind >= 6) {
         const int M = h->cfg.max_batch, bk = kind - 6;
+        L2_CUDA(h, clear_device_error(h, s));
         bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
                                                     h->b_keys, h->st);
         L2_CUDA(h, cudaGetLastError());
@@ -1477,6 +1514,31 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
     L2_CUDA(h, cudaEventElapsedTime(&t, h->ev0, h->ev1));
     *ms = t / iters;
     return check_device_error(h);
+}
+
+int l2_status(l2_handle* h, void* stream) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    L2_CUDA(h, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    int err = 0;
+    L2_CUDA(h, cudaMemcpy(&err, &h->st->err, sizeof(int), cudaMemcpyDeviceToHost));
+    L2_CUDA(h, cudaMemset(&h->st->err, 0, sizeof(int)));
+    return status_of(h, err);
+}
+
+int l2_watchdog_check(l2_handle* h, int64_t spin_cycles) {
+    if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
+    if (spin_cycles < 1 || spin_cycles > kSpinLimitCycles)
+        return fail(h, L2_EINVAL, "spin_cycles outside [1, 2e9]");
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    L2_CUDA(h, cudaMemsetAsync(&h->st->err, 0, sizeof(int), h->stream));
+    watchdog_kernel<<<1, 32, 0, h->stream>>>(h->st, static_cast<long long>(spin_cycles));
+    L2_CUDA(h, cudaGetLastError());
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    int err = 0;
+    L2_CUDA(h, cudaMemcpy(&err, &h->st->err, sizeof(int), cudaMemcpyDeviceToHost));
+    L2_CUDA(h, cudaMemset(&h->st->err, 0, sizeof(int)));
+    return status_of(h, err);
 }
 
 double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {

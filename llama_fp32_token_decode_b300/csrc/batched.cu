@@ -32,7 +32,15 @@ __global__ void __launch_bounds__(kNormThreads) brmsnorm_kernel(const BNormArgs 
     const int b = a.row0 + blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, d4 = d >> 2;
     float4* x4 = reinterpret_cast<float4*>(a.x + static_cast<size_t>(b) * d);
-    const int tok = min(max(__ldcg(a.token + b), 0), a.vocab - 1);
+    // a token or position outside its range (device inputs are not checked
+    // on the host) is reported; the token is clamped so that the read stays
+    // inside the table, positions are clamped by their readers
+    const int raw = __ldcg(a.token + b);
+    const int tok = min(max(raw, 0), a.vocab - 1);
+    if (tid == 0 && a.err != nullptr) {
+        const int p = __ldcg(a.pos + b);
+        if (raw != tok || p < 0 || p >= a.pmax) atomicOr(a.err, ERR_BAD_INPUT);
+    }
     const float4* src4 = reinterpret_cast<const float4*>(a.emb + static_cast<size_t>(tok) * d);
     float4* hi4 = reinterpret_cast<float4*>(a.xn_hi + static_cast<size_t>(b) * d);
     float4* lo4 = reinterpret_cast<float4*>(a.xn_lo + static_cast<size_t>(b) * d);

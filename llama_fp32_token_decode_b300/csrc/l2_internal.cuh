@@ -19,6 +19,7 @@ enum : int {
     ERR_TIMEOUT_TMA = 1,   // a bulk-copy completion wait gave up
     ERR_BAD_PLAN = 2,      // a kernel received an impossible launch plan
     ERR_NAN = 4,           // the classifier met a NaN logit
+    ERR_BAD_INPUT = 8,     // a device token id or position was out of range (clamped)
 };
 
 // Bound for every device-side spin: about one second at 2 GHz.
@@ -170,6 +171,9 @@ struct BNormArgs {
     float* ss_out;         // [M][ss_stride]: slot 0 = sum of squares of x[r]
     int ss_stride;
     int d, vocab;
+    const int* pos;        // [M] position of each row: checked against [0, pmax)
+    int pmax;
+    int* err;              // ERR_BAD_INPUT when a token or position is out of range
 };
 
 struct BAttnArgs {
@@ -279,12 +283,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on a phase of an mbarrier; false when the bound is hit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Bounded wait on a phase of an mbarrier; false once `limit` SM clock cycles
+// have passed without the phase completing.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit = kSpinLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kSpinLimitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }

@@ -170,7 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
 
     const float* src = a.src;
     if (a.emb != nullptr) {
-        const int tok = min(max(__ldcg(&st->token), 0), a.vocab - 1);
+        // every consumed token passes here (from the caller, a prompt or the
+        // previous argmax): an id outside [0, V) is reported, and clamped so
+        // that the read stays inside the table
+        const int raw = __ldcg(&st->token);
+        const int tok = min(max(raw, 0), a.vocab - 1);
+        if (raw != tok && blockIdx.x == 0 && tid == 0) atomicOr(&st->err, ERR_BAD_INPUT);
         src = a.emb + static_cast<size_t>(tok) * K;
     }
     const float4* src4 = reinterpret_cast<const float4*>(src);

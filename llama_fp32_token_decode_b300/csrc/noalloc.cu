@@ -14,8 +14,6 @@
 // stand-in symbol, not a device address. The device address is looked up once
 // per device with cudaGetSymbolAddress (on the first call made with that
 // device current) and passed to the kernels.
-#include <string.h>
-
 #include <mutex>
 
 #include "l2_internal.cuh"
@@ -142,14 +140,10 @@ int l2_classify_greedy_noalloc(const float* d_x, const float* d_gain, const floa
     a.vocab = vocab;
     a.d = dim;
     a.st = st;
-    // same L2 rule as a handle: keep a small classifier resident, stream a large one
-    const double wbytes = 4.0 * static_cast<double>(vocab) * dim;
-    if (wbytes < 100e6) {
-        const float frac = 1.0f;
-        uint32_t bits;
-        memcpy(&bits, &frac, 4);
-        a.l2_policy = bits;
-    }
+    // the classifier belongs to the caller: stream it with the evict_first hint
+    // (policy 0), so that the call leaves none of it marked to stay in L2 at
+    // the expense of the caller's own working set
+    a.l2_policy = 0;
 
     noalloc_init_kernel<<<1, 1, 0, cs>>>(st);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "init launch");

@@ -55,3 +55,42 @@ def check_teacher_forced(dec, consumed, trace, positions=None):
         if top2_gap(trace[p]) > GAP_TOL:
             assert int(np.argmax(lg)) == int(np.argmax(trace[p])), f"pos {p}: argmax differs"
     return worst
+
+
+def _trace_worker(args):
+    """Spawned worker: rebuild the seeded blob, then the oracle's logits at
+    positions 0 .. len(tokens) - 1 of one sequence fed `tokens`."""
+    cfg, seed, std, tokens = args
+    blob = synth.make_blob(cfg, seed, std=std, threads=1)
+    m = oracle.Model(cfg, blob)
+    out = np.stack([m.forward(int(t), p) for p, t in enumerate(tokens)])
+    m.close()
+    return out
+
+
+def _generate_worker(args):
+    cfg, seed, std, prompt, steps = args
+    blob = synth.make_blob(cfg, seed, std=std, threads=1)
+    return oracle.Model(cfg, blob).generate(np.asarray(prompt, np.int32), steps, trace=True)
+
+
+class OracleJobs:
+    """Oracle runs in spawned processes (safe beside an initialised CUDA
+    context), started before the GPU work so that both proceed at once."""
+
+    def __init__(self, n: int):
+        import multiprocessing
+        import os
+        ctx = multiprocessing.get_context("spawn")
+        self.pool = ctx.Pool(max(1, min(n, os.cpu_count() or 1)))
+
+    def traces(self, cfg, seed, std, token_lists):
+        return self.pool.map_async(_trace_worker,
+                                   [(cfg, seed, std, np.asarray(t, np.int32)) for t in token_lists])
+
+    def generate(self, cfg, seed, std, prompt, steps):
+        return self.pool.apply_async(_generate_worker, ((cfg, seed, std, prompt, steps),))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()

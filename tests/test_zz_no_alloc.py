@@ -1,4 +1,5 @@
-"""The no-allocation classifier entry point against the handle-based forward.
+"""The no-allocation classifier entry point against the handle-based forward
+and the oracle.
 
 l2_classify_greedy_noalloc exists for callers that cannot allocate device
 memory themselves (their device memory belongs to another framework's arena,
@@ -17,7 +18,7 @@ import numpy as np
 import pytest
 
 import synth
-from parity_util import REL_L2_TOL, config
+from parity_util import GAP_TOL, REL_L2_TOL, config, rel_l2, top2_gap
 
 pytestmark = pytest.mark.gpu
 
@@ -58,9 +59,15 @@ def test_noalloc_classifier_matches_forward_on_two_calls():
     d_token = torch.full((1,), -7, dtype=torch.int32, device=dev)
     d_logit = torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
 
+    import oracle
+    om = oracle.Model(cfg, blob)
     with l2.Decoder(cfg, blob) as dec:
         for tok in (17, 29001):
             ref = dec.forward([tok], [0])[0]
+            # the closed form of this model, computed by the oracle (its pin:
+            # zero layer weights leave logits = Wcls . rmsnorm(E[tok]))
+            want_lg = om.forward(tok, 0)
+            assert rel_l2(ref, want_lg) <= REL_L2_TOL
             d_x = torch.from_numpy(blob[tok * d:(tok + 1) * d].copy()).to(dev)
             rc = l2.l2_classify_greedy_noalloc(d_x, d_gain, d_wcls, d, V, cfg["norm_eps"],
                                                d_token, d_logit)
@@ -70,6 +77,12 @@ def test_noalloc_classifier_matches_forward_on_two_calls():
             assert int(d_token.item()) == want, (tok, int(d_token.item()), want)
             got = float(d_logit.item())
             assert abs(got - float(ref[want])) <= REL_L2_TOL * abs(float(ref[want])), (got, ref[want])
+            # and against the oracle directly, where its top-2 gap decides the token
+            if top2_gap(want_lg) > GAP_TOL:
+                assert int(d_token.item()) == int(np.argmax(want_lg))
+            o_want = float(want_lg[int(d_token.item())])
+            assert abs(got - o_want) <= REL_L2_TOL * abs(o_want), (got, o_want)
+    om.close()
 
     # sizes beyond the fixed scratch are rejected before any device work
     rc = l2.l2_classify_greedy_noalloc(d_gain, d_gain, d_wcls, d, l2.L2_NOALLOC_MAX_VOCAB + 1,
