@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--cpu-forwards", type=int, default=0,
                     help="oracle forwards in the CPU-baseline sample (0 = about 20 s worth)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-small", action="store_true",
+                    help="default run: skip the 15m / 44m / 110m batch-1 lines")
     ap.add_argument("--kernel-only", type=int, default=None,
                     help="time one kernel kind (0 QKV, 1 attention, 2 Wo, 3 W1/W3, 4 W2, "
                          "5 classifier; 6-13 the batched kinds with --workload batched) on "
@@ -252,12 +254,57 @@ def measured_peaks():
         return {"hbm_gbs": 6400.0}, "fallback"
 
 
+_FP32_PEAKS = None
+
+
+def measured_fp32_peaks():
+    """Dense fp32-input GEMM peaks measured live on this GPU with the library
+    GEMM (cuBLAS through torch.matmul, 8192^3, best of 5 after warm-up): TF32
+    tensor cores (allow_tf32) and plain SGEMM (FFMA). None when not measurable."""
+    global _FP32_PEAKS
+    if _FP32_PEAKS is not None:
+        return _FP32_PEAKS
+    try:
+        import torch
+        n = 8192
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn(n, n, device="cuda", generator=g)
+        b = torch.randn(n, n, device="cuda", generator=g)
+        out = {}
+        old = torch.backends.cuda.matmul.allow_tf32
+        for name, tf in (("tf32_tflops", True), ("sgemm_tflops", False)):
+            torch.backends.cuda.matmul.allow_tf32 = tf
+            for _ in range(2):
+                a @ b
+            best = float("inf")
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                a @ b
+                e1.record()
+                e1.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            out[name] = 2.0 * n ** 3 / (best / 1e3) / 1e12
+        torch.backends.cuda.matmul.allow_tf32 = old
+        del a, b
+        torch.cuda.empty_cache()
+        _FP32_PEAKS = out
+    except Exception:  # noqa: BLE001  (a probe failure only changes the denominator's source)
+        _FP32_PEAKS = {}
+    return _FP32_PEAKS
+
+
 def tf32x3_peak(peaks):
-    """Peak of the 3xTF32 GEMM in fp32-equivalent TFLOP/s: the measured bf16
-    dense peak times the nominal tf32/bf16 ratio (1.1 / 2.25 PFLOP/s), divided
-    by the three tensor passes per product."""
+    """Peak of the 3xTF32 GEMM in fp32-equivalent TFLOP/s and its source: the
+    TF32 tensor peak measured live (cuBLAS TF32, burst) divided by the three
+    tensor passes per product; without it, the measured bf16 dense peak times
+    the nominal tf32/bf16 ratio (1.1 / 2.25 PFLOP/s), divided by three."""
+    m = measured_fp32_peaks()
+    if m.get("tf32_tflops"):
+        return m["tf32_tflops"] / 3.0, "measured live: cuBLAS TF32 8192^3 (burst) / 3"
     bf16 = float(peaks.get("bf16_tflops", 1800.0))
-    return bf16 * (1.1 / 2.25) / 3.0
+    return bf16 * (1.1 / 2.25) / 3.0, "measured bf16_tflops x 1.1/2.25 / 3 (nominal ratio)"
 
 
 def summary_values(path):
@@ -336,7 +383,8 @@ def oracle_sample(cfg, blob, prompt, n_fwd: int):
 
 def default_cpu_forwards(name: str) -> int:
     # about 10-25 s of one core per sample
-    return {"15m": 256, "44m": 120, "110m": 40, "7b": 2, "batched": 120}[name]
+    # (7b: the first 8 forwards, the sample its configuration fixes: about a minute)
+    return {"15m": 256, "44m": 120, "110m": 40, "7b": 8, "batched": 120}[name]
 
 
 # ---------------------------------------------------------------- reference arm
@@ -352,13 +400,39 @@ def run_reference(args, world, rank):
         prompt = prompts[:lens[0]]
     else:
         prompt = synth.prompt(w)
-    per_step = max(1, (args.cpu_forwards or default_cpu_forwards(args.workload)) // 2)
-    for _ in range(args.warmup):
-        oracle_sample(cfg, blob, prompt, 1)
-    t = sum(oracle_sample(cfg, blob, prompt, per_step) for _ in range(args.steps))
+    if args.workload == "7b":
+        # one forward per step over the first 8 positions, in order and then
+        # again (the cache keeps the earlier positions): the configuration times
+        # the oracle on its first 8 steps, a step of seconds each
+        import oracle
+        per_step = 1
+        m = oracle.Model(cfg, blob)
+        toks = [int(t) for t in prompt[:8]]
+        k = 0
+
+        def one():
+            nonlocal k
+            p = k % 8
+            t0 = time.perf_counter()
+            m.forward(toks[p], p)
+            k += 1
+            return time.perf_counter() - t0
+
+        for _ in range(args.warmup):
+            one()
+        t = sum(one() for _ in range(args.steps))
+        m.close()
+        sample = ("one forward per step, positions 0..7 of the 7b workload's prompt in turn "
+                  "(its first 8 steps), single-threaded C oracle (-O2, no fast-math)")
+    else:
+        per_step = max(1, (args.cpu_forwards or default_cpu_forwards(args.workload)) // 2)
+        for _ in range(args.warmup):
+            oracle_sample(cfg, blob, prompt, 1)
+        t = sum(oracle_sample(cfg, blob, prompt, per_step) for _ in range(args.steps))
+        sample = (f"first {per_step} forwards (positions 0..{per_step - 1}) of the "
+                  f"{args.workload} workload per step, single-threaded C oracle (-O2, no "
+                  f"fast-math)")
     value = args.steps * per_step / t
-    sample = (f"first {per_step} forwards (positions 0..{per_step - 1}) of the {args.workload} "
-              f"workload per step, single-threaded C oracle (-O2, no fast-math)")
     line = {"impl": "reference",
             "metric": METRIC_BATCHED if args.workload == "batched" else METRIC, "value": value, "unit": "tok/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -534,8 +608,8 @@ def run_ours(args, world, rank, local):
         flops = 2.0 * n * params
         bytes_fp32 = 4.0 * params
         peaks, _ = measured_peaks()
-        bound_ms = max(bytes_fp32 / (float(peaks["hbm_gbs"]) * 1e6),
-                       flops / (tf32x3_peak(peaks) * 1e9))
+        p3, _ = tf32x3_peak(peaks)
+        bound_ms = max(bytes_fp32 / (float(peaks["hbm_gbs"]) * 1e6), flops / (p3 * 1e9))
         prefill = {"value": n_fwd / (ms_p / 1e3), "unit": "tok/s", "ms_per_step": ms_p,
                    "prefill_ms": ms_pre, "prefill_tok_s": n / (ms_pre / 1e3),
                    "prefill_roofline": {
@@ -582,12 +656,60 @@ def run_ours(args, world, rank, local):
     if blob is not None:
         del blob
     torch.cuda.empty_cache()
+    if args.workload == "7b" and not args.no_small:
+        line["small_models"] = run_small_models(args, world, local)
     if args.workload == "7b" and not args.no_batched:
         # the other half of the metric: batch 256 on the 44M shape, same process
         line["batch256"] = run_ours_batched(args, world, rank, local, compact=True)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_small_models(args, world, local):
+    """The pages' small shapes at batch 1 (15m: dim 288 / 6 layers; 44m: dim 512
+    / 8 layers, context 1024; 110m: dim 768 / 12 layers), each a full greedy
+    generation per step through l2_generate_device, timed like the headline.
+    Their weights (62 / 184 / 476 MB per forward) sit partly or wholly in the
+    126 MB L2, so a forward is bound by the latency of its dependent kernels
+    rather than by HBM; the HBM fraction is reported all the same."""
+    import torch
+
+    import llama_fp32_token_decode_b300 as l2
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    out = {}
+    for name in ("15m", "44m", "110m"):
+        w = synth.workload(name)
+        cfg = synth.model_config(w)
+        prompt = synth.prompt(w)
+        steps, n_fwd = w["steps"], forwards_of(w)
+        blob = synth.make_blob(cfg, w["seed"])
+        with l2.Decoder(cfg, blob) as dec:
+            del blob
+            stream = torch.cuda.Stream()
+            d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
+            d_out = torch.zeros(steps, dtype=torch.int32, device="cuda")
+
+            def step():
+                l2.l2_generate_device(dec.h, d_prompt, len(prompt), steps, d_out, stream)
+
+            for _ in range(args.warmup):
+                step()
+            stream.synchronize()
+            ms_max, clocks, _ = timed_steps(step, stream, args.steps, world, local)
+        step_bytes = sum(workload_bytes_per_forward(cfg, p) for p in range(n_fwd))
+        tok_s = world * args.steps * n_fwd / (ms_max / 1e3)
+        gbs = step_bytes * args.steps / (ms_max / 1e3) / 1e9
+        out[name] = {"value": tok_s, "unit": "tok/s", "ms_per_step": ms_max / args.steps,
+                     "forwards_per_step": n_fwd, "us_per_forward": ms_max * 1e3 / args.steps / n_fwd,
+                     "step_roofline": {"achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                       "frac": gbs / hbm,
+                                       "bytes_per_forward": step_bytes / n_fwd,
+                                       "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"},
+                     "kernels_per_forward": 5 * cfg["n_layers"] + 1,
+                     "clocks": clocks}
+    return out
 
 
 BATCHED_KINDS = {  # batched kernel kinds of l2_time_kernel and their launches per step
@@ -672,7 +794,7 @@ def run_ours_batched(args, world, rank, local, compact=False):
     # per-kernel times at the run's mean position, live, on the bench stream
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
-    p3 = tf32x3_peak(peaks)
+    p3, p3_source = tf32x3_peak(peaks)
     pos_mid = int(np.mean(lens)) - 1 + steps // 2
     per = {}
     for kind, name in BATCHED_KINDS.items():
@@ -697,13 +819,14 @@ def run_ours_batched(args, world, rank, local, compact=False):
                     "traffic": profiled_battn_traffic(dk["bytes"]) if dom == 7 else None}
     roofline.update({"kernel": dk["name"], "launch_ms": dk["launch_ms"],
                      "share_of_kernel_time": dk["ms_per_step"] / total_ms,
-                     "peak_source": (f"{peak_kind} bf16_tflops x 1.1/2.25 / 3 (3xTF32)"
-                                     if dk["flops"] > 0 else f"{peak_kind} hbm_gbs (copy)")})
+                     "peak_source": (p3_source if dk["flops"] > 0
+                                     else f"{peak_kind} hbm_gbs (copy)")})
     g_flops = sum(v["flops"] * v["launches_per_step"] for v in per.values())
     g_ms = sum(v["ms_per_step"] for v in per.values() if v["flops"] > 0)
     gemm_phase = {"achieved": g_flops / (g_ms / 1e3) / 1e12, "peak": p3, "unit": "TFLOP/s",
                   "frac": g_flops / (g_ms / 1e3) / 1e12 / p3, "flops_per_step": g_flops,
-                  "ms_per_step": g_ms}
+                  "ms_per_step": g_ms, "peak_source": p3_source,
+                  "measured_fp32_gemm_peaks": measured_fp32_peaks()}
     attn = per[7]
     attn_roof = {"achieved": attn["bytes"] / (attn["launch_ms"] / 1e3) / 1e9, "peak": hbm,
                  "unit": "GB/s", "frac": attn["bytes"] / (attn["launch_ms"] / 1e3) / 1e9 / hbm,
