@@ -51,6 +51,7 @@ struct l2_handle {
     // activation rows, per-sequence state and the GEMM operand maps
     int mcap = 0;
     int rows = 0;                      // max(max_batch, max_prefill): row buffers of the GEMM path
+    int a_rows = 128;                  // rows of the GEMMs' A tiles: 64 when rows <= 64
     float* bw = nullptr;
     float *qkv_hi = nullptr, *qkv_lo = nullptr, *wo_hi = nullptr, *wo_lo = nullptr;
     float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
@@ -319,8 +320,11 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
     g.M = M;
     g.err = &h->st->err;
     g.layer = l;
+    g.a_rows = h->a_rows;
     // tile width fixed at create (it is the weight maps' box); K split for this M
-    auto plan = [&](const GemmPlan& p, int N, int K) { return plan_split(h->gocc, p.bn, M, N, K); };
+    auto plan = [&](const GemmPlan& p, int N, int K) {
+        return plan_split(h->gocc, p.bn, M, N, K, h->a_rows);
+    };
     switch (kind) {
         case BK_EMB: {
             BNormArgs n{};
@@ -621,26 +625,30 @@ int setup_batched(l2_handle* h) {
     h->b_rmap = h->bst + o_rmap;
 
     const int Mb = static_cast<int>(RW);
-    h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d));
+    // at most 64 rows per GEMM (a prefill-only handle): 64-row A tiles, so the
+    // shared-memory ring holds more weight bytes and the A operand is read once
+    h->a_rows = RW <= 64 ? 64 : 128;
+    const int ar = h->a_rows;
+    h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d), 256, ar);
     // Wo and W2 write the per-row sums of squares of the next norm: tiles <= 128
-    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d), 128);
-    h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d));
-    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128);
-    h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d));
+    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d), 128, ar);
+    h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d), 256, ar);
+    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128, ar);
+    h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d), 256, ar);
     const long long D = d, FF = F, LL = L, MC = Mc;
     struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
     const MapSpec specs[] = {
-        {&h->m_qkv.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_qkv.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_qkv.a_hi, h->xn_hi, D, MC, 1, ar}, {&h->m_qkv.a_lo, h->xn_lo, D, MC, 1, ar},
         {&h->m_qkv.b_hi, h->qkv_hi, D, D + 2 * static_cast<long long>(kvd), LL, h->gp_qkv.bn},
         {&h->m_qkv.b_lo, h->qkv_lo, D, D + 2 * static_cast<long long>(kvd), LL, h->gp_qkv.bn},
-        {&h->m_wo.a_hi, h->att_hi, D, MC, 1, 128}, {&h->m_wo.a_lo, h->att_lo, D, MC, 1, 128},
+        {&h->m_wo.a_hi, h->att_hi, D, MC, 1, ar}, {&h->m_wo.a_lo, h->att_lo, D, MC, 1, ar},
         {&h->m_wo.b_hi, h->wo_hi, D, D, LL, h->gp_wo.bn}, {&h->m_wo.b_lo, h->wo_lo, D, D, LL, h->gp_wo.bn},
-        {&h->m_w13.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_w13.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_w13.a_hi, h->xn_hi, D, MC, 1, ar}, {&h->m_w13.a_lo, h->xn_lo, D, MC, 1, ar},
         {&h->m_w13.b_hi, h->w13_hi, D, 2 * FF, LL, h->gp_w13.bn},
         {&h->m_w13.b_lo, h->w13_lo, D, 2 * FF, LL, h->gp_w13.bn},
-        {&h->m_w2.a_hi, h->hb_hi, FF, MC, 1, 128}, {&h->m_w2.a_lo, h->hb_lo, FF, MC, 1, 128},
+        {&h->m_w2.a_hi, h->hb_hi, FF, MC, 1, ar}, {&h->m_w2.a_lo, h->hb_lo, FF, MC, 1, ar},
         {&h->m_w2.b_hi, h->w2_hi, FF, D, LL, h->gp_w2.bn}, {&h->m_w2.b_lo, h->w2_lo, FF, D, LL, h->gp_w2.bn},
-        {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, 128}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, 128},
+        {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, ar}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, ar},
         {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->gp_cls.bn},
         {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->gp_cls.bn},
     };

@@ -139,6 +139,11 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int STAGES = (BN >= 256) ? 2 : (BN == 128) ? 3 : 4;  // deepest ring that fits
+    static constexpr int MAX_STAGES = 6;  // with 64-row A tiles
+    // bytes of one ring slot when the A tiles hold a_rows rows (Ahi, Alo, Bhi, Blo)
+    __host__ __device__ static constexpr int stage_bytes(int a_rows) {
+        return 2 * a_rows * BK * 4 + 2 * B_BYTES;
+    }
     // TMEM columns: one accumulator, or two when chunks are drained
     __host__ __device__ static constexpr uint32_t tmem_cols(bool drain) {
         return drain ? 2 * BN : BN;
@@ -152,10 +157,13 @@ struct Cfg {
     // dynamic shared memory of a launch: alignment slack, a ring of `stages`
     // slots (>= 2: the staged partial tile reuses the first two), the receive
     // buffer of a split launch, barriers
-    __host__ __device__ static constexpr size_t smem_for(int stages, int ksplit) {
-        return 1024 + static_cast<size_t>(stages) * STAGE + recv_bytes(ksplit) + 256;
+    __host__ __device__ static constexpr size_t smem_for(int stages, int ksplit, int a_rows = 128) {
+        return 1024 + static_cast<size_t>(stages) * stage_bytes(a_rows) + recv_bytes(ksplit) + 256;
     }
     static_assert(128 * PS * 4 <= 2 * STAGE, "partial tile must fit in two slots");
+    static_assert(128 * PS * 4 <= 2 * (2 * 64 * BK * 4 + 2 * B_BYTES),
+                  "partial tile must fit in two slots of 64-row A tiles");
+    static_assert((64 * BK * 4) % 1024 == 0, "64-row A tiles keep 1024-byte alignment");
     static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
 };
@@ -416,15 +424,20 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                        const __grid_constant__ CUtensorMap mB_hi,
                        const __grid_constant__ CUtensorMap mB_lo, const GemmArgs g) {
     using C = Cfg<BN>;
-    const int S = g.stages;       // ring depth of this launch (2..C::STAGES)
+    const int S = g.stages;       // ring depth of this launch
     constexpr int PS = C::PS;     // row stride of the staged partial (floats)
+    // A tiles of g.a_rows rows (128, or 64: the MMA then reads rows 64-127 of
+    // each A operand from the slot after it, garbage that only reaches output
+    // rows at or beyond m_end, which are never written)
+    const int a_bytes = (g.a_rows == 64 ? 64 : 128) * C::BK * 4;
+    const int stage_b = 2 * a_bytes + 2 * C::B_BYTES;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* gbase = smem_raw + (base - raw);
     const int nsplit = gridDim.x, split = blockIdx.x;
-    const uint32_t recv_base = base + static_cast<uint32_t>(S * C::STAGE);
-    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * C::STAGE +
+    const uint32_t recv_base = base + static_cast<uint32_t>(S * stage_b);
+    uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * stage_b +
                                                  C::recv_bytes(nsplit));
     uint64_t* empty = full + S;
     uint64_t* accfull = empty + S;   // [2] chunk accumulated in TMEM buffer b
@@ -478,9 +491,9 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     // collect the peers' announcements only before pushing to them
     if (nsplit > 1) cluster_arrive_release();
 
-    auto a_hi = [&](int s) { return base + static_cast<uint32_t>(s * C::STAGE); };
-    auto a_lo = [&](int s) { return a_hi(s) + C::A_BYTES; };
-    auto b_hi = [&](int s) { return a_hi(s) + 2 * C::A_BYTES; };
+    auto a_hi = [&](int s) { return base + static_cast<uint32_t>(s * stage_b); };
+    auto a_lo = [&](int s) { return a_hi(s) + static_cast<uint32_t>(a_bytes); };
+    auto b_hi = [&](int s) { return a_hi(s) + static_cast<uint32_t>(2 * a_bytes); };
     auto b_lo = [&](int s) { return b_hi(s) + C::B_BYTES; };
 
     float R[DRAIN ? BN : 1];  // DRAIN, warps 0-3: this thread's row, summed over chunks
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             const int pre = NK < S ? NK : S;
             for (int i = 0; i < pre; ++i) {
                 const int kc = (kb0 + i) * 32;
-                mbar_arrive_expect_tx(&full[i], C::STAGE);
+                mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(stage_b));
                 tma_load_3d(b_hi(i), &mB_hi, kc, n0, g.layer, &full[i]);
                 tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
             }
@@ -511,7 +524,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                     s_err = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], C::STAGE);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_b));
                 tma_load_3d(b_hi(s), &mB_hi, kc, n0, g.layer, &full[s]);
                 tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
                 tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
@@ -732,7 +745,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             const int gpr = BN / 4;  // float4 groups per row
             const int ngroups = (r1 - r0) * gpr;
             const float* recv =
-                reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * C::STAGE);
+                reinterpret_cast<const float*>(gbase + static_cast<size_t>(S) * stage_b);
             // Each thread takes its groups kU at a time: group t is row r0 + t / gpr,
             // columns 4 (t % gpr) .. + 3 of the tile. The global operands of a batch
             // are requested first (for the first batch, while the slices travel),
@@ -885,7 +898,7 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(ksplit, mt * nt);
     cfg.blockDim = dim3(gemm_threads(DRAIN));
-    cfg.dynamicSmemBytes = C::smem_for(g.stages, ksplit);
+    cfg.dynamicSmemBytes = C::smem_for(g.stages, ksplit, g.a_rows == 64 ? 64 : 128);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -980,19 +993,25 @@ cudaError_t make_gemm_map(CUtensorMap* map, const float* base, long long inner, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Deepest ring of a tile width: 2-4 slots with 128-row A tiles; with 64-row A
+// tiles the smaller slots allow up to Cfg::MAX_STAGES.
+template <int BN>
+int ring_limit(int a_rows) { return a_rows == 64 ? Cfg<BN>::MAX_STAGES : Cfg<BN>::STAGES; }
+
 // Whether a ring of `stages` slots (and the receive buffer of a split launch)
 // fits in one CTA's shared memory.
 template <int BN>
-bool fits(int stages, int ksplit) {
-    return stages <= Cfg<BN>::STAGES && Cfg<BN>::smem_for(stages, ksplit) <= kMaxDynSmem;
+bool fits(int stages, int ksplit, int a_rows) {
+    return stages <= ring_limit<BN>(a_rows) &&
+           Cfg<BN>::smem_for(stages, ksplit, a_rows) <= kMaxDynSmem;
 }
 
 template <int BN>
-int active_clusters(int ksplit, int stages) {
+int active_clusters(int ksplit, int stages, int a_rows) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ksplit, 1024);
     cfg.blockDim = dim3(gemm_threads(has_drain<BN>()));
-    cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages, ksplit);
+    cfg.dynamicSmemBytes = Cfg<BN>::smem_for(stages, ksplit, a_rows);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ksplit;
@@ -1022,73 +1041,122 @@ cudaError_t prepare_gemm(GemmOccupancy* occ) {
     if ((e = cudaDeviceGetAttribute(&occ->num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
         cudaSuccess)
         return e;
-    for (int sp = 1; sp <= 8; ++sp)
-        for (int st = 2; st <= 4; ++st) {
-            occ->clusters[0][sp][st] = fits<64>(st, sp) ? active_clusters<64>(sp, st) : 0;
-            occ->clusters[1][sp][st] = fits<128>(st, sp) ? active_clusters<128>(sp, st) : 0;
-            occ->clusters[2][sp][st] = fits<256>(st, sp) ? active_clusters<256>(sp, st) : 0;
-        }
+    for (int ar = 0; ar < 2; ++ar) {
+        const int a_rows = ar == 0 ? 128 : 64;
+        for (int sp = 1; sp <= 8; ++sp)
+            for (int st = 2; st <= 6; ++st) {
+                occ->clusters[ar][0][sp][st] = fits<64>(st, sp, a_rows) ? active_clusters<64>(sp, st, a_rows) : 0;
+                occ->clusters[ar][1][sp][st] = fits<128>(st, sp, a_rows) ? active_clusters<128>(sp, st, a_rows) : 0;
+                occ->clusters[ar][2][sp][st] = fits<256>(st, sp, a_rows) ? active_clusters<256>(sp, st, a_rows) : 0;
+            }
+    }
     return cudaSuccess;
 }
 
-// K split and ring depth for a tile width: the largest split S <= 8 that keeps
-// at least two K-blocks per CTA and runs every cluster in one wave; the ring
-// holds one CTA's K-blocks, at least 2 and at most what fits. (Measured on the
-// batched decode GEMMs: two co-resident CTAs per SM with 2-slot rings are no
-// faster than one CTA per SM with a deeper ring.)
 // The ring depth, whether a ring fits, and the occupancy table row of a tile width.
-int max_stages(int bn) {
-    return bn == 256 ? Cfg<256>::STAGES : bn == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
+int max_stages(int bn, int a_rows) {
+    return bn == 256 ? ring_limit<256>(a_rows) : bn == 128 ? ring_limit<128>(a_rows)
+                                                           : ring_limit<64>(a_rows);
 }
-bool fits_bn(int bn, int stages, int ksplit) {
-    return bn == 256 ? fits<256>(stages, ksplit)
-           : bn == 128 ? fits<128>(stages, ksplit)
-                       : fits<64>(stages, ksplit);
+bool fits_bn(int bn, int stages, int ksplit, int a_rows) {
+    return bn == 256 ? fits<256>(stages, ksplit, a_rows)
+           : bn == 128 ? fits<128>(stages, ksplit, a_rows)
+                       : fits<64>(stages, ksplit, a_rows);
 }
 int bn_row(int bn) { return bn == 256 ? 2 : bn == 128 ? 1 : 0; }
+int stage_bytes_bn(int bn, int a_rows) { return 2 * a_rows * 32 * 4 + 2 * bn * 32 * 4; }
+
+// Estimated time of a plan, in bytes one CTA streams: every wave of
+// co-resident clusters takes the per-CTA K range times a slot's bytes, plus
+// the split-K exchange (about three slots' worth); waves are counted whole.
+// Used for GEMMs of at most 64 rows, whose long K ranges make the kernel a
+// weight stream: a plan that leaves SMs idle in a partial last wave, or one
+// wave on two thirds of the SMs, loses to a deeper split in balanced waves.
+long long plan_cost(const GemmOccupancy& occ, int bn, int sp, int st, int tiles, int KB,
+                    int a_rows) {
+    const int cl = occ.clusters[a_rows == 64 ? 1 : 0][bn_row(bn)][sp][st];
+    if (cl < 1) return -1;
+    const long long waves = (tiles + cl - 1) / cl;
+    const long long kb = (KB + sp - 1) / sp;
+    const long long slot = stage_bytes_bn(bn, a_rows);
+    return waves * (kb * slot + (sp > 1 ? 3 * slot : 0));
+}
 
 // ksplit == 0 in the result: no plan with this tile width (a 256-wide tile
 // needs a split that leaves each CTA at most kDrainAbove K-blocks and fits).
-GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K) {
+//
+// 128-row A tiles (decode rows): the largest split S <= 8 that keeps at
+// least two K-blocks per CTA and runs every cluster in one wave; the ring
+// holds one CTA's K-blocks, at least 2 and at most what fits. (Measured on
+// the batched decode GEMMs: two co-resident CTAs per SM with 2-slot rings are
+// no faster than one CTA per SM with a deeper ring.)
+// 64-row A tiles (prefill passes of at most 64 rows): the split of least
+// plan_cost, the ring as deep as fits.
+GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K, int a_rows) {
     const int KB = (K + 31) / 32, mt = (M + 127) / 128;
     const int tiles = mt * ((N + bn - 1) / bn);
-    const int max_st = max_stages(bn);
+    const int max_st = max_stages(bn, a_rows);
     const bool drainable = bn <= 128;
     auto depth = [&](int sp) {
         const int per = (KB + sp - 1) / sp;
         int st = per < 2 ? 2 : per > max_st ? max_st : per;
-        while (st > 2 && !fits_bn(bn, st, sp)) --st;
+        while (st > 2 && !fits_bn(bn, st, sp, a_rows)) --st;
         return st;
     };
     auto ok = [&](int sp) { return drainable || (KB + sp - 1) / sp <= kDrainAbove; };
+    if (a_rows == 64) {
+        GemmPlan best{bn, 0, 2};
+        long long best_cost = -1;
+        for (int sp = 1; sp <= 8; ++sp) {
+            if ((sp > 1 && KB / sp < 2) || !ok(sp)) continue;
+            const int st = depth(sp);
+            if (!fits_bn(bn, st, sp, a_rows)) continue;
+            const long long c = plan_cost(occ, bn, sp, st, tiles, KB, a_rows);
+            if (c >= 0 && (best_cost < 0 || c < best_cost)) {
+                best_cost = c;
+                best = GemmPlan{bn, sp, st};
+            }
+        }
+        return best;
+    }
     for (int sp = 8; sp > 1; --sp) {
         if (KB / sp < 2 || !ok(sp)) continue;
         const int st = depth(sp);
-        if (fits_bn(bn, st, sp) && tiles <= occ.clusters[bn_row(bn)][sp][st])
+        if (fits_bn(bn, st, sp, a_rows) && tiles <= occ.clusters[0][bn_row(bn)][sp][st])
             return GemmPlan{bn, sp, st};
     }
-    if (!ok(1) || !fits_bn(bn, depth(1), 1)) return GemmPlan{bn, 0, 2};
+    if (!ok(1) || !fits_bn(bn, depth(1), 1, a_rows)) return GemmPlan{bn, 0, 2};
     return GemmPlan{bn, 1, depth(1)};
 }
 
-// Tile width and split of an M x N x K GEMM: the plan that keeps more SMs
-// busy in its first wave wins, ties going to the wider tile (fewer
-// activation re-reads, and fewer waves when the tiles outnumber the SMs: the
-// 256 x 32000 classifier runs 250 tiles of 256 columns in two rounds instead
-// of 500 of 128 in four). max_bn caps the width (a GEMM whose epilogue
-// produces per-row sums of squares needs a tile row within one warp: 128).
-GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn) {
+// Tile width and split of an M x N x K GEMM. 128-row A tiles: the plan that
+// keeps more SMs busy in its first wave wins, ties going to the wider tile
+// (fewer activation re-reads, and fewer waves when the tiles outnumber the
+// SMs: the 256 x 32000 classifier runs 250 tiles of 256 columns in two rounds
+// instead of 500 of 128 in four). 64-row A tiles: the plan of least
+// plan_cost. max_bn caps the width (a GEMM whose epilogue produces per-row
+// sums of squares needs a tile row within one warp: 128).
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn, int a_rows) {
     GemmPlan best{64, 1, Cfg<64>::STAGES};
-    long long best_ctas = -1;
-    const int mt = (M + 127) / 128;
+    long long best_score = -1;
+    const int mt = (M + 127) / 128, KB = (K + 31) / 32;
     for (int bn : {256, 128, 64}) {
         if (bn > max_bn || (bn > 64 && bn > N)) continue;  // a tile wider than N is waste
-        const GemmPlan p = plan_split(occ, bn, M, N, K);
+        const GemmPlan p = plan_split(occ, bn, M, N, K, a_rows);
         if (p.ksplit < 1) continue;
-        long long ctas = static_cast<long long>(mt) * ((N + bn - 1) / bn) * p.ksplit;
+        const int tiles = mt * ((N + bn - 1) / bn);
+        if (a_rows == 64) {
+            const long long c = plan_cost(occ, bn, p.ksplit, p.stages, tiles, KB, a_rows);
+            if (c >= 0 && (best_score < 0 || c < best_score)) {
+                best_score = c;
+                best = p;
+            }
+            continue;
+        }
+        long long ctas = static_cast<long long>(tiles) * p.ksplit;
         if (ctas > occ.num_sms) ctas = occ.num_sms;
-        if (ctas > best_ctas) {
-            best_ctas = ctas;
+        if (ctas > best_score) {
+            best_score = ctas;
             best = p;
         }
     }
@@ -1097,7 +1165,9 @@ GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn) {
 
 cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g0,
                         cudaStream_t s, bool pdl) {
-    const int max_st = max_stages(p.bn);
+    const int a_rows = g0.a_rows == 64 ? 64 : 128;
+    if (a_rows == 64 && g0.M > 64) return cudaErrorInvalidValue;  // one 64-row A tile per launch
+    const int max_st = max_stages(p.bn, a_rows);
     if (g0.M < 1 || g0.N < 1 || g0.K < 4 || g0.K % 4 != 0 || p.ksplit < 1 || p.ksplit > 8 ||
         p.stages < 2 || p.stages > max_st)
         return cudaErrorInvalidValue;
@@ -1108,6 +1178,7 @@ cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const Gem
         return cudaErrorInvalidValue;
     GemmArgs g = g0;
     g.stages = p.stages;
+    g.a_rows = a_rows;
     if (p.bn == 256) return launch_bn<256>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 128) return launch_bn<128>(epi, m, g, p.ksplit, s, pdl);
     if (p.bn == 64) return launch_bn<64>(epi, m, g, p.ksplit, s, pdl);

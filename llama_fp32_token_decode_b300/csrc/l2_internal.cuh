@@ -139,6 +139,9 @@ struct GemmArgs {
     unsigned long long* argmax_keys;  // ARGMAX: [M]
     int* err;             // ERR_* bits
     int stages;           // ring depth (set by launch_gemm from the plan)
+    int a_rows;           // rows of an A tile the maps load: 128, or 64 when at most
+                          // 64 rows are ever multiplied (the MMA still spans 128 rows;
+                          // rows 64-127 read the next operand slot and are discarded)
     // RMSNorm folded into the GEMM that consumes the normalised rows. The
     // weights carry the norm gain (W[n][k] * g[k]) and A holds the raw rows x
     // (tf32 pair), so the consumer scales row r of its result by
@@ -387,12 +390,13 @@ struct GemmPlan {
 // Clusters of each (tile width, split, ring depth) that the device runs at
 // once, measured with cudaOccupancyMaxActiveClusters at set-up.
 struct GemmOccupancy {
-    int clusters[3][9][5];  // [tile width 64 / 128 / 256][ksplit][stages]
+    int clusters[2][3][9][7];  // [A tile 128 / 64 rows][tile width 64 / 128 / 256][ksplit][stages]
     int num_sms;
 };
 cudaError_t prepare_gemm(GemmOccupancy* occ);
-GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn = 256);
-GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K);
+GemmPlan plan_gemm(const GemmOccupancy& occ, int M, int N, int K, int max_bn = 256,
+                   int a_rows = 128);
+GemmPlan plan_split(const GemmOccupancy& occ, int bn, int M, int N, int K, int a_rows = 128);
 cudaError_t launch_gemm(int epi, const GemmPlan& p, const GemmMaps& m, const GemmArgs& g,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s);
