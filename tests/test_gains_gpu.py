@@ -82,3 +82,33 @@ def test_gain_segments_reach_the_oracle():
     ma.close()
     mb.close()
     assert rel_l2(b, a) > 1e-2
+
+
+@pytest.mark.gpu
+def test_nonunit_gains_prefill_long_k(l2):
+    # A prefill-only handle (at most 64 rows: 64-row A tiles, wave-balanced K
+    # splits) with K ranges long enough that its GEMM CTAs drain accumulation
+    # chunks, and RMSNorm gains other than 1 folded into the GEMM weights.
+    # Every position against the oracle, in one pass and in two.
+    cfg = config(dim=2048, hidden_dim=5632, n_layers=2, n_heads=16, n_kv_heads=4,
+                 vocab_size=1000, seq_len=48, max_prefill=40)
+    blob = _blob_with_gains(cfg, 37)
+    toks = synth.prompt_ids(37, 40, cfg["vocab_size"])
+    m = oracle.Model(cfg, blob)
+    refs = [m.forward(int(t), p) for p, t in enumerate(toks)]
+    m.close()
+    with l2.Decoder(cfg, blob) as dec:
+        pre = dec.prefill(toks)
+        worst = 0.0
+        for p in range(len(toks)):
+            e = rel_l2(pre[p], refs[p])
+            worst = max(worst, e)
+            assert e <= REL_L2_TOL, f"prefill pos {p}: rel-L2 {e:.3e}"
+        # and the second half again, after the first half is in the cache
+        dec.reset()
+        dec.prefill(toks[:20])
+        pre2 = dec.prefill(toks[20:], pos0=20)
+        for p in range(20, len(toks)):
+            e = rel_l2(pre2[p - 20], refs[p])
+            assert e <= REL_L2_TOL, f"second pass pos {p}: rel-L2 {e:.3e}"
+    print(f"long-K prefill with gains: worst rel-L2 {worst:.3e}")
