@@ -69,7 +69,18 @@ extern "C" {
  * the last seq_len positions (a rolling cache; the openai.wiki page lists
  * decoding beyond max_seq_len as a to-do that has to handle the KV cache,
  * "未排序的待办事项"); RoPE keeps the absolute position. Prompts (and the
- * prefill pass) stay below seq_len. */
+ * prefill pass) stay below seq_len.
+ * layer_kernels: how a batch-1 forward is split into kernels (the same
+ * arithmetic either way, up to summation order). 5: QKV + RoPE + KV append,
+ * attention, Wo + residual, W1/W3 + SwiGLU, W2 + residual, each streaming its
+ * weights over every SM (for models whose layers are large). 2: an attention
+ * block (one cluster of 8 CTAs per query head: its Q/K/V rows, attention and
+ * its share of Wo) and an FFN block (W1/W3, SwiGLU and W2 per hidden-unit
+ * slice), with the residual kept in 64-bit fixed point so that the CTAs' sums
+ * are exact and independent of their order (for models whose per-kernel work
+ * is too small to hide a kernel boundary; needs head_dim a multiple of 4 and at
+ * most 128, 3 * head_dim a multiple of 16, and each CTA's weight slice within
+ * shared memory). 0: 2 for models under 2 GB of weights where it fits, else 5. */
 typedef struct {
     int32_t dim;               /* d, width of the residual stream            */
     int32_t hidden_dim;        /* F, SwiGLU hidden width                     */
@@ -84,6 +95,8 @@ typedef struct {
     int32_t shared_classifier; /* 1: classifier = embedding table (no Wcls)  */
     int32_t max_prefill;       /* prompt positions one prefill pass takes    */
     int32_t rolling_positions; /* > seq_len: decode up to this many positions */
+    int32_t layer_kernels;     /* batch-1 kernels per layer: 0 = chosen at create,
+                                  5 or 2 (see below)                           */
 } l2_config;
 
 typedef struct l2_handle l2_handle;

@@ -49,7 +49,7 @@ class L2Config(ctypes.Structure):
                 ("seq_len", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("norm_eps", ctypes.c_float), ("max_batch", ctypes.c_int32),
                 ("shared_classifier", ctypes.c_int32), ("max_prefill", ctypes.c_int32),
-                ("rolling_positions", ctypes.c_int32)]
+                ("rolling_positions", ctypes.c_int32), ("layer_kernels", ctypes.c_int32)]
 
 
 class L2Error(RuntimeError):
@@ -111,7 +111,8 @@ def make_config(cfg: dict) -> L2Config:
                     cfg.get("n_kv_heads") or cfg["n_heads"], cfg["vocab_size"], cfg["seq_len"],
                     cfg.get("rope_theta", 10000.0), cfg.get("norm_eps", 1e-5),
                     cfg.get("max_batch", 1), cfg.get("shared_classifier", 0),
-                    cfg.get("max_prefill", 0), cfg.get("rolling_positions", 0))
+                    cfg.get("max_prefill", 0), cfg.get("rolling_positions", 0),
+                    cfg.get("layer_kernels", 0))
 
 
 def _check(rc: int, h=None):

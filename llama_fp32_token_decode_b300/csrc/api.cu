@@ -47,6 +47,15 @@ struct l2_handle {
     int nsplit = 1;
     uint64_t policy = 0;
 
+    // two kernels per layer (fused_small.cu): Wo per head, W2 transposed, and
+    // the fixed-point residual buffers P[2], M[2] of d entries each
+    bool fused = false;
+    FAttnArgs fattn{};
+    FFfnArgs fffn{};
+    int ffn_grid = 0;
+    float* fw = nullptr;               // wo_h [L][H][d][hd], then w2t [L][F][d]
+    long long* fx = nullptr;           // P0, P1, M0, M1
+
     // batched path (max_batch > 1): weights as tf32 (hi, lo) pairs, [Mcap][...]
     // activation rows, per-sequence state and the GEMM operand maps
     int mcap = 0;
@@ -142,6 +151,8 @@ bool config_valid(const l2_config* c, std::string* why) {
         return bad("0 <= rolling_positions <= 2^24");
     if (!(c->norm_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("norm_eps >= 0 and rope_theta > 0");
     if (c->shared_classifier != 0 && c->shared_classifier != 1) return bad("shared_classifier is 0 or 1");
+    if (c->layer_kernels != 0 && c->layer_kernels != 2 && c->layer_kernels != 5)
+        return bad("layer_kernels is 0, 2 or 5");
     return true;
 }
 
@@ -244,7 +255,51 @@ cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
     }
 }
 
+// Two kernels per layer: the attention block and the FFN block, the residual
+// in fixed point (P[l % 2] enters layer l, M[l % 2] after its attention).
+cudaError_t enqueue_forward_fused(l2_handle* h, cudaStream_t s) {
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, kvd = h->kvd, L = c.n_layers;
+    long long* P[2] = {h->fx, h->fx + d};
+    long long* M[2] = {h->fx + 2 * d, h->fx + 3 * d};
+    const float* wo_h = h->fw;
+    const float* w2t = h->fw + L * d * d;
+    for (size_t l = 0; l < L; ++l) {
+        FAttnArgs a = h->fattn;
+        a.wqkv = h->wqkv + l * (d + 2 * kvd) * d;
+        a.wo_h = wo_h + l * d * d;
+        a.g_att = h->g_att + l * d;
+        a.x_in = l == 0 ? nullptr : P[l % 2];
+        a.x_mid = M[l % 2];
+        a.x_zero = P[(l + 1) % 2];
+        a.k_cache = h->k_cache + l * h->cache_layer;
+        a.v_cache = h->v_cache + l * h->cache_layer;
+        cudaError_t e = launch_fattn(a, s, true);
+        if (e != cudaSuccess) return e;
+        FFfnArgs f = h->fffn;
+        f.w13 = h->w13 + l * 2 * F * d;
+        f.w2t = w2t + l * F * d;
+        f.g_ffn = h->g_ffn + l * d;
+        f.x_mid = M[l % 2];
+        f.x_out = P[(l + 1) % 2];
+        f.x_zero = M[(l + 1) % 2];
+        if ((e = launch_fffn(f, h->ffn_grid, s, true)) != cudaSuccess) return e;
+    }
+    // classifier on the last residual; it also clears the next forward's M[0]
+    MatvecArgs a = base_args(h);
+    a.W = h->wcls;
+    a.plan = h->p_cls;
+    a.src = h->x;
+    a.src_fixed = P[L % 2];
+    a.gain = h->g_final;
+    a.out = h->logits;
+    a.zero_fixed = M[0];
+    a.zero_n = static_cast<int>(d);
+    return launch_matvec(EPI_CLASSIFIER, a, s, true);
+}
+
 cudaError_t enqueue_forward(l2_handle* h, cudaStream_t s) {
+    if (h->fused) return enqueue_forward_fused(h, s);
     for (int l = 0; l < h->cfg.n_layers; ++l)
         for (int k = 0; k < 5; ++k) {
             cudaError_t e = launch_kind(h, k, l, s);
@@ -705,6 +760,10 @@ int upload(l2_handle* h, const float* blob, cudaMemcpyKind kind) {
 }
 
 void free_all(l2_handle* h) {
+    cudaFree(h->fw);
+    cudaFree(h->fx);
+    h->fw = nullptr;
+    h->fx = nullptr;
     if (h->fwd1) cudaGraphExecDestroy(h->fwd1);
     if (h->fwdN) cudaGraphExecDestroy(h->fwdN);
     if (h->fwd1s) cudaGraphExecDestroy(h->fwd1s);
@@ -729,6 +788,53 @@ void free_all(l2_handle* h) {
     h->ev0 = h->ev1 = nullptr;
     h->stream = nullptr;
     h->weights = h->kv = h->act = nullptr;
+}
+
+// Decides between five and two kernels per layer for the batch-1 forward and,
+// for two, lays out Wo per head and W2 transposed and allocates the
+// fixed-point residual buffers.
+int setup_fused(l2_handle* h) {
+    const l2_config& c = h->cfg;
+    const size_t d = c.dim, F = c.hidden_dim, L = c.n_layers;
+    if (c.layer_kernels == 5) return L2_OK;
+    FAttnArgs& a = h->fattn;
+    FFfnArgs& f = h->fffn;
+    a.emb = h->emb;
+    a.rope = h->rope;
+    a.st = h->st;
+    a.d = c.dim;
+    a.kvd = h->kvd;
+    a.hd = h->hd;
+    a.H = c.n_heads;
+    a.KVH = c.n_kv_heads;
+    a.S = c.seq_len;
+    a.vocab = c.vocab_size;
+    a.eps = c.norm_eps;
+    a.l2_policy = h->policy;
+    f.err = &h->st->err;
+    f.d = c.dim;
+    f.F = c.hidden_dim;
+    f.eps = c.norm_eps;
+    f.l2_policy = h->policy;
+    int optin = 0;
+    L2_CUDA(h, cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev));
+    const bool fits = plan_fused(a, f, h->num_sms, static_cast<size_t>(optin), &h->ffn_grid);
+    if (c.layer_kernels == 2 && !fits)
+        return fail(h, L2_EINVAL, "layer_kernels 2: the shape does not fit the two-kernel layer");
+    if (c.layer_kernels == 0 &&
+        (!fits || static_cast<double>(h->weight_floats) * 4.0 >= 2e9))
+        return L2_OK;
+    L2_CUDA(h, cudaMalloc(&h->fw, (L * d * d + L * F * d) * sizeof(float)));
+    L2_CUDA(h, cudaMalloc(&h->fx, 4 * d * sizeof(long long)));
+    L2_CUDA(h, cudaMemsetAsync(h->fx, 0, 4 * d * sizeof(long long), h->stream));
+    L2_CUDA(h, launch_retile_heads(h->fw, h->wo, static_cast<int>(L), static_cast<int>(d), h->hd,
+                                   h->stream));
+    L2_CUDA(h, launch_transpose_layers(h->fw + L * d * d, h->w2, static_cast<int>(L),
+                                       static_cast<int>(d), static_cast<int>(F), h->stream));
+    L2_CUDA(h, prepare_fused(a, f));
+    L2_CUDA(h, cudaStreamSynchronize(h->stream));
+    h->fused = true;
+    return L2_OK;
 }
 
 // Batched forward of M rows whose tokens and positions are already in
@@ -959,6 +1065,7 @@ static int create_impl(const l2_config* cfg, const float* blob, size_t blob_floa
     if (rc != L2_OK) return bail(rc);
     h->rows = c.max_batch > c.max_prefill ? c.max_batch : c.max_prefill;
     if (h->rows > 1 && (rc = setup_batched(h)) != L2_OK) return bail(rc);
+    if ((rc = setup_fused(h)) != L2_OK) return bail(rc);
 
     if ((rc = capture(h, 1, &h->fwd1)) != L2_OK) return bail(rc);
     if ((rc = capture(h, kGraphBatch, &h->fwdN)) != L2_OK) return bail(rc);

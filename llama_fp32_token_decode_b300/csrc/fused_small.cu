@@ -1,0 +1,552 @@
+// fused_small.cu -- the batch-1 forward of a small model in two kernels per
+// layer instead of five.
+//
+// The step is the same fp32 Llama-2 decode step as matvec.cu + attention.cu
+// compute (the llama2.c pages' single-file engine: per layer RMSNorm, Q/K/V,
+// RoPE, KV append, causal attention, Wo + residual, RMSNorm, SwiGLU FFN +
+// residual). For models whose layers are a few MB, each of those kernels is
+// a few microseconds of dependency latency, not bandwidth, so this path cuts
+// the number of kernel boundaries per layer from five to two:
+//
+//   attention block  grid (8, H), one thread-block cluster of 8 CTAs per query
+//                    head h. CTA j computes rows [j*3hd/8, (j+1)*3hd/8) of the
+//                    head's [q_h; k_kv; v_kv] projections (RoPE applied),
+//                    hands them to every CTA of the cluster through
+//                    distributed shared memory, then takes positions
+//                    [n*j/8, n*(j+1)/8) of the cache in an online softmax;
+//                    the 8 partials are exchanged the same way and merged in
+//                    every CTA, which then multiplies rows [d*j/8, d*(j+1)/8)
+//                    of Wo's head-h column block by att_h and adds the result
+//                    into the residual. The first query head of each kv group
+//                    also appends k and v to the cache.
+//   FFN block        grid G, CTA c owns hidden units [F*c/G, F*(c+1)/G): it
+//                    computes their SwiGLU values from its W1/W3 rows, then
+//                    their contribution W2[:, units] * hb to all d outputs (W2
+//                    stored transposed, so the columns are contiguous rows),
+//                    and adds it into the residual.
+//
+// Both blocks add into a residual that many CTAs update, so the residual
+// stream is kept in 64-bit fixed point (value * 2^32, rounded to nearest;
+// magnitudes below 2^31): integer additions are exact and commutative, so
+// the sum, and therefore every result, is the same whatever order the
+// atomics land in. Each partial is rounded once to 2^-32 (about 2.3e-10),
+// finer than fp32's own rounding for values above 2^-9. Buffers: P[2] (the
+// residual between layers) and M[2] (after attention), each kernel zeroing
+// the buffer the next one accumulates into (a buffer is zeroed only after
+// its last reader has finished: kernel boundaries order them).
+//
+// Each CTA's weights (its Q/K/V rows and Wo block rows, or its W1/W3 rows
+// and W2 columns) fit in shared memory and are requested with bulk copies at
+// kernel start, before griddepcontrol.wait: weights never depend on the
+// previous kernel, so they load while it finishes.
+#include <cooperative_groups.h>
+#include <math.h>
+
+#include "l2_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace l2 {
+
+namespace {
+
+constexpr int kFThreads = 256;
+constexpr int kFWarps = kFThreads / 32;
+constexpr int G8 = kFusedCluster;
+
+__device__ __forceinline__ long long to_fixed(float v) {
+    return __float2ll_rn(v * 4294967296.0f);
+}
+__device__ __forceinline__ float from_fixed(long long x) {
+    return __ll2float_rn(x) * (1.0f / 4294967296.0f);
+}
+// Adds without waiting for the old value (a reduction, not a returning
+// atomic): a thread issues its adds back to back. Kernel completion makes them
+// visible to the next kernel, which is the only reader.
+__device__ __forceinline__ void add_fixed(long long* p, long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Shared-memory carve-up of the attention block (floats; every piece 16-byte aligned).
+struct FAttnLayout {
+    int rows_qkv, rows_o;       // this CTA's Q/K/V rows and Wo block rows (maximum over ranks)
+    int off_wq, off_wo, off_x, off_qkv, off_part, off_red, off_g, total;
+};
+__host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
+    FAttnLayout L;
+    L.rows_qkv = (3 * hd) / G8;
+    L.rows_o = (d + G8 - 1) / G8;
+    L.off_wq = 0;
+    L.off_wo = L.off_wq + L.rows_qkv * d;
+    L.off_x = L.off_wo + ((L.rows_o * hd + 3) & ~3);
+    L.off_qkv = L.off_x + ((d + 3) & ~3);
+    L.off_part = L.off_qkv + ((3 * hd + 3) & ~3);
+    L.off_red = L.off_part + G8 * ((hd + 2 + 3) & ~3);
+    L.off_g = L.off_red + kFWarps * ((hd + 2 + 3) & ~3) + 64;
+    L.total = L.off_g + ((d + 3) & ~3);
+    return L;
+}
+
+// RMS-normalised input row: xs = g * x / sqrt(mean(x^2) + eps), x given in
+// float (src) or fixed point (srcf), the gain g in shared memory.
+__device__ __forceinline__ void norm_row(float* xs, const float* src, const long long* srcf,
+                                         const float* g, int d, float eps, float* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float ss = 0.0f;
+    for (int i = tid; i < d; i += kFThreads) {
+        const float v = srcf ? from_fixed(__ldcg(srcf + i)) : __ldg(src + i);
+        xs[i] = v;
+        ss += v * v;
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < kFWarps ? red[lane] : 0.0f;
+        t = warp_sum(t);
+        if (lane == 0) red[32] = 1.0f / sqrtf(t / static_cast<float>(d) + eps);
+    }
+    __syncthreads();
+    const float inv = red[32];
+    for (int i = tid; i < d; i += kFThreads) xs[i] = g[i] * (inv * xs[i]);
+    __syncthreads();
+}
+
+// Dot product of a shared-memory row with xs by one warp (16-byte loads).
+__device__ __forceinline__ float warp_dot(const float* w, const float* xs, int d, int lane) {
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const float4* x4 = reinterpret_cast<const float4*>(xs);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = lane; c < (d >> 2); c += 32) {
+        const float4 a = w4[c], b = x4[c];
+        acc.x = fmaf(a.x, b.x, acc.x);
+        acc.y = fmaf(a.y, b.y, acc.y);
+        acc.z = fmaf(a.z, b.z, acc.z);
+        acc.w = fmaf(a.w, b.w, acc.w);
+    }
+    return warp_sum((acc.x + acc.y) + (acc.z + acc.w));
+}
+
+// LPR lanes read one 16-byte-vectorised cache row (head_dim <= 4 LPR).
+template <int LPR>
+__global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant__ FAttnArgs a) {
+    constexpr int RPW = 32 / LPR;  // rows per warp load
+    constexpr int GR = 4;          // row slots per lane group and iteration
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* sm = reinterpret_cast<float*>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int j = static_cast<int>(cluster.block_rank());
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = a.d, hd = a.hd, kvd = a.kvd;
+    const int grp = a.H / a.KVH, kvh = h / grp;
+    const FAttnLayout L = fattn_layout(d, hd);
+    float* wq = sm + L.off_wq;
+    float* wo = sm + L.off_wo;
+    float* xs = sm + L.off_x;
+    float* qkv = sm + L.off_qkv;
+    float* part = sm + L.off_part;
+    float* red = sm + L.off_red;
+    float* gs = sm + L.off_g;
+    const int pstride = (hd + 2 + 3) & ~3;
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int s_fail;
+
+    // this CTA's slices
+    const int t0 = (3 * hd) * j / G8, t1 = (3 * hd) * (j + 1) / G8;  // rows of [q; k; v]
+    const int r0 = d * j / G8, r1 = d * (j + 1) / G8;                  // rows of the Wo block
+
+    if (tid == 0) {
+        s_fail = 0;
+        mbar_init(&wbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint64_t pol = (a.l2_policy == 0) ? make_policy_evict_first()
+                                                : make_policy_evict_last(__uint_as_float(
+                                                      static_cast<uint32_t>(a.l2_policy)));
+        const uint32_t bytes = static_cast<uint32_t>(((t1 - t0) * d + (r1 - r0) * hd + d) * 4);
+        mbar_arrive_expect_tx(&wbar, bytes);
+        bulk_g2s(gs, a.g_att, static_cast<uint32_t>(d * 4), &wbar, pol);
+        // [q; k; v] rows t0..t1 as up to three runs of contiguous global rows
+        int t = t0;
+        while (t < t1) {
+            const int part_end = t < hd ? hd : t < 2 * hd ? 2 * hd : 3 * hd;
+            const int e = min(t1, part_end);
+            const int g0 = t < hd ? h * hd + t : t < 2 * hd ? d + kvh * hd + (t - hd)
+                                                               : d + kvd + kvh * hd + (t - 2 * hd);
+            bulk_g2s(wq + static_cast<size_t>(t - t0) * d, a.wqkv + static_cast<size_t>(g0) * d,
+                     static_cast<uint32_t>((e - t) * d * 4), &wbar, pol);
+            t = e;
+        }
+        bulk_g2s(wo, a.wo_h + (static_cast<size_t>(h) * d + r0) * hd,
+                 static_cast<uint32_t>((r1 - r0) * hd * 4), &wbar, pol);
+    }
+    pdl_launch_dependents();
+    cluster_arrive_relaxed();  // this CTA runs (waited for before remote writes)
+
+    // ---- everything below reads results of earlier kernels
+    pdl_wait();
+    L2State* st = a.st;
+    const int pos = __ldcg(&st->pos);
+    const int slot_cur = pos % a.S;
+    const int n = min(pos + 1, a.S);
+    const float* emb_row = nullptr;
+    if (a.x_in == nullptr) {
+        const int raw = __ldcg(&st->token);
+        const int tok = min(max(raw, 0), a.vocab - 1);
+        if (raw != tok && h == 0 && j == 0 && tid == 0) atomicOr(&st->err, ERR_BAD_INPUT);
+        emb_row = a.emb + static_cast<size_t>(tok) * d;
+    }
+    // head 0's CTAs carry the residual into x_mid and clear the FFN output
+    if (h == 0) {
+        for (int r = r0 + tid; r < r1; r += kFThreads) {
+            const long long xr = a.x_in ? __ldcg(a.x_in + r) : to_fixed(__ldg(emb_row + r));
+            add_fixed(a.x_mid + r, xr);
+            a.x_zero[r] = 0;
+        }
+    }
+    if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
+        atomicOr(&st->err, ERR_TIMEOUT_TMA);
+        s_fail = 1;
+        mbar_wait_bounded(&wbar, 0u);  // drain the copies still in flight (bounded)
+    }
+    __syncthreads();
+    const bool ok = s_fail == 0;  // on a timeout the exchange still runs (every CTA
+                                  // takes the cluster barriers), with zero rows
+    if (!ok)
+        for (int i = tid; i < d; i += kFThreads) gs[i] = 0.0f;
+    norm_row(xs, emb_row, a.x_in, gs, d, a.eps, red);
+
+    // ---- Q/K/V rows of this CTA (pairs per warp: RoPE needs both)
+    const int half = hd >> 1;
+    const float2* rope = a.rope + static_cast<size_t>(pos) * half;
+    const bool writer = (h % grp) == 0;  // appends k and v for its kv head
+    float* kc = a.k_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
+    float* vc = a.v_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
+    cluster_wait_all();  // every CTA of the cluster runs: remote writes allowed
+    for (int p = warp; 2 * p < t1 - t0; p += kFWarps) {
+        const int tl = 2 * p, tg = t0 + tl;  // even: a pair never straddles q/k/v
+        float v0 = 0.0f, v1 = 0.0f;
+        if (ok) {
+            v0 = warp_dot(wq + static_cast<size_t>(tl) * d, xs, d, lane);
+            v1 = warp_dot(wq + static_cast<size_t>(tl + 1) * d, xs, d, lane);
+        }
+        if (tg < 2 * hd) {  // q or k: rotate the pair
+            const int e = tg < hd ? tg : tg - hd;
+            const float2 cs = rope[e >> 1];
+            const float y0 = v0 * cs.x - v1 * cs.y, y1 = v0 * cs.y + v1 * cs.x;
+            v0 = y0;
+            v1 = y1;
+            if (tg >= hd && writer && lane == 0) {
+                kc[e] = v0;
+                kc[e + 1] = v1;
+            }
+        } else if (writer && lane == 0) {
+            const int e = tg - 2 * hd;
+            vc[e] = v0;
+            vc[e + 1] = v1;
+        }
+        if (lane < G8) {  // lane q writes the pair into rank q's copy
+            float* dst = cluster.map_shared_rank(qkv, lane);
+            dst[tg] = v0;
+            dst[tg + 1] = v1;
+        }
+    }
+    cluster.sync();  // q, k, v of the head are in every CTA
+
+    // ---- attention over this CTA's share of the cache slots
+    {
+        const int hd4 = hd >> 2;
+        const int c4 = lane % LPR, slot = lane / LPR;
+        const bool lane_on = c4 < hd4;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4* K4 = reinterpret_cast<const float4*>(a.k_cache + static_cast<size_t>(kvh) * a.S * hd);
+        const float4* V4 = reinterpret_cast<const float4*>(a.v_cache + static_cast<size_t>(kvh) * a.S * hd);
+        const float4 q = lane_on ? reinterpret_cast<const float4*>(qkv)[c4] : z;
+        const float4 kcur = lane_on ? reinterpret_cast<const float4*>(qkv + hd)[c4] : z;
+        const float4 vcur = lane_on ? reinterpret_cast<const float4*>(qkv + 2 * hd)[c4] : z;
+        const int s0 = static_cast<int>(static_cast<long long>(n) * j / G8);
+        const int s1 = static_cast<int>(static_cast<long long>(n) * (j + 1) / G8);
+        const float scale_div = sqrtf(static_cast<float>(hd));
+        float m = -INFINITY, l = 0.0f;
+        float4 o = z;
+        constexpr int PER_IT = GR * RPW;
+        for (int tb = s0 + warp * PER_IT; tb < s1; tb += kFWarps * PER_IT) {
+            float4 kr[GR], vr[GR];
+#pragma unroll
+            for (int g = 0; g < GR; ++g) {
+                const int t = tb + g * RPW + slot;
+                const bool in = lane_on && t < s1;
+                if (in && t == slot_cur) {  // this position: from shared memory
+                    kr[g] = kcur;
+                    vr[g] = vcur;
+                } else {
+                    kr[g] = in ? __ldcg(K4 + static_cast<size_t>(t) * hd4 + c4) : z;
+                    vr[g] = in ? __ldcg(V4 + static_cast<size_t>(t) * hd4 + c4) : z;
+                }
+            }
+            float sc[GR];
+            float gmax = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < GR; ++g) {
+                float pq = q.x * kr[g].x;
+                pq = fmaf(q.y, kr[g].y, pq);
+                pq = fmaf(q.z, kr[g].z, pq);
+                pq = fmaf(q.w, kr[g].w, pq);
+#pragma unroll
+                for (int off = LPR / 2; off > 0; off >>= 1) pq += __shfl_xor_sync(0xffffffffu, pq, off);
+                sc[g] = (tb + g * RPW + slot < s1) ? pq / scale_div : -INFINITY;
+                gmax = fmaxf(gmax, sc[g]);
+            }
+            if (gmax == -INFINITY) continue;
+            const float mnew = fmaxf(m, gmax);
+            const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+            l *= corr;
+            o.x *= corr;
+            o.y *= corr;
+            o.z *= corr;
+            o.w *= corr;
+#pragma unroll
+            for (int g = 0; g < GR; ++g) {
+                const float pe = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+                l += pe;
+                o.x = fmaf(pe, vr[g].x, o.x);
+                o.y = fmaf(pe, vr[g].y, o.y);
+                o.z = fmaf(pe, vr[g].z, o.z);
+                o.w = fmaf(pe, vr[g].w, o.w);
+            }
+            m = mnew;
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {  // merge the row slots of the warp
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float l2v = __shfl_xor_sync(0xffffffffu, l, off);
+            float4 o2;
+            o2.x = __shfl_xor_sync(0xffffffffu, o.x, off);
+            o2.y = __shfl_xor_sync(0xffffffffu, o.y, off);
+            o2.z = __shfl_xor_sync(0xffffffffu, o.z, off);
+            o2.w = __shfl_xor_sync(0xffffffffu, o.w, off);
+            const float M = fmaxf(m, m2);
+            const float f1 = (m == -INFINITY) ? 0.0f : expf(m - M);
+            const float f2 = (m2 == -INFINITY) ? 0.0f : expf(m2 - M);
+            l = l * f1 + l2v * f2;
+            o.x = o.x * f1 + o2.x * f2;
+            o.y = o.y * f1 + o2.y * f2;
+            o.z = o.z * f1 + o2.z * f2;
+            o.w = o.w * f1 + o2.w * f2;
+            m = M;
+        }
+        float* wp = red + warp * pstride;  // per-warp partial: o[hd], m, l
+        if (slot == 0 && lane_on) reinterpret_cast<float4*>(wp)[c4] = o;
+        if (lane == 0) {
+            wp[hd] = m;
+            wp[hd + 1] = l;
+        }
+        __syncthreads();
+        // the CTA's partial, sent to every CTA of the cluster (slot j)
+        float M = -INFINITY;
+        for (int w = 0; w < kFWarps; ++w) M = fmaxf(M, red[w * pstride + hd]);
+        for (int e = tid; e < hd + 2; e += kFThreads) {
+            float acc = 0.0f;
+            for (int w = 0; w < kFWarps; ++w) {
+                const float mw = red[w * pstride + hd];
+                if (mw == -INFINITY) continue;
+                acc += (e < hd ? red[w * pstride + e] : red[w * pstride + hd + 1]) * expf(mw - M);
+            }
+            const float val = (e == hd) ? M : acc;
+            for (int q2 = 0; q2 < G8; ++q2) cluster.map_shared_rank(part, q2)[j * pstride + e] = val;
+        }
+    }
+    cluster.sync();  // every CTA holds the 8 partials; no remote access after this
+
+    // ---- merge the partials into att_h (in xs: x is no longer needed)
+    float* att = xs;
+    {
+        float Mg = -INFINITY;
+        for (int q2 = 0; q2 < G8; ++q2) Mg = fmaxf(Mg, part[q2 * pstride + hd]);
+        float Lg = 0.0f;
+        for (int q2 = 0; q2 < G8; ++q2) {
+            const float mq = part[q2 * pstride + hd];
+            if (mq != -INFINITY) Lg += part[q2 * pstride + hd + 1] * expf(mq - Mg);
+        }
+        for (int e = tid; e < hd; e += kFThreads) {
+            float acc = 0.0f;
+            for (int q2 = 0; q2 < G8; ++q2) {
+                const float mq = part[q2 * pstride + hd];
+                if (mq != -INFINITY) acc += part[q2 * pstride + e] * expf(mq - Mg);
+            }
+            att[e] = acc / Lg;
+        }
+    }
+    __syncthreads();
+
+    // ---- rows r0..r1 of Wo's head-h block times att_h, into x_mid
+    for (int r = r0 + warp; r < r1; r += kFWarps) {
+        const float* w = wo + static_cast<size_t>(r - r0) * hd;
+        float acc = 0.0f;
+        for (int e = lane; e < hd; e += 32) acc = fmaf(w[e], att[e], acc);
+        acc = warp_sum(acc);
+        if (lane == 0 && ok) add_fixed(a.x_mid + r, to_fixed(acc));
+    }
+}
+
+// Shared-memory carve-up of the FFN block for at most `units` hidden units.
+struct FFfnLayout {
+    int off_w13, off_w2, off_x, off_hb, off_red, off_g, total;
+};
+__host__ __device__ inline FFfnLayout fffn_layout(int d, int units) {
+    FFfnLayout L;
+    L.off_w13 = 0;
+    L.off_w2 = L.off_w13 + 2 * units * d;
+    L.off_x = L.off_w2 + units * d;
+    L.off_hb = L.off_x + ((d + 3) & ~3);
+    L.off_red = L.off_hb + ((units + 3) & ~3);
+    L.off_g = L.off_red + 64;
+    L.total = L.off_g + ((d + 3) & ~3);
+    return L;
+}
+
+__global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__ FFfnArgs f) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float* sm = reinterpret_cast<float*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = f.d, G = gridDim.x, c = blockIdx.x;
+    const int u0 = static_cast<int>(static_cast<long long>(f.F) * c / G);
+    const int u1 = static_cast<int>(static_cast<long long>(f.F) * (c + 1) / G);
+    const int nu = u1 - u0;
+    const int umax = (f.F + G - 1) / G;
+    const FFfnLayout L = fffn_layout(d, umax);
+    float* w13 = sm + L.off_w13;
+    float* w2t = sm + L.off_w2;
+    float* xs = sm + L.off_x;
+    float* hb = sm + L.off_hb;
+    float* red = sm + L.off_red;
+    float* gs = sm + L.off_g;
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int s_fail;
+
+    if (tid == 0) {
+        s_fail = 0;
+        mbar_init(&wbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
+                                                : make_policy_evict_last(__uint_as_float(
+                                                      static_cast<uint32_t>(f.l2_policy)));
+        mbar_arrive_expect_tx(&wbar, static_cast<uint32_t>((3 * nu * d + d) * 4));
+        bulk_g2s(gs, f.g_ffn, static_cast<uint32_t>(d * 4), &wbar, pol);
+    }
+    if (tid == 0 && nu > 0) {
+        const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
+                                                : make_policy_evict_last(__uint_as_float(
+                                                      static_cast<uint32_t>(f.l2_policy)));
+        bulk_g2s(w13, f.w13 + static_cast<size_t>(2 * u0) * d, static_cast<uint32_t>(2 * nu * d * 4),
+                 &wbar, pol);
+        bulk_g2s(w2t, f.w2t + static_cast<size_t>(u0) * d, static_cast<uint32_t>(nu * d * 4), &wbar,
+                 pol);
+    }
+    pdl_launch_dependents();
+
+    pdl_wait();
+    // carry the residual into x_out and clear the next attention output,
+    // rows split over the CTAs
+    {
+        const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
+        const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
+        for (int r = q0 + tid; r < q1; r += kFThreads) {
+            add_fixed(f.x_out + r, __ldcg(f.x_mid + r));
+            f.x_zero[r] = 0;
+        }
+    }
+    if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
+        atomicOr(f.err, ERR_TIMEOUT_TMA);
+        s_fail = 1;
+        mbar_wait_bounded(&wbar, 0u);  // drain the copies still in flight (bounded)
+    }
+    __syncthreads();
+    if (s_fail || nu == 0) return;
+    norm_row(xs, nullptr, f.x_mid, gs, d, f.eps, red);
+
+    // SwiGLU of the CTA's hidden units (interleaved rows: 2u gate, 2u + 1 up)
+    for (int u = warp; u < nu; u += kFWarps) {
+        const float g = warp_dot(w13 + static_cast<size_t>(2 * u) * d, xs, d, lane);
+        const float up = warp_dot(w13 + static_cast<size_t>(2 * u + 1) * d, xs, d, lane);
+        if (lane == 0) hb[u] = (g / (1.0f + expf(-g))) * up;
+    }
+    __syncthreads();
+    // their contribution to every output: y[i] = sum_u W2[i][u0 + u] hb[u]
+    for (int i = tid; i < d; i += kFThreads) {
+        float acc = 0.0f;
+        for (int u = 0; u < nu; ++u) acc = fmaf(w2t[static_cast<size_t>(u) * d + i], hb[u], acc);
+        add_fixed(f.x_out + i, to_fixed(acc));
+    }
+}
+
+template <typename Kernel>
+cudaError_t set_smem(Kernel k, int bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+bool plan_fused(FAttnArgs& a, FFfnArgs& f, int num_sms, size_t smem_optin, int* ffn_grid) {
+    const int d = a.d, hd = a.hd;
+    if (hd % 4 != 0 || hd > 128 || d % 4 != 0) return false;
+    if ((3 * hd) % (2 * G8) != 0) return false;  // even row slices (RoPE pairs)
+    const size_t budget = smem_optin - 1024;     // static shared memory
+    const FAttnLayout la = fattn_layout(d, hd);
+    a.smem_bytes = la.total * 4;
+    if (static_cast<size_t>(a.smem_bytes) > budget) return false;
+    int G = num_sms < f.F ? num_sms : f.F;
+    const FFfnLayout lf = fffn_layout(d, (f.F + G - 1) / G);
+    f.smem_bytes = lf.total * 4;
+    if (static_cast<size_t>(f.smem_bytes) > budget) return false;
+    *ffn_grid = G;
+    return true;
+}
+
+cudaError_t prepare_fused(const FAttnArgs& a, const FFfnArgs& f) {
+    cudaError_t e;
+    if ((e = set_smem(fattn_kernel<16>, a.smem_bytes)) != cudaSuccess) return e;
+    if ((e = set_smem(fattn_kernel<32>, a.smem_bytes)) != cudaSuccess) return e;
+    return set_smem(fffn_kernel, f.smem_bytes);
+}
+
+cudaError_t launch_fattn(const FAttnArgs& a, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(G8, a.H);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = a.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G8;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    if (a.hd <= 64) return cudaLaunchKernelEx(&cfg, fattn_kernel<16>, a);
+    return cudaLaunchKernelEx(&cfg, fattn_kernel<32>, a);
+}
+
+cudaError_t launch_fffn(const FFfnArgs& f, int grid, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = f.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fffn_kernel, f);
+}
+
+}  // namespace l2

@@ -90,6 +90,49 @@ struct MatvecArgs {
     // state
     L2State* st;
     uint64_t l2_policy;    // createpolicy descriptor for the weight stream
+    // two-kernels-per-layer path: the input vector in fixed point (instead of
+    // src) and a fixed-point buffer CTA 0 zeroes (n entries)
+    const long long* src_fixed;
+    long long* zero_fixed;
+    int zero_n;
+};
+
+// Small-model batch-1 forward in two kernels per layer (fused_small.cu). The
+// residual stream lives in 64-bit fixed point (value * 2^32) so that many CTAs
+// can add into it with integer atomics, whose result does not depend on their
+// order.
+constexpr int kFusedCluster = 8;  // CTAs per query head in the attention block
+
+struct FAttnArgs {
+    const float* wqkv;     // this layer's [d + 2 kvd][d]
+    const float* wo_h;     // this layer's Wo re-tiled per head: [H][d][hd]
+    const float* g_att;    // this layer's attention RMSNorm gain [d]
+    const float* emb;      // layer 0: the input row is emb[token]
+    const long long* x_in; // residual entering the layer (null at layer 0)
+    long long* x_mid;      // += x_in + sum over heads of Wo_h att_h (zero on entry)
+    long long* x_zero;     // zeroed here: the FFN block's output buffer
+    float* k_cache;        // this layer's caches, head-major [KVH][S][hd]
+    float* v_cache;
+    const float2* rope;    // [positions][hd/2]
+    L2State* st;
+    int d, kvd, hd, H, KVH, S, vocab;
+    float eps;
+    uint64_t l2_policy;
+    int smem_bytes;
+};
+
+struct FFfnArgs {
+    const float* w13;      // this layer's interleaved W1/W3 rows [2F][d]
+    const float* w2t;      // this layer's W2 transposed: [F][d]
+    const float* g_ffn;    // this layer's FFN RMSNorm gain [d]
+    const long long* x_mid;  // residual after attention
+    long long* x_out;      // += x_mid + W2 (silu(W1 xn) * W3 xn) (zero on entry)
+    long long* x_zero;     // zeroed here: the next layer's attention output buffer
+    int* err;
+    int d, F;
+    float eps;
+    uint64_t l2_policy;
+    int smem_bytes;
 };
 
 struct AttnArgs {
@@ -414,8 +457,22 @@ cudaError_t launch_badvance(const BAdvanceArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_bsample(const BSampleArgs& a, int M, cudaStream_t s, bool pdl);
 
+// fused_small.cu
+// Whether the two-kernels-per-layer path fits this shape; fills the launch
+// shared-memory sizes of the two kernels and the FFN block's grid.
+bool plan_fused(FAttnArgs& a, FFfnArgs& f, int num_sms, size_t smem_optin, int* ffn_grid);
+cudaError_t prepare_fused(const FAttnArgs& a, const FFfnArgs& f);
+cudaError_t launch_fattn(const FAttnArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_fffn(const FFfnArgs& f, int grid, cudaStream_t s, bool pdl);
+
 // layout.cu
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
                                    int cols, cudaStream_t s);
+// dst[l][h][r][e] = src[l][r][h*hd + e]: Wo [L][d][d] as per-head column blocks.
+cudaError_t launch_retile_heads(float* dst, const float* src, int layers, int d, int hd,
+                                cudaStream_t s);
+// dst[l][c][r] = src[l][r][c]: per-layer transpose of [rows][cols].
+cudaError_t launch_transpose_layers(float* dst, const float* src, int layers, int rows, int cols,
+                                    cudaStream_t s);
 
 }  // namespace l2

@@ -27,7 +27,52 @@ __global__ void interleave_rows_kernel(float4* __restrict__ dst, const float4* _
     }
 }
 
+// Wo as per-head column blocks, so that the CTAs of head h read rows of a
+// contiguous [d][hd] block.
+__global__ void retile_heads_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                    long long total, int d, int hd) {
+    const int H = d / hd;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int e = static_cast<int>(i % hd);
+        long long t = i / hd;
+        const int r = static_cast<int>(t % d);
+        t /= d;
+        const int h = static_cast<int>(t % H);
+        const long long l = t / H;
+        dst[i] = src[(l * d + r) * d + static_cast<long long>(h) * hd + e];
+    }
+}
+
+// W2 transposed per layer, so that the CTA owning hidden units u0..u1 reads
+// their columns as contiguous rows.
+__global__ void transpose_layers_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                        long long total, int rows, int cols) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i % rows);
+        long long t = i / rows;
+        const int c = static_cast<int>(t % cols);
+        const long long l = t / cols;
+        dst[i] = src[(l * rows + r) * cols + c];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_retile_heads(float* dst, const float* src, int layers, int d, int hd,
+                                cudaStream_t s) {
+    if (hd < 1 || d % hd != 0) return cudaErrorInvalidValue;
+    retile_heads_kernel<<<4096, 256, 0, s>>>(dst, src, static_cast<long long>(layers) * d * d, d, hd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_layers(float* dst, const float* src, int layers, int rows, int cols,
+                                    cudaStream_t s) {
+    transpose_layers_kernel<<<4096, 256, 0, s>>>(
+        dst, src, static_cast<long long>(layers) * rows * cols, rows, cols);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_interleave_rows(float* dst, const float* a, const float* b, long long rows,
                                    int cols, cudaStream_t s) {

@@ -180,7 +180,30 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
     }
     const float4* src4 = reinterpret_cast<const float4*>(src);
     float4* xs4 = reinterpret_cast<float4*>(xs);
-    if (a.gain != nullptr) {
+    if (a.zero_fixed != nullptr && blockIdx.x == 0)
+        for (int i = tid; i < a.zero_n; i += kThreads) a.zero_fixed[i] = 0;
+    if (a.src_fixed != nullptr) {
+        // the residual in fixed point (value * 2^32): converted once into xs
+        float ss = 0.0f;
+        for (int i = tid; i < K; i += kThreads) {
+            const float v = __ll2float_rn(__ldcg(a.src_fixed + i)) * (1.0f / 4294967296.0f);
+            xs[i] = v;
+            ss += v * v;
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) scratch[warp] = ss;
+        __syncthreads();
+        if (warp == 0) {
+            float t = lane < kWarps ? scratch[lane] : 0.0f;
+            t = warp_sum(t);
+            if (lane == 0) scratch[32] = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
+        }
+        __syncthreads();
+        if (a.gain != nullptr) {
+            const float inv = scratch[32];
+            for (int i = tid; i < K; i += kThreads) xs[i] = __ldg(a.gain + i) * (inv * xs[i]);
+        }
+    } else if (a.gain != nullptr) {
         float ss = 0.0f;
         for (int i = tid; i < K4; i += kThreads) {
             const float4 v = __ldcg(src4 + i);
