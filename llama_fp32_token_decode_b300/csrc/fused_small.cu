@@ -87,28 +87,55 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     return L;
 }
 
-// RMS-normalised input row: xs = g * x / sqrt(mean(x^2) + eps), x given in
-// float (src) or fixed point (srcf), the gain g in shared memory.
-__device__ __forceinline__ void norm_row(float* xs, const float* src, const long long* srcf,
-                                         const float* g, int d, float eps, float* red) {
+// First half of the RMS norm: loads x (float src, or fixed point srcf) into
+// xs and returns 1 / sqrt(mean(x^2) + eps). Each thread issues all its loads
+// before using one (one L2 round trip for d <= 4 * threads). Rows c0..c1 of x
+// are also added into `carry` and cleared in `zero` from the same loads.
+constexpr int kRowRegs = 4;
+__device__ __forceinline__ float norm_load(float* xs, const float* src, const long long* srcf,
+                                           int d, float eps, float* red, long long* carry,
+                                           long long* zero, int c0, int c1) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float ss = 0.0f;
-    for (int i = tid; i < d; i += kFThreads) {
-        const float v = srcf ? from_fixed(__ldcg(srcf + i)) : __ldg(src + i);
-        xs[i] = v;
-        ss += v * v;
+    for (int base = 0; base < d; base += kRowRegs * kFThreads) {
+        long long fx[kRowRegs];
+        float v[kRowRegs];
+#pragma unroll
+        for (int k = 0; k < kRowRegs; ++k) {
+            const int i = base + k * kFThreads + tid;
+            fx[k] = 0;
+            v[k] = 0.0f;
+            if (i < d) {
+                if (srcf) fx[k] = __ldcg(srcf + i);
+                else v[k] = __ldg(src + i);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRowRegs; ++k) {
+            const int i = base + k * kFThreads + tid;
+            if (i < d) {
+                if (srcf) v[k] = from_fixed(fx[k]);
+                xs[i] = v[k];
+                ss += v[k] * v[k];
+                if (i >= c0 && i < c1) {
+                    add_fixed(carry + i, srcf ? fx[k] : to_fixed(v[k]));
+                    zero[i] = 0;
+                }
+            }
+        }
     }
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
-    if (warp == 0) {
-        float t = lane < kFWarps ? red[lane] : 0.0f;
-        t = warp_sum(t);
-        if (lane == 0) red[32] = 1.0f / sqrtf(t / static_cast<float>(d) + eps);
-    }
-    __syncthreads();
-    const float inv = red[32];
-    for (int i = tid; i < d; i += kFThreads) xs[i] = g[i] * (inv * xs[i]);
+    float t = lane < kFWarps ? red[lane] : 0.0f;  // every warp forms the same total
+    t = warp_sum(t);
+    return 1.0f / sqrtf(t / static_cast<float>(d) + eps);
+}
+
+// Second half: xs = g * (inv * x), g in shared memory. Each thread scales the
+// elements it loaded, so only the barrier after it is needed.
+__device__ __forceinline__ void norm_scale(float* xs, const float* g, float inv, int d) {
+    for (int i = threadIdx.x; i < d; i += kFThreads) xs[i] = g[i] * (inv * xs[i]);
     __syncthreads();
 }
 
@@ -200,13 +227,8 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         emb_row = a.emb + static_cast<size_t>(tok) * d;
     }
     // head 0's CTAs carry the residual into x_mid and clear the FFN output
-    if (h == 0) {
-        for (int r = r0 + tid; r < r1; r += kFThreads) {
-            const long long xr = a.x_in ? __ldcg(a.x_in + r) : to_fixed(__ldg(emb_row + r));
-            add_fixed(a.x_mid + r, xr);
-            a.x_zero[r] = 0;
-        }
-    }
+    const float inv = norm_load(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
+                                h == 0 ? r0 : 0, h == 0 ? r1 : 0);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(&st->err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -217,7 +239,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
                                   // takes the cluster barriers), with zero rows
     if (!ok)
         for (int i = tid; i < d; i += kFThreads) gs[i] = 0.0f;
-    norm_row(xs, emb_row, a.x_in, gs, d, a.eps, red);
+    norm_scale(xs, gs, inv, d);
 
     // ---- Q/K/V rows of this CTA (pairs per warp: RoPE needs both)
     const int half = hd >> 1;
@@ -454,14 +476,9 @@ __global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__
     pdl_wait();
     // carry the residual into x_out and clear the next attention output,
     // rows split over the CTAs
-    {
-        const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
-        const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
-        for (int r = q0 + tid; r < q1; r += kFThreads) {
-            add_fixed(f.x_out + r, __ldcg(f.x_mid + r));
-            f.x_zero[r] = 0;
-        }
-    }
+    const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
+    const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
+    const float inv = norm_load(xs, nullptr, f.x_mid, d, f.eps, red, f.x_out, f.x_zero, q0, q1);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(f.err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -469,7 +486,7 @@ __global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__
     }
     __syncthreads();
     if (s_fail || nu == 0) return;
-    norm_row(xs, nullptr, f.x_mid, gs, d, f.eps, red);
+    norm_scale(xs, gs, inv, d);
 
     // SwiGLU of the CTA's hidden units (interleaved rows: 2u gate, 2u + 1 up)
     for (int u = warp; u < nu; u += kFWarps) {
@@ -498,13 +515,13 @@ bool plan_fused(FAttnArgs& a, FFfnArgs& f, int num_sms, size_t smem_optin, int* 
     if (hd % 4 != 0 || hd > 128 || d % 4 != 0) return false;
     if ((3 * hd) % (2 * G8) != 0) return false;  // even row slices (RoPE pairs)
     const size_t budget = smem_optin - 1024;     // static shared memory
-    const FAttnLayout la = fattn_layout(d, hd);
-    a.smem_bytes = la.total * 4;
-    if (static_cast<size_t>(a.smem_bytes) > budget) return false;
-    int G = num_sms < f.F ? num_sms : f.F;
-    const FFfnLayout lf = fffn_layout(d, (f.F + G - 1) / G);
-    f.smem_bytes = lf.total * 4;
-    if (static_cast<size_t>(f.smem_bytes) > budget) return false;
+    const int attn_bytes = fattn_layout(d, hd).total * 4;
+    if (static_cast<size_t>(attn_bytes) > budget) return false;
+    const int G = num_sms < f.F ? num_sms : f.F;
+    const int ffn_bytes = fffn_layout(d, (f.F + G - 1) / G).total * 4;
+    if (static_cast<size_t>(ffn_bytes) > budget) return false;
+    a.smem_bytes = attn_bytes;  // written only when the plan fits
+    f.smem_bytes = ffn_bytes;
     *ffn_grid = G;
     return true;
 }
