@@ -70,7 +70,7 @@ __device__ __forceinline__ void add_fixed(long long* p, long long v) {
 // Shared-memory carve-up of the attention block (floats; every piece 16-byte aligned).
 struct FAttnLayout {
     int rows_qkv, rows_o;       // this CTA's Q/K/V rows and Wo block rows (maximum over ranks)
-    int off_wq, off_wo, off_x, off_qkv, off_part, off_red, off_g, total;
+    int off_wq, off_wo, off_x, off_qkv, off_part, off_red, off_g, off_c, off_rs, total;
 };
 __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     FAttnLayout L;
@@ -83,18 +83,22 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     L.off_part = L.off_qkv + ((3 * hd + 3) & ~3);
     L.off_red = L.off_part + G8 * ((hd + 2 + 3) & ~3);
     L.off_g = L.off_red + kFWarps * ((hd + 2 + 3) & ~3) + 64;
-    L.total = L.off_g + ((d + 3) & ~3);
+    L.off_c = L.off_g + ((d + 3) & ~3);                         // carried rows, 8 bytes each
+    L.off_rs = L.off_c + 2 * ((d / G8 + 1 + 3) & ~3);           // RoPE pairs of the rows
+    L.total = L.off_rs + 2 * ((L.rows_qkv / 2 + 3) & ~3);
     return L;
 }
 
 // First half of the RMS norm: loads x (float src, or fixed point srcf) into
 // xs and returns 1 / sqrt(mean(x^2) + eps). Each thread issues all its loads
 // before using one (one L2 round trip for d <= 4 * threads). Rows c0..c1 of x
-// are also added into `carry` and cleared in `zero` from the same loads.
+// are also added into `carry` and cleared in `zero` from the same loads, or,
+// with `stash`, kept there in fixed point for the caller to add later.
 constexpr int kRowRegs = 4;
 __device__ __forceinline__ float norm_load(float* xs, const float* src, const long long* srcf,
                                            int d, float eps, float* red, long long* carry,
-                                           long long* zero, int c0, int c1) {
+                                           long long* zero, int c0, int c1,
+                                           long long* stash = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float ss = 0.0f;
     for (int base = 0; base < d; base += kRowRegs * kFThreads) {
@@ -118,8 +122,13 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
                 xs[i] = v[k];
                 ss += v[k] * v[k];
                 if (i >= c0 && i < c1) {
-                    add_fixed(carry + i, srcf ? fx[k] : to_fixed(v[k]));
-                    zero[i] = 0;
+                    const long long xf = srcf ? fx[k] : to_fixed(v[k]);
+                    if (stash) {
+                        stash[i - c0] = xf;
+                    } else {
+                        add_fixed(carry + i, xf);
+                        zero[i] = 0;
+                    }
                 }
             }
         }
@@ -139,19 +148,32 @@ __device__ __forceinline__ void norm_scale(float* xs, const float* g, float inv,
     __syncthreads();
 }
 
-// Dot product of a shared-memory row with xs by one warp (16-byte loads).
-__device__ __forceinline__ float warp_dot(const float* w, const float* xs, int d, int lane) {
-    const float4* w4 = reinterpret_cast<const float4*>(w);
+// Dot products of two shared-memory rows with xs by one warp (16-byte
+// loads; the x loads are shared).
+__device__ __forceinline__ float2 warp_dot2(const float* w0, const float* w1, const float* xs,
+                                            int d, int lane) {
+    const float4* a4 = reinterpret_cast<const float4*>(w0);
+    const float4* b4 = reinterpret_cast<const float4*>(w1);
     const float4* x4 = reinterpret_cast<const float4*>(xs);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
     for (int c = lane; c < (d >> 2); c += 32) {
-        const float4 a = w4[c], b = x4[c];
-        acc.x = fmaf(a.x, b.x, acc.x);
-        acc.y = fmaf(a.y, b.y, acc.y);
-        acc.z = fmaf(a.z, b.z, acc.z);
-        acc.w = fmaf(a.w, b.w, acc.w);
+        const float4 x = x4[c], a = a4[c], b = b4[c];
+        p.x = fmaf(a.x, x.x, p.x);
+        p.y = fmaf(a.y, x.y, p.y);
+        p.z = fmaf(a.z, x.z, p.z);
+        p.w = fmaf(a.w, x.w, p.w);
+        q.x = fmaf(b.x, x.x, q.x);
+        q.y = fmaf(b.y, x.y, q.y);
+        q.z = fmaf(b.z, x.z, q.z);
+        q.w = fmaf(b.w, x.w, q.w);
     }
-    return warp_sum((acc.x + acc.y) + (acc.z + acc.w));
+    float u = (p.x + p.y) + (p.z + p.w), v = (q.x + q.y) + (q.z + q.w);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        u += __shfl_xor_sync(0xffffffffu, u, off);
+        v += __shfl_xor_sync(0xffffffffu, v, off);
+    }
+    return make_float2(u, v);
 }
 
 // LPR lanes read one 16-byte-vectorised cache row (head_dim <= 4 LPR).
@@ -175,6 +197,8 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     float* part = sm + L.off_part;
     float* red = sm + L.off_red;
     float* gs = sm + L.off_g;
+    long long* cst = reinterpret_cast<long long*>(sm + L.off_c);
+    float2* rs = reinterpret_cast<float2*>(sm + L.off_rs);
     const int pstride = (hd + 2 + 3) & ~3;
     __shared__ __align__(8) uint64_t wbar;
     __shared__ int s_fail;
@@ -226,9 +250,17 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         if (raw != tok && h == 0 && j == 0 && tid == 0) atomicOr(&st->err, ERR_BAD_INPUT);
         emb_row = a.emb + static_cast<size_t>(tok) * d;
     }
-    // head 0's CTAs carry the residual into x_mid and clear the FFN output
+    // RoPE (cos, sin) of this CTA's q and k pairs, loaded beside x
+    const int half = hd >> 1;
+    const float2* rope = a.rope + static_cast<size_t>(pos) * half;
+    for (int p = tid; 2 * p < t1 - t0; p += kFThreads) {
+        const int tg = t0 + 2 * p;
+        if (tg < 2 * hd) rs[p] = __ldg(rope + ((tg < hd ? tg : tg - hd) >> 1));
+    }
+    // head 0's CTAs keep their rows of the residual, added into x_mid once the
+    // cluster barriers are behind them
     const float inv = norm_load(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
-                                h == 0 ? r0 : 0, h == 0 ? r1 : 0);
+                                h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(&st->err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -242,33 +274,21 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     norm_scale(xs, gs, inv, d);
 
     // ---- Q/K/V rows of this CTA (pairs per warp: RoPE needs both)
-    const int half = hd >> 1;
-    const float2* rope = a.rope + static_cast<size_t>(pos) * half;
-    const bool writer = (h % grp) == 0;  // appends k and v for its kv head
-    float* kc = a.k_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
-    float* vc = a.v_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
     cluster_wait_all();  // every CTA of the cluster runs: remote writes allowed
     for (int p = warp; 2 * p < t1 - t0; p += kFWarps) {
         const int tl = 2 * p, tg = t0 + tl;  // even: a pair never straddles q/k/v
         float v0 = 0.0f, v1 = 0.0f;
         if (ok) {
-            v0 = warp_dot(wq + static_cast<size_t>(tl) * d, xs, d, lane);
-            v1 = warp_dot(wq + static_cast<size_t>(tl + 1) * d, xs, d, lane);
+            const float2 r = warp_dot2(wq + static_cast<size_t>(tl) * d,
+                                       wq + static_cast<size_t>(tl + 1) * d, xs, d, lane);
+            v0 = r.x;
+            v1 = r.y;
         }
         if (tg < 2 * hd) {  // q or k: rotate the pair
-            const int e = tg < hd ? tg : tg - hd;
-            const float2 cs = rope[e >> 1];
+            const float2 cs = rs[p];
             const float y0 = v0 * cs.x - v1 * cs.y, y1 = v0 * cs.y + v1 * cs.x;
             v0 = y0;
             v1 = y1;
-            if (tg >= hd && writer && lane == 0) {
-                kc[e] = v0;
-                kc[e + 1] = v1;
-            }
-        } else if (writer && lane == 0) {
-            const int e = tg - 2 * hd;
-            vc[e] = v0;
-            vc[e + 1] = v1;
         }
         if (lane < G8) {  // lane q writes the pair into rank q's copy
             float* dst = cluster.map_shared_rank(qkv, lane);
@@ -383,6 +403,26 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     }
     cluster.sync();  // every CTA holds the 8 partials; no remote access after this
 
+    // ---- global writes that nothing in this kernel reads, issued after the
+    // last cluster barrier (whose release would otherwise wait for them):
+    // the carried residual rows, and this position's k and v, appended by the
+    // first cluster of each kv head, 1/8 of the 2 hd values per CTA
+    if (h == 0) {
+        for (int r = r0 + tid; r < r1; r += kFThreads) {
+            add_fixed(a.x_mid + r, cst[r - r0]);
+            a.x_zero[r] = 0;
+        }
+    }
+    if ((h % grp) == 0) {
+        float* kc = a.k_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
+        float* vc = a.v_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
+        const int e0 = 2 * hd * j / G8, e1 = 2 * hd * (j + 1) / G8;
+        for (int e = e0 + tid; e < e1; e += kFThreads) {
+            if (e < hd) kc[e] = qkv[hd + e];
+            else vc[e - hd] = qkv[hd + e];
+        }
+    }
+
     // ---- merge the partials into att_h (in xs: x is no longer needed)
     float* att = xs;
     {
@@ -404,13 +444,31 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     }
     __syncthreads();
 
-    // ---- rows r0..r1 of Wo's head-h block times att_h, into x_mid
-    for (int r = r0 + warp; r < r1; r += kFWarps) {
-        const float* w = wo + static_cast<size_t>(r - r0) * hd;
-        float acc = 0.0f;
-        for (int e = lane; e < hd; e += 32) acc = fmaf(w[e], att[e], acc);
-        acc = warp_sum(acc);
-        if (lane == 0 && ok) add_fixed(a.x_mid + r, to_fixed(acc));
+    // ---- rows r0..r1 of Wo's head-h block times att_h, into x_mid: 8 lanes
+    // per row (16-byte steps), 4 rows per warp at once
+    {
+        const int sub = lane >> 3, l8 = lane & 7, hd4 = hd >> 2;
+        const float4* a4 = reinterpret_cast<const float4*>(att);
+        for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * kFWarps) {
+            const int r = rb + sub;
+            float acc = 0.0f;
+            if (r < r1) {
+                const float4* w4 = reinterpret_cast<const float4*>(wo + static_cast<size_t>(r - r0) * hd);
+                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = l8; c < hd4; c += 8) {
+                    const float4 w = w4[c], x = a4[c];
+                    t.x = fmaf(w.x, x.x, t.x);
+                    t.y = fmaf(w.y, x.y, t.y);
+                    t.z = fmaf(w.z, x.z, t.z);
+                    t.w = fmaf(w.w, x.w, t.w);
+                }
+                acc = (t.x + t.y) + (t.z + t.w);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            if (l8 == 0 && r < r1 && ok) add_fixed(a.x_mid + r, to_fixed(acc));
+        }
     }
 }
 
@@ -490,9 +548,9 @@ __global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__
 
     // SwiGLU of the CTA's hidden units (interleaved rows: 2u gate, 2u + 1 up)
     for (int u = warp; u < nu; u += kFWarps) {
-        const float g = warp_dot(w13 + static_cast<size_t>(2 * u) * d, xs, d, lane);
-        const float up = warp_dot(w13 + static_cast<size_t>(2 * u + 1) * d, xs, d, lane);
-        if (lane == 0) hb[u] = (g / (1.0f + expf(-g))) * up;
+        const float2 gu = warp_dot2(w13 + static_cast<size_t>(2 * u) * d,
+                                    w13 + static_cast<size_t>(2 * u + 1) * d, xs, d, lane);
+        if (lane == 0) hb[u] = (gu.x / (1.0f + expf(-gu.x))) * gu.y;
     }
     __syncthreads();
     // their contribution to every output: y[i] = sum_u W2[i][u0 + u] hb[u]
