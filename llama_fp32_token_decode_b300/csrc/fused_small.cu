@@ -201,6 +201,8 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     float2* rs = reinterpret_cast<float2*>(sm + L.off_rs);
     const int pstride = (hd + 2 + 3) & ~3;
     __shared__ __align__(8) uint64_t wbar;
+    __shared__ __align__(8) uint64_t qbar;  // q, k, v rows from the cluster's CTAs
+    __shared__ __align__(8) uint64_t pbar;  // the 8 attention partials
     __shared__ int s_fail;
 
     // this CTA's slices
@@ -210,7 +212,11 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     if (tid == 0) {
         s_fail = 0;
         mbar_init(&wbar, 1);
+        mbar_init(&qbar, 1);
+        mbar_init(&pbar, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&qbar, static_cast<uint32_t>(3 * hd * 4));
+        mbar_arrive_expect_tx(&pbar, static_cast<uint32_t>(G8 * (hd + 2) * 4));
     }
     __syncthreads();
     if (tid == 0) {
@@ -290,13 +296,11 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             v0 = y0;
             v1 = y1;
         }
-        if (lane < G8) {  // lane q writes the pair into rank q's copy
-            float* dst = cluster.map_shared_rank(qkv, lane);
-            dst[tg] = v0;
-            dst[tg + 1] = v1;
-        }
+        if (lane < G8)  // lane q sends the pair to rank q's copy
+            st_async_f2(cluster_smem(qkv + tg, lane), v0, v1, cluster_smem(&qbar, lane));
     }
-    cluster.sync();  // q, k, v of the head are in every CTA
+    // q, k, v of the head are in every CTA once 3 hd floats have landed here
+    if (!mbar_wait_cluster_bounded(&qbar, 0u) && tid == 0) atomicOr(&st->err, ERR_TIMEOUT_TMA);
 
     // ---- attention over this CTA's share of the cache slots
     {
@@ -398,10 +402,14 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
                 acc += (e < hd ? red[w * pstride + e] : red[w * pstride + hd + 1]) * expf(mw - M);
             }
             const float val = (e == hd) ? M : acc;
-            for (int q2 = 0; q2 < G8; ++q2) cluster.map_shared_rank(part, q2)[j * pstride + e] = val;
+            for (int q2 = 0; q2 < G8; ++q2)
+                st_async_f1(cluster_smem(part + j * pstride + e, q2), val, cluster_smem(&pbar, q2));
         }
     }
-    cluster.sync();  // every CTA holds the 8 partials; no remote access after this
+    // every CTA holds the 8 partials once 8 (hd + 2) floats have landed here
+    if (!mbar_wait_cluster_bounded(&pbar, 0u) && tid == 0) atomicOr(&st->err, ERR_TIMEOUT_TMA);
+    cluster_arrive_relaxed();  // all remote writes into this CTA are done (waited
+                               // for at the end: no CTA leaves before its peers)
 
     // ---- global writes that nothing in this kernel reads, issued after the
     // last cluster barrier (whose release would otherwise wait for them):
@@ -470,6 +478,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             if (l8 == 0 && r < r1 && ok) add_fixed(a.x_mid + r, to_fixed(acc));
         }
     }
+    cluster_wait_all();
 }
 
 // Shared-memory carve-up of the FFN block for at most `units` hidden units.

@@ -341,6 +341,49 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// The same wait with acquire at cluster scope, for phases completed by other
+// CTAs' st.async writes into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          long long limit = kSpinLimitCycles) {
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+
+// Address of `p` (this CTA's shared memory) in the shared memory window of
+// cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_smem(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Non-blocking stores into another CTA's shared memory that count their bytes
+// on that CTA's mbarrier (at `bar`, in the same rank's window).
+__device__ __forceinline__ void st_async_f2(uint32_t addr, float x, float y, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            addr),
+        "f"(x), "f"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void st_async_f1(uint32_t addr, float x, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     addr),
+                 "r"(__float_as_uint(x)), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t make_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
