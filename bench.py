@@ -65,8 +65,10 @@ def parse_args():
                     help="default run: skip the 15m / 44m / 110m batch-1 lines")
     ap.add_argument("--kernel-only", type=int, default=None,
                     help="time one kernel kind (0 QKV, 1 attention, 2 Wo, 3 W1/W3, 4 W2, "
-                         "5 classifier; 6-13 the batched kinds with --workload batched) on "
-                         "the workload's shape and exit: the profiling case")
+                         "5 classifier; 6-13 the batched kinds with --workload batched; "
+                         "14 attention block, 15 FFN block on a two-kernels-per-layer "
+                         "workload: 15m, 44m, 110m) on the workload's shape and exit: the "
+                         "profiling case")
     ap.add_argument("--layers", type=int, default=0,
                     help="with --kernel-only: layers of the reduced-depth model (0 = all)")
     return ap.parse_args()
@@ -687,6 +689,7 @@ def run_small_models(args, world, local):
         blob = synth.make_blob(cfg, w["seed"])
         with l2.Decoder(cfg, blob) as dec:
             del blob
+            layer_kernels = l2.l2_layer_kernels(dec.h)
             stream = torch.cuda.Stream()
             d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
             d_out = torch.zeros(steps, dtype=torch.int32, device="cuda")
@@ -707,7 +710,8 @@ def run_small_models(args, world, local):
                                        "frac": gbs / hbm,
                                        "bytes_per_forward": step_bytes / n_fwd,
                                        "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"},
-                     "kernels_per_forward": 5 * cfg["n_layers"] + 1,
+                     "layer_kernels": layer_kernels,
+                     "kernels_per_forward": layer_kernels * cfg["n_layers"] + 1,
                      "clocks": clocks}
     return out
 

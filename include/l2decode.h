@@ -325,11 +325,19 @@ L2_API const char* l2_last_error(const l2_handle* h);
  * 9 W1/W3 GEMM, 10 W2 GEMM, 11 classifier GEMM + argmax, 12 embedding gather
  * (residual rows, their tf32 pair and sums of squares; the RMSNorms are folded
  * into the GEMMs that consume them),
- * 13 advance. It reads and writes the handle's own run state (the KV cache
+ * 13 advance. Kinds 14 and 15 (handles that run two kernels per layer, see
+ * l2_layer_kernels): 14 the attention block (RMSNorm, Q/K/V, RoPE, KV append,
+ * attention, Wo, residual), 15 the FFN block (RMSNorm, W1/W3, SwiGLU, W2,
+ * residual), at batch 1. It reads and writes the handle's own run state (the KV cache
  * contents are left as they were, except slot `pos` of the caches used).
  * Errors: L2_EINVAL, L2_ECUDA. Synchronous. */
 L2_API int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
                    float* ms);
+
+/* Kernels per layer of the batch-1 forward this handle runs: 5 (Q/K/V, attention,
+ * Wo, W1/W3, W2) or 2 (attention block, FFN block; l2_config.layer_kernels).
+ * 0 for a NULL handle. */
+L2_API int32_t l2_layer_kernels(const l2_handle* h);
 
 /* Algorithmic bytes one launch of `kind` reads and writes at position pos
  * (fp32 weights once + activations + KV rows; batched kinds count max_batch

@@ -8,7 +8,7 @@ l2_generate, l2_generate_device, l2_generate_batch, l2_generate_batch_device,
 l2_generate_batch_sample, l2_generate_batch_sample_device, l2_generate_batch_prefill,
 l2_generate_batch_prefill_device, l2_prefill, l2_generate_prefill, l2_generate_prefill_device, l2_generate_sample,
 l2_generate_sample_device, l2_reset, l2_destroy,
-l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes,
+l2_last_error, l2_blob_floats, l2_time_kernel, l2_kernel_bytes, l2_layer_kernels,
 l2_classify_greedy_noalloc, l2_gemm_tf32x3, l2_status, l2_watchdog_check.
 """
 from __future__ import annotations
@@ -28,7 +28,8 @@ ERROR_NAMES = {L2_EINVAL: "L2_EINVAL", L2_ENOMEM: "L2_ENOMEM", L2_ECUDA: "L2_ECU
 # kinds of l2_time_kernel / l2_kernel_bytes
 KERNEL_KINDS = ("qkv_rope", "attention", "wo_residual", "w13_swiglu", "w2_residual",
                 "classifier_argmax", "b_qkv_gemm", "b_attention", "b_wo_gemm", "b_w13_gemm",
-                "b_w2_gemm", "b_classifier_gemm", "b_embedding", "b_advance")
+                "b_w2_gemm", "b_classifier_gemm", "b_embedding", "b_advance",
+                "attention_block", "ffn_block")
 
 EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward", "l2_forward_device", "l2_generate",
            "l2_generate_device", "l2_generate_batch", "l2_generate_batch_device",
@@ -36,7 +37,8 @@ EXPORTS = ("l2_blob_floats", "l2_create", "l2_create_from_device", "l2_forward",
            "l2_generate_batch_prefill", "l2_generate_batch_prefill_device", "l2_prefill",
            "l2_generate_prefill", "l2_generate_prefill_device", "l2_generate_sample",
            "l2_generate_sample_device", "l2_reset", "l2_destroy",
-           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_classify_greedy_noalloc",
+           "l2_last_error", "l2_time_kernel", "l2_kernel_bytes", "l2_layer_kernels",
+           "l2_classify_greedy_noalloc",
            "l2_gemm_tf32x3", "l2_status", "l2_watchdog_check")
 
 L2_NOALLOC_MAX_VOCAB = 262144
@@ -93,6 +95,7 @@ _SIG = {
     "l2_last_error": (ctypes.c_char_p, [_P]),
     "l2_time_kernel": (ctypes.c_int, [_P, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_float)]),
     "l2_kernel_bytes": (ctypes.c_double, [_P, _I, _I]),
+    "l2_layer_kernels": (ctypes.c_int32, [_P]),
     "l2_gemm_tf32x3": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_float),
                                       _P]),
     "l2_classify_greedy_noalloc": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P, _P,
@@ -306,6 +309,10 @@ def l2_time_kernel(h, kind: int, pos: int, iters: int, stream=None) -> float:
 
 def l2_kernel_bytes(h, kind: int, pos: int) -> float:
     return float(_lib.l2_kernel_bytes(h, kind, pos))
+
+
+def l2_layer_kernels(h) -> int:
+    return int(_lib.l2_layer_kernels(h))
 
 
 def l2_gemm_tf32x3(d_A, d_W, d_C, M: int, N: int, K: int, iters: int = 0, stream=None):

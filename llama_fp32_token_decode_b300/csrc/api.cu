@@ -194,9 +194,17 @@ MatvecArgs base_args(l2_handle* h) {
 }
 
 // Launches kernel `kind` of layer l on stream s (kind as in l2_time_kernel).
+void fused_layer_args(const l2_handle* h, size_t l, FAttnArgs* a, FFfnArgs* f);
+
 cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, kvd = h->kvd;
+    if (kind == 14 || kind == 15) {  // the two-kernels-per-layer blocks
+        FAttnArgs fa;
+        FFfnArgs ff;
+        fused_layer_args(h, static_cast<size_t>(l), &fa, &ff);
+        return kind == 14 ? launch_fattn(fa, s, true) : launch_fffn(ff, h->ffn_grid, s, true);
+    }
     MatvecArgs a = base_args(h);
     switch (kind) {
         case 0:
@@ -257,35 +265,42 @@ cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
 
 // Two kernels per layer: the attention block and the FFN block, the residual
 // in fixed point (P[l % 2] enters layer l, M[l % 2] after its attention).
-cudaError_t enqueue_forward_fused(l2_handle* h, cudaStream_t s) {
+void fused_layer_args(const l2_handle* h, size_t l, FAttnArgs* a, FFfnArgs* f) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, kvd = h->kvd, L = c.n_layers;
     long long* P[2] = {h->fx, h->fx + d};
     long long* M[2] = {h->fx + 2 * d, h->fx + 3 * d};
-    const float* wo_h = h->fw;
-    const float* w2t = h->fw + L * d * d;
+    *a = h->fattn;
+    a->wqkv = h->wqkv + l * (d + 2 * kvd) * d;
+    a->wo_h = h->fw + l * d * d;
+    a->g_att = h->g_att + l * d;
+    a->x_in = l == 0 ? nullptr : P[l % 2];
+    a->x_mid = M[l % 2];
+    a->x_zero = P[(l + 1) % 2];
+    a->k_cache = h->k_cache + l * h->cache_layer;
+    a->v_cache = h->v_cache + l * h->cache_layer;
+    *f = h->fffn;
+    f->w13 = h->w13 + l * 2 * F * d;
+    f->w2t = h->fw + L * d * d + l * F * d;
+    f->g_ffn = h->g_ffn + l * d;
+    f->x_mid = M[l % 2];
+    f->x_out = P[(l + 1) % 2];
+    f->x_zero = M[(l + 1) % 2];
+}
+
+cudaError_t enqueue_forward_fused(l2_handle* h, cudaStream_t s) {
+    const size_t d = h->cfg.dim, L = h->cfg.n_layers;
     for (size_t l = 0; l < L; ++l) {
-        FAttnArgs a = h->fattn;
-        a.wqkv = h->wqkv + l * (d + 2 * kvd) * d;
-        a.wo_h = wo_h + l * d * d;
-        a.g_att = h->g_att + l * d;
-        a.x_in = l == 0 ? nullptr : P[l % 2];
-        a.x_mid = M[l % 2];
-        a.x_zero = P[(l + 1) % 2];
-        a.k_cache = h->k_cache + l * h->cache_layer;
-        a.v_cache = h->v_cache + l * h->cache_layer;
+        FAttnArgs a;
+        FFfnArgs f;
+        fused_layer_args(h, l, &a, &f);
         cudaError_t e = launch_fattn(a, s, true);
         if (e != cudaSuccess) return e;
-        FFfnArgs f = h->fffn;
-        f.w13 = h->w13 + l * 2 * F * d;
-        f.w2t = w2t + l * F * d;
-        f.g_ffn = h->g_ffn + l * d;
-        f.x_mid = M[l % 2];
-        f.x_out = P[(l + 1) % 2];
-        f.x_zero = M[(l + 1) % 2];
         if ((e = launch_fffn(f, h->ffn_grid, s, true)) != cudaSuccess) return e;
     }
     // classifier on the last residual; it also clears the next forward's M[0]
+    long long* P[2] = {h->fx, h->fx + d};
+    long long* M0 = h->fx + 2 * d;
     MatvecArgs a = base_args(h);
     a.W = h->wcls;
     a.plan = h->p_cls;
@@ -293,7 +308,7 @@ cudaError_t enqueue_forward_fused(l2_handle* h, cudaStream_t s) {
     a.src_fixed = P[L % 2];
     a.gain = h->g_final;
     a.out = h->logits;
-    a.zero_fixed = M[0];
+    a.zero_fixed = M0;
     a.zero_n = static_cast<int>(d);
     return launch_matvec(EPI_CLASSIFIER, a, s, true);
 }
@@ -1606,12 +1621,14 @@ int l2_generate_batch_sample_device(l2_handle* h, const int32_t* d_prompts, cons
 int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void* stream,
                    float* ms) {
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
-    if (kind < 0 || kind > 13 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
+    if (kind < 0 || kind > 15 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
         return fail(h, L2_EINVAL, "bad kind, iters, pos or output");
-    if (kind >= 6 && h->cfg.max_batch < 2)
+    if (kind >= 6 && kind <= 13 && h->cfg.max_batch < 2)
         return fail(h, L2_EINVAL, "batched kernel kinds need a handle with max_batch > 1");
+    if (kind >= 14 && !h->fused)
+        return fail(h, L2_EINVAL, "kinds 14 and 15 need a handle with two kernels per layer");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (kind >= 6) {
+    if (kind >= 6 && kind <= 13) {
         const int M = h->cfg.max_batch, bk = kind - 6;
         L2_CUDA(h, clear_device_error(h, s));
         bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
@@ -1636,10 +1653,14 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
     L2_CUDA(h, cudaEventRecord(h->ev0, s));
     for (int i = 0; i < iters; ++i) L2_CUDA(h, launch_kind(h, kind, i % h->cfg.n_layers, s));
     L2_CUDA(h, cudaEventRecord(h->ev1, s));
+    // a forward starts from zeroed fixed-point residual buffers
+    if (kind >= 14)
+        L2_CUDA(h, cudaMemsetAsync(h->fx, 0, 4 * h->cfg.dim * sizeof(long long), s));
     L2_CUDA(h, cudaEventSynchronize(h->ev1));
     float t = 0.0f;
     L2_CUDA(h, cudaEventElapsedTime(&t, h->ev0, h->ev1));
     *ms = t / iters;
+    L2_CUDA(h, cudaStreamSynchronize(s));
     return check_device_error(h);
 }
 
@@ -1668,6 +1689,8 @@ int l2_watchdog_check(l2_handle* h, int64_t spin_cycles) {
     return status_of(h, err);
 }
 
+int32_t l2_layer_kernels(const l2_handle* h) { return h ? (h->fused ? 2 : 5) : 0; }
+
 double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
     if (!h) return 0.0;
     const double d = h->cfg.dim, F = h->cfg.hidden_dim, V = h->cfg.vocab_size, kvd = h->kvd;
@@ -1678,6 +1701,11 @@ double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
         case 3: return 4.0 * (2 * F * d + 2 * d + F);
         case 4: return 4.0 * (d * F + F + 2 * d);
         case 5: return 4.0 * (V * d + 2 * d + V);
+        // the two-kernels-per-layer blocks: weights once, the KV rows once per
+        // kv head, the residual in and out in 8-byte fixed point
+        case 14: return 4.0 * ((d + 2 * kvd) * d + d * d + 2.0 * (pos + 1) * kvd + 2 * kvd + d) +
+                        8.0 * 3 * d;
+        case 15: return 4.0 * (3 * F * d + d) + 8.0 * 3 * d;
         default: break;
     }
     // batched kinds: fp32 operands once (weights, input rows), outputs, KV rows

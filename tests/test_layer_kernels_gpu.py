@@ -76,4 +76,18 @@ def test_two_kernel_path_is_taken_and_rejected_where_it_does_not_fit(l2):
     # the same shape with the default choice falls back to five kernels
     cfg["layer_kernels"] = 0
     with l2.Decoder(cfg, synth.make_blob(cfg, 1, std=0.05)) as dec:
+        assert l2.l2_layer_kernels(dec.h) == 5
         assert np.all(np.isfinite(dec.forward([3], [0])[0]))
+        with pytest.raises(l2.L2Error) as e:  # the block kinds need the two-kernel path
+            l2.l2_time_kernel(dec.h, 14, 0, 1)
+        assert e.value.code == l2.L2_EINVAL
+    # a shape that fits takes two kernels by default; its blocks time alone
+    cfg = dict(SHAPES["gqa"])
+    with l2.Decoder(cfg, synth.make_blob(cfg, 1, std=0.05)) as dec:
+        assert l2.l2_layer_kernels(dec.h) == 2
+        before = dec.forward([3], [0])[0]
+        for kind in (14, 15):
+            assert l2.l2_time_kernel(dec.h, kind, 5, 3) > 0.0
+            assert l2.l2_kernel_bytes(dec.h, kind, 5) > 0.0
+        # the timing launches leave nothing behind that a forward reads
+        np.testing.assert_array_equal(dec.forward([3], [0])[0], before)
