@@ -65,7 +65,8 @@ def parse_args():
                     help="default run: skip the 15m / 44m / 110m batch-1 lines")
     ap.add_argument("--kernel-only", type=int, default=None,
                     help="time one kernel kind (0 QKV, 1 attention, 2 Wo, 3 W1/W3, 4 W2, "
-                         "5 classifier; 6-13 the batched kinds with --workload batched; "
+                         "5 classifier; 6-13 the batched kinds with --workload batched "
+                         "(8-10 with --workload 7b: the prefill pass's GEMMs on its 64 rows); "
                          "14 attention block, 15 FFN block on a two-kernels-per-layer "
                          "workload: 15m, 44m, 110m) on the workload's shape and exit: the "
                          "profiling case")
@@ -897,6 +898,9 @@ def run_kernel_only(args):
     cfg = synth.model_config(w)
     if args.layers:
         cfg["n_layers"] = args.layers
+    if args.workload == "7b" and args.kernel_only in (8, 9, 10):
+        # the GEMMs of the 7B prefill pass: its prompt's rows, one KV cache
+        cfg["max_prefill"] = w["n_prompt"]
     # a short cache keeps the case to a few GB (batched: 256 caches)
     cfg["seq_len"] = min(cfg["seq_len"], 384 if cfg.get("max_batch", 1) > 1 else 512)
     blob = synth.make_blob(cfg, w["seed"])

@@ -325,7 +325,9 @@ L2_API const char* l2_last_error(const l2_handle* h);
  * 9 W1/W3 GEMM, 10 W2 GEMM, 11 classifier GEMM + argmax, 12 embedding gather
  * (residual rows, their tf32 pair and sums of squares; the RMSNorms are folded
  * into the GEMMs that consume them),
- * 13 advance. Kinds 14 and 15 (handles that run two kernels per layer, see
+ * 13 advance; a handle with max_batch 1 and max_prefill > 1 times kinds
+ * 8-10 (the GEMMs that touch no KV cache) on its max_prefill rows, the GEMMs of
+ * a prefill pass. Kinds 14 and 15 (handles that run two kernels per layer, see
  * l2_layer_kernels): 14 the attention block (RMSNorm, Q/K/V, RoPE, KV append,
  * attention, Wo, residual), 15 the FFN block (RMSNorm, W1/W3, SwiGLU, W2,
  * residual), at batch 1. It reads and writes the handle's own run state (the KV cache

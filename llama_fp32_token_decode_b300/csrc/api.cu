@@ -1623,13 +1623,16 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
     if (!h) return fail(nullptr, L2_EINVAL, "handle is NULL");
     if (kind < 0 || kind > 15 || iters < 1 || !ms || pos < 0 || pos >= h->cfg.seq_len)
         return fail(h, L2_EINVAL, "bad kind, iters, pos or output");
-    if (kind >= 6 && kind <= 13 && h->cfg.max_batch < 2)
+    // a prefill-only handle (max_batch 1, max_prefill > 1) times the GEMMs that
+    // touch no KV cache (Wo, W1/W3, W2) on its max_prefill rows
+    const bool prefill_gemm = kind >= 8 && kind <= 10 && h->cfg.max_batch < 2 && h->rows > 1;
+    if (kind >= 6 && kind <= 13 && h->cfg.max_batch < 2 && !prefill_gemm)
         return fail(h, L2_EINVAL, "batched kernel kinds need a handle with max_batch > 1");
     if (kind >= 14 && !h->fused)
         return fail(h, L2_EINVAL, "kinds 14 and 15 need a handle with two kernels per layer");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kind >= 6 && kind <= 13) {
-        const int M = h->cfg.max_batch, bk = kind - 6;
+        const int M = prefill_gemm ? h->rows : h->cfg.max_batch, bk = kind - 6;
         L2_CUDA(h, clear_device_error(h, s));
         bset_kernel<<<(M + 127) / 128, 128, 0, s>>>(M, pos, h->b_pos, h->b_token, h->b_active,
                                                     h->b_keys, h->st);
@@ -1709,7 +1712,8 @@ double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
         default: break;
     }
     // batched kinds: fp32 operands once (weights, input rows), outputs, KV rows
-    const double M = h->cfg.max_batch;
+    const bool prefill_gemm = kind >= 8 && kind <= 10 && h->cfg.max_batch < 2 && h->rows > 1;
+    const double M = prefill_gemm ? h->rows : h->cfg.max_batch;
     if (kind >= 6 && M < 2) return 0.0;
     switch (kind) {
         case 6: return 4.0 * ((d + 2 * kvd) * d + M * d + M * (d + 2 * kvd));

@@ -53,6 +53,7 @@ namespace {
 constexpr int kFThreads = 256;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int G8 = kFusedCluster;
+static_assert(G8 <= kFThreads, "one thread per partial forms its factor");
 
 __device__ __forceinline__ long long to_fixed(float v) {
     return __float2ll_rn(v * 4294967296.0f);
@@ -203,6 +204,8 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     __shared__ __align__(8) uint64_t wbar;
     __shared__ __align__(8) uint64_t qbar;  // q, k, v rows from the cluster's CTAs
     __shared__ __align__(8) uint64_t pbar;  // the 8 attention partials
+    __shared__ float s_fac[kFWarps + 1];    // the warps' softmax rescale factors, and M
+    __shared__ float s_mfac[G8];            // the partials' rescale factors
     __shared__ int s_fail;
 
     // this CTA's slices
@@ -348,7 +351,9 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             }
             if (gmax == -INFINITY) continue;
             const float mnew = fmaxf(m, gmax);
-            const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+            // __expf: the SFU exponential, within a few ulp for these
+            // non-positive arguments, as close as the fp32 sums it weights
+            const float corr = (m == -INFINITY) ? 0.0f : __expf(m - mnew);
             l *= corr;
             o.x *= corr;
             o.y *= corr;
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             o.w *= corr;
 #pragma unroll
             for (int g = 0; g < GR; ++g) {
-                const float pe = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+                const float pe = (sc[g] == -INFINITY) ? 0.0f : __expf(sc[g] - mnew);
                 l += pe;
                 o.x = fmaf(pe, vr[g].x, o.x);
                 o.y = fmaf(pe, vr[g].y, o.y);
@@ -375,8 +380,8 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             o2.z = __shfl_xor_sync(0xffffffffu, o.z, off);
             o2.w = __shfl_xor_sync(0xffffffffu, o.w, off);
             const float M = fmaxf(m, m2);
-            const float f1 = (m == -INFINITY) ? 0.0f : expf(m - M);
-            const float f2 = (m2 == -INFINITY) ? 0.0f : expf(m2 - M);
+            const float f1 = (m == -INFINITY) ? 0.0f : __expf(m - M);
+            const float f2 = (m2 == -INFINITY) ? 0.0f : __expf(m2 - M);
             l = l * f1 + l2v * f2;
             o.x = o.x * f1 + o2.x * f2;
             o.y = o.y * f1 + o2.y * f2;
@@ -391,15 +396,23 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
             wp[hd + 1] = l;
         }
         __syncthreads();
-        // the CTA's partial, sent to every CTA of the cluster (slot j)
-        float M = -INFINITY;
-        for (int w = 0; w < kFWarps; ++w) M = fmaxf(M, red[w * pstride + hd]);
+        // the CTA's partial, sent to every CTA of the cluster (slot j); the
+        // warps' rescale factors exp(m_w - M) are formed once, by 8 threads
+        if (tid < kFWarps) {
+            float M = -INFINITY;
+            for (int w = 0; w < kFWarps; ++w) M = fmaxf(M, red[w * pstride + hd]);
+            const float mw = red[tid * pstride + hd];
+            s_fac[tid] = (mw == -INFINITY) ? 0.0f : __expf(mw - M);
+            if (tid == 0) s_fac[kFWarps] = M;
+        }
+        __syncthreads();
+        const float M = s_fac[kFWarps];
         for (int e = tid; e < hd + 2; e += kFThreads) {
             float acc = 0.0f;
             for (int w = 0; w < kFWarps; ++w) {
-                const float mw = red[w * pstride + hd];
-                if (mw == -INFINITY) continue;
-                acc += (e < hd ? red[w * pstride + e] : red[w * pstride + hd + 1]) * expf(mw - M);
+                const float fw = s_fac[w];
+                if (fw != 0.0f)
+                    acc += (e < hd ? red[w * pstride + e] : red[w * pstride + hd + 1]) * fw;
             }
             const float val = (e == hd) ? M : acc;
             for (int q2 = 0; q2 < G8; ++q2)
@@ -434,19 +447,21 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     // ---- merge the partials into att_h (in xs: x is no longer needed)
     float* att = xs;
     {
-        float Mg = -INFINITY;
-        for (int q2 = 0; q2 < G8; ++q2) Mg = fmaxf(Mg, part[q2 * pstride + hd]);
-        float Lg = 0.0f;
-        for (int q2 = 0; q2 < G8; ++q2) {
-            const float mq = part[q2 * pstride + hd];
-            if (mq != -INFINITY) Lg += part[q2 * pstride + hd + 1] * expf(mq - Mg);
+        // the partials' rescale factors exp(m_q - max m), formed once
+        if (tid < G8) {
+            float Mg = -INFINITY;
+            for (int q2 = 0; q2 < G8; ++q2) Mg = fmaxf(Mg, part[q2 * pstride + hd]);
+            const float mq = part[tid * pstride + hd];
+            s_mfac[tid] = (mq == -INFINITY) ? 0.0f : expf(mq - Mg);
         }
+        __syncthreads();
+        float Lg = 0.0f;
+        for (int q2 = 0; q2 < G8; ++q2)
+            if (s_mfac[q2] != 0.0f) Lg += part[q2 * pstride + hd + 1] * s_mfac[q2];
         for (int e = tid; e < hd; e += kFThreads) {
             float acc = 0.0f;
-            for (int q2 = 0; q2 < G8; ++q2) {
-                const float mq = part[q2 * pstride + hd];
-                if (mq != -INFINITY) acc += part[q2 * pstride + e] * expf(mq - Mg);
-            }
+            for (int q2 = 0; q2 < G8; ++q2)
+                if (s_mfac[q2] != 0.0f) acc += part[q2 * pstride + e] * s_mfac[q2];
             att[e] = acc / Lg;
         }
     }
