@@ -50,10 +50,12 @@ namespace l2 {
 
 namespace {
 
-constexpr int kFThreads = 256;
-constexpr int kFWarps = kFThreads / 32;
+constexpr int kFAttnThreads = 512;  // attention block: 16 warps
+constexpr int kFAttnWarps = kFAttnThreads / 32;
+constexpr int kFFfnThreads = 512;   // FFN block
+constexpr int kFFfnWarps = kFFfnThreads / 32;
 constexpr int G8 = kFusedCluster;
-static_assert(G8 <= kFThreads, "one thread per partial forms its factor");
+static_assert(G8 <= kFAttnThreads, "one thread per partial forms its factor");
 
 __device__ __forceinline__ long long to_fixed(float v) {
     return __float2ll_rn(v * 4294967296.0f);
@@ -83,7 +85,7 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     L.off_qkv = L.off_x + ((d + 3) & ~3);
     L.off_part = L.off_qkv + ((3 * hd + 3) & ~3);
     L.off_red = L.off_part + G8 * ((hd + 2 + 3) & ~3);
-    L.off_g = L.off_red + kFWarps * ((hd + 2 + 3) & ~3) + 64;
+    L.off_g = L.off_red + kFAttnWarps * ((hd + 2 + 3) & ~3) + 64;
     L.off_c = L.off_g + ((d + 3) & ~3);                         // carried rows, 8 bytes each
     L.off_rs = L.off_c + 2 * ((d / G8 + 1 + 3) & ~3);           // RoPE pairs of the rows
     L.total = L.off_rs + 2 * ((L.rows_qkv / 2 + 3) & ~3);
@@ -96,18 +98,19 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
 // are also added into `carry` and cleared in `zero` from the same loads, or,
 // with `stash`, kept there in fixed point for the caller to add later.
 constexpr int kRowRegs = 4;
+template <int NT>
 __device__ __forceinline__ float norm_load(float* xs, const float* src, const long long* srcf,
                                            int d, float eps, float* red, long long* carry,
                                            long long* zero, int c0, int c1,
                                            long long* stash = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float ss = 0.0f;
-    for (int base = 0; base < d; base += kRowRegs * kFThreads) {
+    for (int base = 0; base < d; base += kRowRegs * NT) {
         long long fx[kRowRegs];
         float v[kRowRegs];
 #pragma unroll
         for (int k = 0; k < kRowRegs; ++k) {
-            const int i = base + k * kFThreads + tid;
+            const int i = base + k * NT + tid;
             fx[k] = 0;
             v[k] = 0.0f;
             if (i < d) {
@@ -117,7 +120,7 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
         }
 #pragma unroll
         for (int k = 0; k < kRowRegs; ++k) {
-            const int i = base + k * kFThreads + tid;
+            const int i = base + k * NT + tid;
             if (i < d) {
                 if (srcf) v[k] = from_fixed(fx[k]);
                 xs[i] = v[k];
@@ -137,15 +140,16 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
-    float t = lane < kFWarps ? red[lane] : 0.0f;  // every warp forms the same total
+    float t = lane < NT / 32 ? red[lane] : 0.0f;  // every warp forms the same total
     t = warp_sum(t);
     return 1.0f / sqrtf(t / static_cast<float>(d) + eps);
 }
 
 // Second half: xs = g * (inv * x), g in shared memory. Each thread scales the
 // elements it loaded, so only the barrier after it is needed.
+template <int NT>
 __device__ __forceinline__ void norm_scale(float* xs, const float* g, float inv, int d) {
-    for (int i = threadIdx.x; i < d; i += kFThreads) xs[i] = g[i] * (inv * xs[i]);
+    for (int i = threadIdx.x; i < d; i += NT) xs[i] = g[i] * (inv * xs[i]);
     __syncthreads();
 }
 
@@ -179,7 +183,7 @@ __device__ __forceinline__ float2 warp_dot2(const float* w0, const float* w1, co
 
 // LPR lanes read one 16-byte-vectorised cache row (head_dim <= 4 LPR).
 template <int LPR>
-__global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant__ FAttnArgs a) {
+__global__ void __launch_bounds__(kFAttnThreads) fattn_kernel(const __grid_constant__ FAttnArgs a) {
     constexpr int RPW = 32 / LPR;  // rows per warp load
     constexpr int GR = 4;          // row slots per lane group and iteration
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     __shared__ __align__(8) uint64_t wbar;
     __shared__ __align__(8) uint64_t qbar;  // q, k, v rows from the cluster's CTAs
     __shared__ __align__(8) uint64_t pbar;  // the 8 attention partials
-    __shared__ float s_fac[kFWarps + 1];    // the warps' softmax rescale factors, and M
+    __shared__ float s_fac[kFAttnWarps + 1];    // the warps' softmax rescale factors, and M
     __shared__ float s_mfac[G8];            // the partials' rescale factors
     __shared__ int s_fail;
 
@@ -262,13 +266,13 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     // RoPE (cos, sin) of this CTA's q and k pairs, loaded beside x
     const int half = hd >> 1;
     const float2* rope = a.rope + static_cast<size_t>(pos) * half;
-    for (int p = tid; 2 * p < t1 - t0; p += kFThreads) {
+    for (int p = tid; 2 * p < t1 - t0; p += kFAttnThreads) {
         const int tg = t0 + 2 * p;
         if (tg < 2 * hd) rs[p] = __ldg(rope + ((tg < hd ? tg : tg - hd) >> 1));
     }
     // head 0's CTAs keep their rows of the residual, added into x_mid once the
     // cluster barriers are behind them
-    const float inv = norm_load(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
+    const float inv = norm_load<kFAttnThreads>(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
                                 h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(&st->err, ERR_TIMEOUT_TMA);
@@ -279,12 +283,12 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     const bool ok = s_fail == 0;  // on a timeout the exchange still runs (every CTA
                                   // takes the cluster barriers), with zero rows
     if (!ok)
-        for (int i = tid; i < d; i += kFThreads) gs[i] = 0.0f;
-    norm_scale(xs, gs, inv, d);
+        for (int i = tid; i < d; i += kFAttnThreads) gs[i] = 0.0f;
+    norm_scale<kFAttnThreads>(xs, gs, inv, d);
 
     // ---- Q/K/V rows of this CTA (pairs per warp: RoPE needs both)
     cluster_wait_all();  // every CTA of the cluster runs: remote writes allowed
-    for (int p = warp; 2 * p < t1 - t0; p += kFWarps) {
+    for (int p = warp; 2 * p < t1 - t0; p += kFAttnWarps) {
         const int tl = 2 * p, tg = t0 + tl;  // even: a pair never straddles q/k/v
         float v0 = 0.0f, v1 = 0.0f;
         if (ok) {
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         float m = -INFINITY, l = 0.0f;
         float4 o = z;
         constexpr int PER_IT = GR * RPW;
-        for (int tb = s0 + warp * PER_IT; tb < s1; tb += kFWarps * PER_IT) {
+        for (int tb = s0 + warp * PER_IT; tb < s1; tb += kFAttnWarps * PER_IT) {
             float4 kr[GR], vr[GR];
 #pragma unroll
             for (int g = 0; g < GR; ++g) {
@@ -398,18 +402,18 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         __syncthreads();
         // the CTA's partial, sent to every CTA of the cluster (slot j); the
         // warps' rescale factors exp(m_w - M) are formed once, by 8 threads
-        if (tid < kFWarps) {
+        if (tid < kFAttnWarps) {
             float M = -INFINITY;
-            for (int w = 0; w < kFWarps; ++w) M = fmaxf(M, red[w * pstride + hd]);
+            for (int w = 0; w < kFAttnWarps; ++w) M = fmaxf(M, red[w * pstride + hd]);
             const float mw = red[tid * pstride + hd];
             s_fac[tid] = (mw == -INFINITY) ? 0.0f : __expf(mw - M);
-            if (tid == 0) s_fac[kFWarps] = M;
+            if (tid == 0) s_fac[kFAttnWarps] = M;
         }
         __syncthreads();
-        const float M = s_fac[kFWarps];
-        for (int e = tid; e < hd + 2; e += kFThreads) {
+        const float M = s_fac[kFAttnWarps];
+        for (int e = tid; e < hd + 2; e += kFAttnThreads) {
             float acc = 0.0f;
-            for (int w = 0; w < kFWarps; ++w) {
+            for (int w = 0; w < kFAttnWarps; ++w) {
                 const float fw = s_fac[w];
                 if (fw != 0.0f)
                     acc += (e < hd ? red[w * pstride + e] : red[w * pstride + hd + 1]) * fw;
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     // the carried residual rows, and this position's k and v, appended by the
     // first cluster of each kv head, 1/8 of the 2 hd values per CTA
     if (h == 0) {
-        for (int r = r0 + tid; r < r1; r += kFThreads) {
+        for (int r = r0 + tid; r < r1; r += kFAttnThreads) {
             add_fixed(a.x_mid + r, cst[r - r0]);
             a.x_zero[r] = 0;
         }
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         float* kc = a.k_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
         float* vc = a.v_cache + (static_cast<size_t>(kvh) * a.S + slot_cur) * hd;
         const int e0 = 2 * hd * j / G8, e1 = 2 * hd * (j + 1) / G8;
-        for (int e = e0 + tid; e < e1; e += kFThreads) {
+        for (int e = e0 + tid; e < e1; e += kFAttnThreads) {
             if (e < hd) kc[e] = qkv[hd + e];
             else vc[e - hd] = qkv[hd + e];
         }
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
         float Lg = 0.0f;
         for (int q2 = 0; q2 < G8; ++q2)
             if (s_mfac[q2] != 0.0f) Lg += part[q2 * pstride + hd + 1] * s_mfac[q2];
-        for (int e = tid; e < hd; e += kFThreads) {
+        for (int e = tid; e < hd; e += kFAttnThreads) {
             float acc = 0.0f;
             for (int q2 = 0; q2 < G8; ++q2)
                 if (s_mfac[q2] != 0.0f) acc += part[q2 * pstride + e] * s_mfac[q2];
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kFThreads) fattn_kernel(const __grid_constant_
     {
         const int sub = lane >> 3, l8 = lane & 7, hd4 = hd >> 2;
         const float4* a4 = reinterpret_cast<const float4*>(att);
-        for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * kFWarps) {
+        for (int rb = r0 + 4 * warp; rb < r1; rb += 4 * kFAttnWarps) {
             const int r = rb + sub;
             float acc = 0.0f;
             if (r < r1) {
@@ -512,7 +516,7 @@ __host__ __device__ inline FFfnLayout fffn_layout(int d, int units) {
     return L;
 }
 
-__global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__ FFfnArgs f) {
+__global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constant__ FFfnArgs f) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float* sm = reinterpret_cast<float*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__
     // rows split over the CTAs
     const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
     const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
-    const float inv = norm_load(xs, nullptr, f.x_mid, d, f.eps, red, f.x_out, f.x_zero, q0, q1);
+    const float inv = norm_load<kFFfnThreads>(xs, nullptr, f.x_mid, d, f.eps, red, f.x_out, f.x_zero, q0, q1);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(f.err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -568,17 +572,17 @@ __global__ void __launch_bounds__(kFThreads) fffn_kernel(const __grid_constant__
     }
     __syncthreads();
     if (s_fail || nu == 0) return;
-    norm_scale(xs, gs, inv, d);
+    norm_scale<kFFfnThreads>(xs, gs, inv, d);
 
     // SwiGLU of the CTA's hidden units (interleaved rows: 2u gate, 2u + 1 up)
-    for (int u = warp; u < nu; u += kFWarps) {
+    for (int u = warp; u < nu; u += kFFfnWarps) {
         const float2 gu = warp_dot2(w13 + static_cast<size_t>(2 * u) * d,
                                     w13 + static_cast<size_t>(2 * u + 1) * d, xs, d, lane);
         if (lane == 0) hb[u] = (gu.x / (1.0f + expf(-gu.x))) * gu.y;
     }
     __syncthreads();
     // their contribution to every output: y[i] = sum_u W2[i][u0 + u] hb[u]
-    for (int i = tid; i < d; i += kFThreads) {
+    for (int i = tid; i < d; i += kFFfnThreads) {
         float acc = 0.0f;
         for (int u = 0; u < nu; ++u) acc = fmaf(w2t[static_cast<size_t>(u) * d + i], hb[u], acc);
         add_fixed(f.x_out + i, to_fixed(acc));
@@ -618,7 +622,7 @@ cudaError_t prepare_fused(const FAttnArgs& a, const FFfnArgs& f) {
 cudaError_t launch_fattn(const FAttnArgs& a, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G8, a.H);
-    cfg.blockDim = dim3(kFThreads);
+    cfg.blockDim = dim3(kFAttnThreads);
     cfg.dynamicSmemBytes = a.smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -637,7 +641,7 @@ cudaError_t launch_fattn(const FAttnArgs& a, cudaStream_t s, bool pdl) {
 cudaError_t launch_fffn(const FFfnArgs& f, int grid, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kFThreads);
+    cfg.blockDim = dim3(kFFfnThreads);
     cfg.dynamicSmemBytes = f.smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
