@@ -7,7 +7,9 @@ rows, attention, its share of Wo) and an FFN block (W1/W3, SwiGLU and W2 per
 hidden-unit slice), the residual kept in 64-bit fixed point. Both compute the
 same step; each must match the oracle under teacher forcing (logits within
 relative L2 1e-4), generate the oracle's tokens up to its first near-tie, and
-leave a KV cache that the other path's forwards can continue from.
+leave a KV cache that the other path's forwards can continue from. The long
+shapes spread each CTA's share of the cache over several of its warps, whose
+partials the CTA combines before the cluster's exchange.
 """
 import numpy as np
 import pytest
@@ -38,6 +40,12 @@ SHAPES = {
                                seq_len=40),
     "rolling": config(dim=128, hidden_dim=344, n_layers=2, n_heads=8, n_kv_heads=2,
                       vocab_size=3001, seq_len=16, rolling_positions=56, rolling_cache=1),
+    # up to 25 / 13 cache slots per CTA of a head's cluster: several warps'
+    # partials per CTA (8 slots a warp at head_dim <= 64, 4 at 128)
+    "gqa_long": config(dim=128, hidden_dim=344, n_layers=2, n_heads=8, n_kv_heads=2,
+                       vocab_size=3000, seq_len=200),
+    "hd128_long": config(dim=512, hidden_dim=1376, n_layers=1, n_heads=4, vocab_size=1000,
+                         seq_len=100),
 }
 
 
