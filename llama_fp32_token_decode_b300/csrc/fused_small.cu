@@ -183,7 +183,10 @@ __device__ __forceinline__ float2 warp_dot2(const float* w0, const float* w1, co
 
 // LPR lanes read one 16-byte-vectorised cache row (head_dim <= 4 LPR).
 template <int LPR>
-__global__ void __launch_bounds__(kFAttnThreads) fattn_kernel(const __grid_constant__ FAttnArgs a) {
+// 80 registers: with the FFN block's 48 at the same thread count, an FFN CTA
+// fits on an SM beside an attention CTA (where shared memory allows) and
+// starts, copying its weights, while the attention block runs.
+__global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a) {
     constexpr int RPW = 32 / LPR;  // rows per warp load
     constexpr int GR = 4;          // row slots per lane group and iteration
     extern __shared__ __align__(128) unsigned char smem_raw[];
