@@ -15,7 +15,8 @@
 //     with 3-D TMA tile loads (completion on mbarriers); weight tiles of the
 //     first stages are requested before griddepcontrol.wait, since weights
 //     never depend on the previous kernel;
-//   * warp 1 lane 0 issues tcgen05.mma kind::tf32 (M 128, N BN, K 8) from the
+//   * warp 1 lane 0 issues tcgen05.mma kind::tf32 (M 128, or 64 for launches of
+//     at most 64 rows; N BN, K 8) from the
 //     stages into a TMEM accumulator (128 lanes x BN fp32 columns) and frees
 //     each stage with tcgen05.commit; idle warps meanwhile stage per-row data
 //     the epilogue needs (row positions, RMSNorm row scales);
@@ -426,9 +427,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     using C = Cfg<BN>;
     const int S = g.stages;       // ring depth of this launch
     constexpr int PS = C::PS;     // row stride of the staged partial (floats)
-    // A tiles of g.a_rows rows (128, or 64: the MMA then reads rows 64-127 of
-    // each A operand from the slot after it, garbage that only reaches output
-    // rows at or beyond m_end, which are never written)
+    // A tiles of g.a_rows rows (128, or 64 with M = 64 MMAs: launches of at
+    // most 64 rows)
     const int a_bytes = (g.a_rows == 64 ? 64 : 128) * C::BK * 4;
     const int stage_b = 2 * a_bytes + 2 * C::B_BYTES;
     extern __shared__ unsigned char smem_raw[];
@@ -538,8 +538,9 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         }
     } else if (warp == kMmaWarp && (DRAIN || lane == 0)) {
         if (lane == 0) {
-            // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1
-            constexpr uint32_t idesc = idesc_tf32(128, BN);
+            // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1; 64-row
+            // A tiles take M = 64 MMAs (half the tensor work and A reads)
+            const uint32_t idesc = g.a_rows == 64 ? idesc_tf32(64, BN) : idesc_tf32(128, BN);
             for (int i = 0; i < NK; ++i) {
                 const int c = i / CH, w = i % CH, buf = c & 1;
                 if (w == 0 && c >= 2 &&
@@ -630,7 +631,11 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     constexpr int kHalves = DRAIN ? 1 : NT / 128;
     const int half = DRAIN ? 0 : (warp >> 2);
     const bool reader = DRAIN ? (warp < 4) : true;
-    const int row = 32 * (warp & 3) + lane;  // this reader's tile row
+    // this reader's tile row: an M = 128 accumulator keeps row i in TMEM lane
+    // i; an M = 64 one keeps rows 16 q .. 16 q + 15 in the first 16 lanes of
+    // lane quarter q (-1: a lane that holds no row)
+    const int TR = g.a_rows == 64 ? 64 : 128;  // rows of the tile
+    const int row = TR == 128 ? 32 * (warp & 3) + lane : (lane < 16 ? 16 * (warp & 3) + lane : -1);
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     auto rstate = [&](int lr) {
         if constexpr (EPI == GEPI_QKV_ROPE) return s_rows[lr];
@@ -647,7 +652,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
         } else if (reader) {
             const int r = m0 + row;
-            const bool row_ok = r < m_end;
+            const bool row_ok = row >= 0 && r < m_end;
             const RowState rs = row_ok ? rstate(row) : RowState{0, 0, 0};
             const float sc = row_ok ? rscale(row) : 1.0f;
             unsigned long long best = 0ull;
@@ -702,10 +707,12 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         float* P = reinterpret_cast<float*>(gbase);
         if (reader) {
             if constexpr (DRAIN) {
+                if (row >= 0) {
 #pragma unroll
-                for (int j = 0; j < BN; j += 4)
-                    *reinterpret_cast<float4*>(P + row * PS + j) =
-                        make_float4(R[j], R[j + 1], R[j + 2], R[j + 3]);
+                    for (int j = 0; j < BN; j += 4)
+                        *reinterpret_cast<float4*>(P + row * PS + j) =
+                            make_float4(R[j], R[j + 1], R[j + 2], R[j + 3]);
+                }
             } else {
 #pragma unroll 1
                 for (int c = half; c < BN / 32; c += kHalves) {
@@ -716,6 +723,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                     }
+                    if (row < 0) continue;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4*>(P + row * PS + 32 * c + j) =
@@ -726,15 +734,15 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         }
         __syncthreads();
         cluster_wait_acquire();  // every peer's barriers are initialised
-        const int R_ = (128 + nsplit - 1) / nsplit;  // rows of a receive slot
-        const int r0 = 128 * split / nsplit, r1 = 128 * (split + 1) / nsplit;
+        const int R_ = (TR + nsplit - 1) / nsplit;  // rows of a receive slot
+        const int r0 = TR * split / nsplit, r1 = TR * (split + 1) / nsplit;
         const uint32_t pbase = smem_u32(P);
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(recvb, static_cast<uint32_t>((nsplit - 1) * (r1 - r0) * PS * 4));
-            // push rows [128q/S, 128(q+1)/S) of this partial to their owner q
+            // push rows [TR q/S, TR (q+1)/S) of this partial to their owner q
             for (int q = 0; q < nsplit; ++q) {
                 if (q == split) continue;
-                const int q0 = 128 * q / nsplit, q1 = 128 * (q + 1) / nsplit;
+                const int q0 = TR * q / nsplit, q1 = TR * (q + 1) / nsplit;
                 const int slot = split < q ? split : split - 1;  // slot of this sender at q
                 bulk_s2peer(map_peer(recv_base + static_cast<uint32_t>(slot * R_ * PS * 4), q),
                             pbase + static_cast<uint32_t>(q0 * PS * 4),

@@ -183,8 +183,7 @@ struct GemmArgs {
     int* err;             // ERR_* bits
     int stages;           // ring depth (set by launch_gemm from the plan)
     int a_rows;           // rows of an A tile the maps load: 128, or 64 when at most
-                          // 64 rows are ever multiplied (the MMA still spans 128 rows;
-                          // rows 64-127 read the next operand slot and are discarded)
+                          // 64 rows are ever multiplied (M = 64 MMAs then)
     // RMSNorm folded into the GEMM that consumes the normalised rows. The
     // weights carry the norm gain (W[n][k] * g[k]) and A holds the raw rows x
     // (tf32 pair), so the consumer scales row r of its result by
