@@ -468,6 +468,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.x_lo = h->xn_lo;
             g.ss_out = h->ss_ffn;
             g.ss_stride = h->ss_stride;
+            g.conv = h->a_rows == 64 ? 1 : 0;  // fp32 Wo split in shared memory (no gain)
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_wo, g.N, g.K), h->m_wo, g, s, true);
         case BK_W13:
             g.N = 2 * F;
@@ -488,6 +489,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.x_lo = h->xn_lo;
             g.ss_out = h->ss_att;
             g.ss_stride = h->ss_stride;
+            g.conv = h->a_rows == 64 ? 1 : 0;  // fp32 W2 split in shared memory (no gain)
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_w2, g.N, g.K), h->m_w2, g, s, true);
         case BK_CLS:
             g.layer = 0;
@@ -721,6 +723,10 @@ int setup_batched(l2_handle* h) {
         {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, ar}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, ar},
         {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->gp_cls.bn},
         {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->gp_cls.bn},
+        // Wo and W2 in fp32, for the 64-row launches that split them in
+        // shared memory (the GEMMs without a folded gain)
+        {&h->m_wo.b_raw, h->wo, D, D, LL, h->gp_wo.bn},
+        {&h->m_w2.b_raw, h->w2, FF, D, LL, h->gp_w2.bn},
     };
     for (const MapSpec& m : specs) {
         cudaError_t e = make_gemm_map(m.m, m.p, m.inner, m.rows, m.layers, m.box);

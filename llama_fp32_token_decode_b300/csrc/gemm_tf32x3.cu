@@ -411,15 +411,27 @@ __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
 // peer's mbarrier); CTA s adds rows [128 s / S, 128 (s+1) / S) of the S
 // partials in rank order (a fixed order: the result does not depend on
 // timing) and applies the epilogue to them.
-constexpr int gemm_threads(bool drain) { return drain ? 192 : 256; }
+// CONV (drained launches of 64-row handles for the GEMMs without a folded
+// gain: Wo, W2): the weight tiles arrive as fp32 (one copy, half the bytes of
+// the tf32 pair) and kConvWarps extra warps split each landed tile in shared
+// memory: the tensor core reads an fp32 operand as tf32 by dropping its 13
+// low mantissa bits, so hi = w stays in place and lo = w - trunc(w), exact in
+// fp32, goes to the lo tile (the tensor core truncates lo in turn: a relative
+// error below 2^-20 of w, against 2^-23 for the rounded pair of the copies);
+// the MMA warp waits for the split tile. (A folded gain would add a product
+// and a second store per element: measured slower than the pair copies.)
+constexpr int kConvWarps = 2;  // 8 warps in all: a ninth would cap a thread at 168 registers
+constexpr int gemm_threads(bool drain, bool conv = false) {
+    return drain ? (conv ? 192 + 32 * kConvWarps : 192) : 256;
+}
 constexpr int kChunk = 2;         // K-blocks per TMEM accumulation chunk (DRAIN)
 constexpr int kDrainAbove = 16;   // a CTA with more K-blocks than this drains chunks
 
 // DRAIN == false (a CTA's K range is at most kDrainAbove K-blocks, error below
 // about 4e-6): one accumulator takes the whole range and the epilogue reads it
 // from TMEM 32 columns at a time, without a register copy of the tile row.
-template <int BN, int EPI, bool DRAIN>
-__global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
+template <int BN, int EPI, bool DRAIN, bool CONV>
+__global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mA_hi,
                        const __grid_constant__ CUtensorMap mA_lo,
                        const __grid_constant__ CUtensorMap mB_hi,
@@ -443,7 +455,9 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     uint64_t* accfull = empty + S;   // [2] chunk accumulated in TMEM buffer b
     uint64_t* accfree = accfull + 2; // [2] TMEM buffer b drained
     uint64_t* recvb = accfree + 2;   // split-K: the peers' slices of this CTA's rows
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
+    uint64_t* convb = recvb + 1;     // CONV: [S] the slot's weight tile is split
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(convb + (CONV ? S : 0));
+    static_assert(!CONV || DRAIN, "the split warps come with the drained layout");
     __shared__ int s_err;
     // QKV epilogue: state of the tile's rows, loaded once during the mainloop
     __shared__ RowState s_rows[EPI == GEPI_QKV_ROPE ? 128 : 1];
@@ -471,6 +485,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
             mbar_init(&accfree[b], 4);
         }
         mbar_init(recvb, 1);
+        if constexpr (CONV)
+            for (int s = 0; s < S; ++s) mbar_init(&convb[s], kConvWarps);
         fence_mbar_init();
         s_err = 0;
         prefetch_map(&mA_hi);
@@ -501,15 +517,17 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
     for (int j = 0; j < (DRAIN ? BN : 1); ++j) R[j] = 0.0f;
 
     constexpr int kProdWarp = DRAIN ? 4 : 0, kMmaWarp = DRAIN ? 5 : 1;
+    // bytes a slot's copies bring: with CONV one fp32 weight tile, not the pair
+    const uint32_t slot_tx = static_cast<uint32_t>(CONV ? 2 * a_bytes + C::B_BYTES : stage_b);
     if (warp == kProdWarp && (DRAIN || lane == 0)) {
         if (lane == 0) {
             // ---- producer: local K-block i is global K-block kb0 + i
             const int pre = NK < S ? NK : S;
             for (int i = 0; i < pre; ++i) {
                 const int kc = (kb0 + i) * 32;
-                mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(stage_b));
+                mbar_arrive_expect_tx(&full[i], slot_tx);
                 tma_load_3d(b_hi(i), &mB_hi, kc, n0, g.layer, &full[i]);
-                tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
+                if (!CONV) tma_load_3d(b_lo(i), &mB_lo, kc, n0, g.layer, &full[i]);
             }
             pdl_wait();  // activations come from the previous kernel
             for (int i = 0; i < pre; ++i) {
@@ -524,9 +542,9 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                     s_err = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_b));
+                mbar_arrive_expect_tx(&full[s], slot_tx);
                 tma_load_3d(b_hi(s), &mB_hi, kc, n0, g.layer, &full[s]);
-                tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
+                if (!CONV) tma_load_3d(b_lo(s), &mB_lo, kc, n0, g.layer, &full[s]);
                 tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
                 tma_load_3d(a_lo(s), &mA_lo, kc, m0, 0, &full[s]);
                 issued = i + 1;
@@ -549,7 +567,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                     break;
                 }
                 const int s = i % S;
-                if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
+                uint64_t* ready = CONV ? &convb[s] : &full[s];
+                if (!mbar_wait_bounded(ready, static_cast<uint32_t>(i / S) & 1u)) {
                     s_err = 1;
                     break;
                 }
@@ -568,6 +587,32 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
                 mma_commit(&empty[s]);
                 if (w == CH - 1 || i == NK - 1) mma_commit(&accfull[buf]);
             }
+        }
+    } else if (CONV && warp >= 6) {
+        // ---- split warps (see CONV): lo of each landed fp32 weight tile (an
+        // elementwise map, so the tiles' 128-byte swizzle needs no decoding)
+        const int ct = threadIdx.x - 192;
+        constexpr int NCV = 32 * kConvWarps;
+        constexpr int PER = BN * 8 / NCV;  // float4 per thread and tile
+        static_assert(BN * 8 % NCV == 0, "whole float4 passes over a tile");
+        for (int i = 0; i < NK; ++i) {
+            const int s = i % S;
+            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
+                s_err = 1;
+                break;
+            }
+            const float4* bh = reinterpret_cast<const float4*>(gbase + (b_hi(s) - base));
+            float4* bl = reinterpret_cast<float4*>(gbase + (b_lo(s) - base));
+            float4 v[PER];
+#pragma unroll
+            for (int j = 0; j < PER; ++j) v[j] = bh[ct + NCV * j];
+#pragma unroll
+            for (int j = 0; j < PER; ++j)
+                bl[ct + NCV * j] = make_float4(v[j].x - tf32_trunc(v[j].x), v[j].y - tf32_trunc(v[j].y),
+                                               v[j].z - tf32_trunc(v[j].z), v[j].w - tf32_trunc(v[j].w));
+            fence_proxy_async_smem();  // the tensor core reads what was just written
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&convb[s]);
         }
     } else if constexpr (!DRAIN) {
         // the other warps wait below for the single accumulator; warp 2 first
@@ -625,7 +670,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN), 1)
         tc_fence_after();
     }
     __syncthreads();  // mainloop and drain done; s_err settled; s_rows loaded
-    constexpr int NT = gemm_threads(DRAIN);
+    constexpr int NT = gemm_threads(DRAIN, CONV);
     // TMEM readers: warps 0-3 with the drain (all columns, from R); without
     // it every warp, warp w taking chunks w / 4, w / 4 + NT / 128, ...
     constexpr int kHalves = DRAIN ? 1 : NT / 128;
@@ -899,13 +944,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BN, int EPI, bool DRAIN>
+template <int BN, int EPI, bool DRAIN, bool CONV = false>
 cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStream_t s, bool pdl) {
     using C = Cfg<BN>;
     cudaLaunchConfig_t cfg{};
     const int mt = (g.M + 127) / 128, nt = (g.N + BN - 1) / BN;
     cfg.gridDim = dim3(ksplit, mt * nt);
-    cfg.blockDim = dim3(gemm_threads(DRAIN));
+    cfg.blockDim = dim3(gemm_threads(DRAIN, CONV));
     cfg.dynamicSmemBytes = C::smem_for(g.stages, ksplit, g.a_rows == 64 ? 64 : 128);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -917,8 +962,9 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& g, int ksplit, cudaStrea
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI, DRAIN>, m.a_hi, m.a_lo, m.b_hi,
-                              m.b_lo, g);
+    // CONV: the weight map is the fp32 array's (the lo map is not read)
+    return cudaLaunchKernelEx(&cfg, gemm_tf32x3_kernel<BN, EPI, DRAIN, CONV>, m.a_hi, m.a_lo,
+                              CONV ? m.b_raw : m.b_hi, m.b_lo, g);
 }
 
 // Tiles wider than 128 columns have no drained variant (its register copy of
@@ -929,14 +975,19 @@ constexpr bool has_drain() { return BN <= 128; }
 
 template <int BN, int EPI>
 cudaError_t set_smem() {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, false>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, false, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMaxDynSmem));
     if (e != cudaSuccess) return e;
-    if constexpr (has_drain<BN>())
-        e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true>,
+    if constexpr (has_drain<BN>()) {
+        e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kMaxDynSmem));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_tf32x3_kernel<BN, EPI, true, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kMaxDynSmem));
+    }
     return e;
 }
 
@@ -950,15 +1001,15 @@ cudaError_t set_smem_bn() {
     return set_smem<BN, GEPI_ARGMAX>();
 }
 
-template <int BN, bool DRAIN>
+template <int BN, bool DRAIN, bool CONV = false>
 cudaError_t launch_bd(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cudaStream_t s,
                       bool pdl) {
     switch (epi) {
-        case GEPI_STORE: return launch_t<BN, GEPI_STORE, DRAIN>(m, g, ks, s, pdl);
-        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL, DRAIN>(m, g, ks, s, pdl);
-        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU, DRAIN>(m, g, ks, s, pdl);
-        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE, DRAIN>(m, g, ks, s, pdl);
-        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX, DRAIN>(m, g, ks, s, pdl);
+        case GEPI_STORE: return launch_t<BN, GEPI_STORE, DRAIN, CONV>(m, g, ks, s, pdl);
+        case GEPI_RESIDUAL: return launch_t<BN, GEPI_RESIDUAL, DRAIN, CONV>(m, g, ks, s, pdl);
+        case GEPI_SWIGLU: return launch_t<BN, GEPI_SWIGLU, DRAIN, CONV>(m, g, ks, s, pdl);
+        case GEPI_QKV_ROPE: return launch_t<BN, GEPI_QKV_ROPE, DRAIN, CONV>(m, g, ks, s, pdl);
+        case GEPI_ARGMAX: return launch_t<BN, GEPI_ARGMAX, DRAIN, CONV>(m, g, ks, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -970,7 +1021,10 @@ cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cud
     const int KB = (g.K + 31) / 32;
     const int per_cta = (KB + ks - 1) / ks;
     if (per_cta > kDrainAbove) {
-        if constexpr (has_drain<BN>()) return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
+        if constexpr (has_drain<BN>()) {
+            if (g.conv) return launch_bd<BN, true, true>(epi, m, g, ks, s, pdl);
+            return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
+        }
         return cudaErrorInvalidValue;
     }
     return launch_bd<BN, false>(epi, m, g, ks, s, pdl);
@@ -1029,7 +1083,7 @@ int active_clusters(int ksplit, int stages, int a_rows) {
     cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(
-            &n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE, has_drain<BN>()>, &cfg) != cudaSuccess) {
+            &n, gemm_tf32x3_kernel<BN, GEPI_QKV_ROPE, has_drain<BN>(), false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

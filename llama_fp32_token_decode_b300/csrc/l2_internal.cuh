@@ -158,6 +158,7 @@ enum GemmEpilogue : int {
 // W (hi, lo) [L][N][K].
 struct GemmMaps {
     CUtensorMap a_hi, a_lo, b_hi, b_lo;
+    CUtensorMap b_raw;  // W in fp32, [L][N][K] (split in shared memory: GemmArgs::conv)
 };
 
 struct GemmArgs {
@@ -182,6 +183,8 @@ struct GemmArgs {
     unsigned long long* argmax_keys;  // ARGMAX: [M]
     int* err;             // ERR_* bits
     int stages;           // ring depth (set by launch_gemm from the plan)
+    int conv;             // drained launches read W once, in fp32 (GemmMaps::b_raw),
+                          // and split it into the tf32 pair in shared memory
     int a_rows;           // rows of an A tile the maps load: 128, or 64 when at most
                           // 64 rows are ever multiplied (M = 64 MMAs then)
     // RMSNorm folded into the GEMM that consumes the normalised rows. The
@@ -407,6 +410,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // Nearest tf32 value of v (10 explicit mantissa bits, ties away from zero);
 // infinities and NaN pass through. v - tf32_round(v) is exact in fp32.
+// v with its 13 low mantissa bits cleared: the part of v a tf32 operand keeps.
+__device__ __forceinline__ float tf32_trunc(float v) {
+    return __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+}
+
 __device__ __forceinline__ float tf32_round(float v) {
     uint32_t u = __float_as_uint(v);
     if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x1000u) & 0xffffe000u;
