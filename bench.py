@@ -620,7 +620,8 @@ def run_ours(args, world, rank, local):
                        "flops": flops, "fp32_weight_bytes": bytes_fp32,
                        "note": "bound = max(fp32 weights once / HBM peak, 2 n params FLOPs / "
                                "3xTF32 peak); the pass reads the tf32 hi and lo weight "
-                               "copies (2x the fp32 bytes)"},
+                               "copies of Wq/Wk/Wv and W1/W3 (2x their fp32 bytes) and "
+                               "Wo and W2 in fp32, split in shared memory"},
                    "tokens_equal_to_decode_path": same,
                    "note": "prompt through l2_generate_prefill_device (one causal "
                            "tensor-core pass), then 255 decode forwards; not the headline"}
