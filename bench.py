@@ -712,6 +712,9 @@ def run_small_models(args, world, local):
                                        "frac": gbs / hbm,
                                        "bytes_per_forward": step_bytes / n_fwd,
                                        "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"},
+                     # weights under 100 MB are kept in L2 (evict_last) from
+                     # token to token: their bytes then come from L2, not HBM
+                     "weights_in_l2": bool(step_bytes / n_fwd < 100e6),
                      "layer_kernels": layer_kernels,
                      "kernels_per_forward": layer_kernels * cfg["n_layers"] + 1,
                      "clocks": clocks}
