@@ -184,10 +184,19 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
     const float4* V4 = reinterpret_cast<const float4*>(a.v_cache + static_cast<size_t>(kvh) * a.seq_len * hd);
 
     __shared__ float4 s_inbox[kMaxCluster][HD4MAX];    // rank 0: partial outputs of the cluster
-    __shared__ float s_ml[kMaxCluster][2];             // rank 0: (max, sum) of the cluster
+    __shared__ __align__(8) float s_ml[kMaxCluster][2];  // rank 0: (max, sum) of the cluster
     __shared__ float s_m[kAttnWarps], s_l[kAttnWarps];
     __shared__ float4 s_o[kAttnWarps][HD4MAX];
+    __shared__ __align__(8) uint64_t s_inbar;  // rank 0: the cluster's partials have landed
 
+    // rank 0 counts the partials' bytes (st.async from every rank, itself
+    // included) on an mbarrier instead of a cluster-wide barrier, so the other
+    // ranks leave as soon as they have sent theirs
+    if (rank == 0 && tid == 0) {
+        mbar_init(&s_inbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&s_inbar, static_cast<uint32_t>(nsplit * (hd4 * 16 + 8)));
+    }
     pdl_launch_dependents();
 
     // ---- early loads: the first iteration's rows of earlier positions
@@ -249,7 +258,9 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
         }
         if (gmax == -INFINITY) continue;
         const float mnew = fmaxf(m, gmax);
-        const float corr = (m == -INFINITY) ? 0.0f : expf(m - mnew);
+        // __expf: the SFU exponential, within a few ulp for these non-positive
+        // arguments, as close as the fp32 sums it weights
+        const float corr = (m == -INFINITY) ? 0.0f : __expf(m - mnew);
         l *= corr;
         o.x *= corr;
         o.y *= corr;
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
         o.w *= corr;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const float p = (sc[g] == -INFINITY) ? 0.0f : expf(sc[g] - mnew);
+            const float p = (sc[g] == -INFINITY) ? 0.0f : __expf(sc[g] - mnew);
             l += p;
             o.x = fmaf(p, vr[g].x, o.x);
             o.y = fmaf(p, vr[g].y, o.y);
@@ -277,8 +288,8 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
         o2.z = __shfl_xor_sync(0xffffffffu, o.z, off);
         o2.w = __shfl_xor_sync(0xffffffffu, o.w, off);
         const float M = fmaxf(m, m2);
-        const float f1 = (m == -INFINITY) ? 0.0f : expf(m - M);
-        const float f2 = (m2 == -INFINITY) ? 0.0f : expf(m2 - M);
+        const float f1 = (m == -INFINITY) ? 0.0f : __expf(m - M);
+        const float f2 = (m2 == -INFINITY) ? 0.0f : __expf(m2 - M);
         l = l * f1 + l2v * f2;
         o.x = o.x * f1 + o2.x * f2;
         o.y = o.y * f1 + o2.y * f2;
@@ -297,40 +308,43 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attn4_kernel(const AttnArgs a
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w]);
     cluster_wait_all();  // every CTA of the cluster is running: rank 0's inbox exists
+    const uint32_t inbar0 = cluster_smem(&s_inbar, 0);
     if (tid < hd4) {
         float4 acc = z;
 #pragma unroll
         for (int w = 0; w < kAttnWarps; ++w) {
             if (s_m[w] == -INFINITY) continue;
-            const float f = expf(s_m[w] - M);
+            const float f = __expf(s_m[w] - M);
             const float4 v = s_o[w][tid];
             acc.x += v.x * f;
             acc.y += v.y * f;
             acc.z += v.z * f;
             acc.w += v.w * f;
         }
-        *cluster.map_shared_rank(&s_inbox[rank][tid], 0) = acc;
+        st_async_f4(cluster_smem(&s_inbox[rank][tid], 0), acc, inbar0);
     }
     if (tid == 0) {
         float L = 0.0f;
         for (int w = 0; w < kAttnWarps; ++w)
-            if (s_m[w] != -INFINITY) L += s_l[w] * expf(s_m[w] - M);
-        float* ml = cluster.map_shared_rank(&s_ml[rank][0], 0);
-        ml[0] = M;
-        ml[1] = L;
+            if (s_m[w] != -INFINITY) L += s_l[w] * __expf(s_m[w] - M);
+        st_async_f2(cluster_smem(&s_ml[rank][0], 0), M, L, inbar0);
     }
-    cluster.sync();  // partials of every rank are in rank 0's shared memory
-    if (rank != 0) return;
+    if (rank != 0) return;  // nothing of this CTA's shared memory is read remotely
+    // partials of every rank are in rank 0's shared memory once their bytes land
+    if (!mbar_wait_cluster_bounded(&s_inbar, 0u)) {
+        if (tid == 0) atomicOr(&a.st->err, ERR_TIMEOUT_TMA);
+        return;
+    }
     float Mg = -INFINITY;
     for (int r = 0; r < nsplit; ++r) Mg = fmaxf(Mg, s_ml[r][0]);
     float Lg = 0.0f;
     for (int r = 0; r < nsplit; ++r)
-        if (s_ml[r][0] != -INFINITY) Lg += s_ml[r][1] * expf(s_ml[r][0] - Mg);
+        if (s_ml[r][0] != -INFINITY) Lg += s_ml[r][1] * __expf(s_ml[r][0] - Mg);
     if (tid < hd4) {
         float4 acc = z;
         for (int r = 0; r < nsplit; ++r) {
             if (s_ml[r][0] == -INFINITY) continue;
-            const float f = expf(s_ml[r][0] - Mg);
+            const float f = __expf(s_ml[r][0] - Mg);
             const float4 v = s_inbox[r][tid];
             acc.x += v.x * f;
             acc.y += v.y * f;

@@ -379,6 +379,13 @@ __device__ __forceinline__ void st_async_f2(uint32_t addr, float x, float y, uin
         "f"(x), "f"(y), "r"(bar)
         : "memory");
 }
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+            "r"(addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void st_async_f1(uint32_t addr, float x, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
                      addr),
