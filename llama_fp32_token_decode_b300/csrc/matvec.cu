@@ -96,8 +96,10 @@ namespace {
 // ring slot are spread over the 16 / WPR warp groups. Each warp leaves one
 // partial sum per (row, column part) in shared memory; the epilogue adds the
 // WPR partials of a row in a fixed order.
+// 88 registers: 544 threads x 88 leave a 256-thread, 64-register attention
+// CTA room on the same SM (programmatic dependent launch overlaps the two).
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a) {
+__global__ void __maxnreg__(88) matvec_kernel(const MatvecArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const MatvecPlan& P = a.plan;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,6 +169,21 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
     // ---- everything below reads results of earlier kernels
     pdl_wait();
     L2State* st = a.st;
+    // QKV: the epilogue's position and this thread's first RoPE pair, requested
+    // now so that their two dependent round trips hide under the input load
+    // (kept in shared memory through the stream: no registers held there)
+    __shared__ int s_pos;
+    __shared__ float2 s_cs[EPI == EPI_QKV_ROPE ? kThreads : 1];
+    int e_pos = 0;
+    float2 e_cs = make_float2(1.0f, 0.0f);
+    if constexpr (EPI == EPI_QKV_ROPE) {
+        e_pos = __ldcg(&st->pos);
+        const int gr = r0 + 2 * tid;
+        if (tid < nrows / 2 && gr < a.d + a.kvd) {
+            const int e = (gr < a.d ? gr : gr - a.d) % a.head_dim;
+            e_cs = a.rope[static_cast<size_t>(e_pos) * (a.head_dim >> 1) + (e >> 1)];
+        }
+    }
 
     const float* src = a.src;
     if (a.emb != nullptr) {
@@ -229,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
         }
     } else {
         for (int i = tid; i < K4; i += kThreads) xs4[i] = __ldcg(src4 + i);
+    }
+    if constexpr (EPI == EPI_QKV_ROPE) {
+        if (tid == 0) s_pos = e_pos;
+        s_cs[tid] = e_cs;
     }
     __syncthreads();
 
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
             a.out[r0 / 2 + i] = (g / (1.0f + expf(-g))) * u;
         }
     } else if constexpr (EPI == EPI_QKV_ROPE) {
-        const int pos = __ldcg(&st->pos);
+        const int pos = s_pos;
         const int slot = pos % a.seq_len;  // == pos unless the cache rolls
         const int hd = a.head_dim, half = hd >> 1;
         const float2* rope = a.rope + static_cast<size_t>(pos) * half;  // absolute position
@@ -352,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_kernel(const MatvecArgs a)
             const int gr = r0 + 2 * i;
             const float x0 = rowval(2 * i), x1 = rowval(2 * i + 1);
             if (gr < a.d) {
-                const float2 cs = rope[(gr % hd) >> 1];
+                const float2 cs = i == tid ? s_cs[tid] : rope[(gr % hd) >> 1];
                 a.q_out[gr] = x0 * cs.x - x1 * cs.y;
                 a.q_out[gr + 1] = x0 * cs.y + x1 * cs.x;
             } else if (gr < a.d + a.kvd) {
                 const int j = gr - a.d, kvh = j / hd, e = j % hd;
-                const float2 cs = rope[e >> 1];
+                const float2 cs = i == tid ? s_cs[tid] : rope[e >> 1];
                 float* dst = a.k_cache + (static_cast<size_t>(kvh) * a.seq_len + slot) * hd + e;
                 dst[0] = x0 * cs.x - x1 * cs.y;
                 dst[1] = x0 * cs.y + x1 * cs.x;
