@@ -19,7 +19,10 @@
 // The CTA merges its warps, then stores (max, sum, unnormalised output) into
 // the shared memory of the cluster's rank-0 CTA (distributed shared memory);
 // after one hardware cluster barrier rank 0 merges the nsplit partials with
-// log-sum-exp rescaling and writes att_h. No global atomics, fences or spins.
+// log-sum-exp rescaling and writes att_h (attn_kernel). attn4_kernel sends
+// its partials with st.async instead, their bytes counted on an mbarrier in
+// rank 0, whose bounded wait replaces the barrier: the other ranks leave as
+// soon as they have sent. No global atomics or fences.
 #include <cooperative_groups.h>
 #include <math.h>
 
