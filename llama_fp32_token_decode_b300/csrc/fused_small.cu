@@ -274,7 +274,7 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
         if (tg < 2 * hd) rs[p] = __ldg(rope + ((tg < hd ? tg : tg - hd) >> 1));
     }
     // head 0's CTAs keep their rows of the residual, added into x_mid once the
-    // cluster barriers are behind them
+    // cluster's exchanges are behind them
     const float inv = norm_load<kFAttnThreads>(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
                                 h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
@@ -283,8 +283,8 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
         mbar_wait_bounded(&wbar, 0u);  // drain the copies still in flight (bounded)
     }
     __syncthreads();
-    const bool ok = s_fail == 0;  // on a timeout the exchange still runs (every CTA
-                                  // takes the cluster barriers), with zero rows
+    const bool ok = s_fail == 0;  // on a timeout the exchanges still run (every CTA
+                                  // sends its rows and partials), with zeros
     if (!ok)
         for (int i = tid; i < d; i += kFAttnThreads) gs[i] = 0.0f;
     norm_scale<kFAttnThreads>(xs, gs, inv, d);
@@ -432,7 +432,7 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
                                // for at the end: no CTA leaves before its peers)
 
     // ---- global writes that nothing in this kernel reads, issued after the
-    // last cluster barrier (whose release would otherwise wait for them):
+    // last exchange (a cluster barrier's release would have waited for them):
     // the carried residual rows, and this position's k and v, appended by the
     // first cluster of each kv head, 1/8 of the 2 hd values per CTA
     if (h == 0) {
