@@ -61,6 +61,9 @@ struct l2_handle {
     int mcap = 0;
     int rows = 0;                      // max(max_batch, max_prefill): row buffers of the GEMM path
     int a_rows = 128;                  // rows of the GEMMs' A tiles: 64 when rows <= 64
+    // 64-row handles whose QKV / W1W3 / classifier launches are drained: the
+    // *_hi copy holds W * g in fp32 (no lo copy), split in shared memory
+    bool conv_qkv = false, conv_w13 = false, conv_cls = false;
     float* bw = nullptr;
     float *qkv_hi = nullptr, *qkv_lo = nullptr, *wo_hi = nullptr, *wo_lo = nullptr;
     float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
@@ -430,6 +433,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.rope_positions = h->pmax;
             g.cache_seq = h->cache_seq;
             g.ss_in = h->ss_att;  // attention RMSNorm (gain in the weights)
+            g.conv = h->conv_qkv ? 1 : 0;
             g.ss_count = l == 0 ? 1 : ss_slots(h->gp_w2, d);
             g.ss_stride = h->ss_stride;
             g.eps = c.norm_eps;
@@ -476,6 +480,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.out_hi = h->hb_hi;
             g.out_lo = h->hb_lo;
             g.ss_in = h->ss_ffn;  // FFN RMSNorm (gain in the weights)
+            g.conv = h->conv_w13 ? 1 : 0;
             g.ss_count = ss_slots(h->gp_wo, d);
             g.ss_stride = h->ss_stride;
             g.eps = c.norm_eps;
@@ -499,6 +504,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.ldc = V;
             g.argmax_keys = h->b_keys;
             g.ss_in = h->ss_att;  // final RMSNorm (gain in the weights)
+            g.conv = h->conv_cls ? 1 : 0;
             g.ss_count = ss_slots(h->gp_w2, d);
             g.ss_stride = h->ss_stride;
             g.eps = c.norm_eps;
@@ -655,13 +661,38 @@ int setup_batched(l2_handle* h) {
     h->cls_hi = h->bw + o_ch; h->cls_lo = h->bw + o_cl;
     cudaStream_t s = h->stream;
     L2_CUDA(h, prepare_gemm(&h->gocc));
+    const int Mb = static_cast<int>(RW);
+    // at most 64 rows per GEMM (a prefill-only handle): 64-row A tiles, so the
+    // shared-memory ring holds more weight bytes and the A operand is read once
+    h->a_rows = RW <= 64 ? 64 : 128;
+    const int ar = h->a_rows;
+    h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d), 256, ar);
+    // Wo and W2 write the per-row sums of squares of the next norm: tiles <= 128
+    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d), 128, ar);
+    h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d), 256, ar);
+    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128, ar);
+    h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d), 256, ar);
+    h->conv_qkv = ar == 64 && gemm_drained(h->gp_qkv, static_cast<int>(d));
+    h->conv_w13 = ar == 64 && gemm_drained(h->gp_w13, static_cast<int>(d));
+    h->conv_cls = ar == 64 && gemm_drained(h->gp_cls, static_cast<int>(d));
     // the GEMMs that consume a normalised row carry the RMSNorm gain in their
-    // weights (W[n][k] * g[k]); the row scale is applied in their epilogue
-    L2_CUDA(h, launch_split_tf32_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, h->qkv_lo, s));
+    // weights (W[n][k] * g[k]); the row scale is applied in their epilogue.
+    // Launches that split W in shared memory read W * g in fp32 from the hi
+    // copy (the lo copy is not read).
+    if (h->conv_qkv)
+        L2_CUDA(h, launch_scale_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, s));
+    else
+        L2_CUDA(h, launch_split_tf32_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, h->qkv_lo, s));
     L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
-    L2_CUDA(h, launch_split_tf32_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, h->w13_lo, s));
+    if (h->conv_w13)
+        L2_CUDA(h, launch_scale_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, s));
+    else
+        L2_CUDA(h, launch_split_tf32_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, h->w13_lo, s));
     L2_CUDA(h, launch_split_tf32(h->w2, h->w2_hi, h->w2_lo, n_w2, s));
-    L2_CUDA(h, launch_split_tf32_gain(h->wcls, h->g_final, d, V, 1, h->cls_hi, h->cls_lo, s));
+    if (h->conv_cls)
+        L2_CUDA(h, launch_scale_gain(h->wcls, h->g_final, d, V, 1, h->cls_hi, s));
+    else
+        L2_CUDA(h, launch_split_tf32_gain(h->wcls, h->g_final, d, V, 1, h->cls_hi, h->cls_lo, s));
 
     off = 0;
     const size_t o_x = take(Mc * d), o_nh = take(Mc * d), o_nl = take(Mc * d), o_q = take(Mc * d);
@@ -696,17 +727,6 @@ int setup_batched(l2_handle* h) {
     h->d_sparams = reinterpret_cast<SampleParams*>(h->bst + o_sp);
     h->b_rmap = h->bst + o_rmap;
 
-    const int Mb = static_cast<int>(RW);
-    // at most 64 rows per GEMM (a prefill-only handle): 64-row A tiles, so the
-    // shared-memory ring holds more weight bytes and the A operand is read once
-    h->a_rows = RW <= 64 ? 64 : 128;
-    const int ar = h->a_rows;
-    h->gp_qkv = plan_gemm(h->gocc, Mb, static_cast<int>(d + 2 * kvd), static_cast<int>(d), 256, ar);
-    // Wo and W2 write the per-row sums of squares of the next norm: tiles <= 128
-    h->gp_wo = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(d), 128, ar);
-    h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d), 256, ar);
-    h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128, ar);
-    h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d), 256, ar);
     const long long D = d, FF = F, LL = L, MC = Mc;
     struct MapSpec { CUtensorMap* m; const float* p; long long inner, rows, layers; int box; };
     const MapSpec specs[] = {
@@ -723,10 +743,13 @@ int setup_batched(l2_handle* h) {
         {&h->m_cls.a_hi, h->xn_hi, D, MC, 1, ar}, {&h->m_cls.a_lo, h->xn_lo, D, MC, 1, ar},
         {&h->m_cls.b_hi, h->cls_hi, D, static_cast<long long>(V), 1, h->gp_cls.bn},
         {&h->m_cls.b_lo, h->cls_lo, D, static_cast<long long>(V), 1, h->gp_cls.bn},
-        // Wo and W2 in fp32, for the 64-row launches that split them in
-        // shared memory (the GEMMs without a folded gain)
+        // W in fp32 (times the folded gain), for the 64-row launches that
+        // split it in shared memory
+        {&h->m_qkv.b_raw, h->qkv_hi, D, D + 2 * static_cast<long long>(kvd), LL, h->gp_qkv.bn},
         {&h->m_wo.b_raw, h->wo, D, D, LL, h->gp_wo.bn},
+        {&h->m_w13.b_raw, h->w13_hi, D, 2 * FF, LL, h->gp_w13.bn},
         {&h->m_w2.b_raw, h->w2, FF, D, LL, h->gp_w2.bn},
+        {&h->m_cls.b_raw, h->cls_hi, D, static_cast<long long>(V), 1, h->gp_cls.bn},
     };
     for (const MapSpec& m : specs) {
         cudaError_t e = make_gemm_map(m.m, m.p, m.inner, m.rows, m.layers, m.box);

@@ -1256,6 +1256,29 @@ cudaError_t launch_split_tf32_gain(const float* x, const float* gain, long long 
     return cudaGetLastError();
 }
 
+__global__ void scale_gain_kernel(const float* __restrict__ x, const float* __restrict__ gain,
+                                  long long K, long long rows, long long n, float* __restrict__ out) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long k = i % K, layer = i / (K * rows);
+        out[i] = x[i] * gain[layer * K + k];  // the product the pair split starts from
+    }
+}
+
+cudaError_t launch_scale_gain(const float* x, const float* gain, long long K, long long rows,
+                              long long layers, float* out, cudaStream_t s) {
+    if (K < 1 || rows < 1 || layers < 1) return cudaErrorInvalidValue;
+    const long long n = K * rows * layers;
+    const int blocks = static_cast<int>(n / 256 + 1 < 8192 ? n / 256 + 1 : 8192);
+    scale_gain_kernel<<<blocks, 256, 0, s>>>(x, gain, K, rows, n, out);
+    return cudaGetLastError();
+}
+
+bool gemm_drained(const GemmPlan& p, int K) {
+    const int KB = (K + 31) / 32;
+    return p.ksplit >= 1 && p.bn <= 128 && (KB + p.ksplit - 1) / p.ksplit > kDrainAbove;
+}
+
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n, cudaStream_t s) {
     if (n % 4 != 0) return cudaErrorInvalidValue;
     const long long n4 = n / 4;

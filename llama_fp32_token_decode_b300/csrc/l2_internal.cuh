@@ -504,6 +504,13 @@ cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, long long n,
 // is multiplied by gain[l * K + k] first ([layers][rows][K] weights).
 cudaError_t launch_split_tf32_gain(const float* x, const float* gain, long long K, long long rows,
                                    long long layers, float* hi, float* lo, cudaStream_t s);
+// The gain-scaled weights themselves in fp32 (what the GEMMs that split W in
+// shared memory read).
+cudaError_t launch_scale_gain(const float* x, const float* gain, long long K, long long rows,
+                              long long layers, float* out, cudaStream_t s);
+// Whether launches of this plan take the drained (and, on 64-row handles,
+// split-in-shared-memory) build: more than 16 K-blocks per CTA.
+bool gemm_drained(const GemmPlan& p, int K);
 
 // batched.cu
 cudaError_t launch_brmsnorm(const BNormArgs& a, int M, cudaStream_t s, bool pdl);
