@@ -619,9 +619,9 @@ def run_ours(args, world, rank, local):
                        "bound_ms": bound_ms, "frac": bound_ms / ms_pre,
                        "flops": flops, "fp32_weight_bytes": bytes_fp32,
                        "note": "bound = max(fp32 weights once / HBM peak, 2 n params FLOPs / "
-                               "3xTF32 peak); the pass reads the tf32 hi and lo weight "
-                               "copies of Wq/Wk/Wv and W1/W3 (2x their fp32 bytes) and "
-                               "Wo and W2 in fp32, split in shared memory"},
+                               "3xTF32 peak); the pass reads each weight once in fp32 "
+                               "(times its folded RMSNorm gain) and splits it into the "
+                               "tf32 pair in shared memory"},
                    "tokens_equal_to_decode_path": same,
                    "note": "prompt through l2_generate_prefill_device (one causal "
                            "tensor-core pass), then 255 decode forwards; not the headline"}
