@@ -198,6 +198,9 @@ MatvecArgs base_args(l2_handle* h) {
 
 // Launches kernel `kind` of layer l on stream s (kind as in l2_time_kernel).
 void fused_layer_args(const l2_handle* h, size_t l, FAttnArgs* a, FFfnArgs* f);
+// 64-bit words of the two-kernel path's residual buffers: two output rows of
+// the FFN block in kFfnCopies copies each, two of the attention block.
+inline size_t fx_words(size_t d) { return (2 * kFfnCopies + 2) * d; }
 
 cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
     const l2_config& c = h->cfg;
@@ -271,8 +274,10 @@ cudaError_t launch_kind(l2_handle* h, int kind, int l, cudaStream_t s) {
 void fused_layer_args(const l2_handle* h, size_t l, FAttnArgs* a, FFfnArgs* f) {
     const l2_config& c = h->cfg;
     const size_t d = c.dim, F = c.hidden_dim, kvd = h->kvd, L = c.n_layers;
-    long long* P[2] = {h->fx, h->fx + d};
-    long long* M[2] = {h->fx + 2 * d, h->fx + 3 * d};
+    // P[b]: kFfnCopies copies of d (the FFN blocks' output), M[b]: one copy
+    const size_t R = kFfnCopies;
+    long long* P[2] = {h->fx, h->fx + R * d};
+    long long* M[2] = {h->fx + 2 * R * d, h->fx + 2 * R * d + d};
     *a = h->fattn;
     a->wqkv = h->wqkv + l * (d + 2 * kvd) * d;
     a->wo_h = h->fw + l * d * d;
@@ -302,8 +307,8 @@ cudaError_t enqueue_forward_fused(l2_handle* h, cudaStream_t s) {
         if ((e = launch_fffn(f, h->ffn_grid, s, true)) != cudaSuccess) return e;
     }
     // classifier on the last residual; it also clears the next forward's M[0]
-    long long* P[2] = {h->fx, h->fx + d};
-    long long* M0 = h->fx + 2 * d;
+    long long* P[2] = {h->fx, h->fx + kFfnCopies * d};
+    long long* M0 = h->fx + 2 * kFfnCopies * d;
     MatvecArgs a = base_args(h);
     a.W = h->wcls;
     a.plan = h->p_cls;
@@ -869,8 +874,8 @@ int setup_fused(l2_handle* h) {
         (!fits || static_cast<double>(h->weight_floats) * 4.0 >= 2e9))
         return L2_OK;
     L2_CUDA(h, cudaMalloc(&h->fw, (L * d * d + L * F * d) * sizeof(float)));
-    L2_CUDA(h, cudaMalloc(&h->fx, 4 * d * sizeof(long long)));
-    L2_CUDA(h, cudaMemsetAsync(h->fx, 0, 4 * d * sizeof(long long), h->stream));
+    L2_CUDA(h, cudaMalloc(&h->fx, fx_words(d) * sizeof(long long)));
+    L2_CUDA(h, cudaMemsetAsync(h->fx, 0, fx_words(d) * sizeof(long long), h->stream));
     L2_CUDA(h, launch_retile_heads(h->fw, h->wo, static_cast<int>(L), static_cast<int>(d), h->hd,
                                    h->stream));
     L2_CUDA(h, launch_transpose_layers(h->fw + L * d * d, h->w2, static_cast<int>(L),
@@ -1687,7 +1692,7 @@ int l2_time_kernel(l2_handle* h, int32_t kind, int32_t pos, int32_t iters, void*
     L2_CUDA(h, cudaEventRecord(h->ev1, s));
     // a forward starts from zeroed fixed-point residual buffers
     if (kind >= 14)
-        L2_CUDA(h, cudaMemsetAsync(h->fx, 0, 4 * h->cfg.dim * sizeof(long long), s));
+        L2_CUDA(h, cudaMemsetAsync(h->fx, 0, fx_words(h->cfg.dim) * sizeof(long long), s));
     L2_CUDA(h, cudaEventSynchronize(h->ev1));
     float t = 0.0f;
     L2_CUDA(h, cudaEventElapsedTime(&t, h->ev0, h->ev1));

@@ -92,8 +92,8 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     return L;
 }
 
-// First half of the RMS norm: loads x (float src, or fixed point srcf) into
-// xs and returns 1 / sqrt(mean(x^2) + eps). Each thread issues all its loads
+// First half of the RMS norm: loads x (float src, or fixed point srcf, the
+// sum of `copies` copies d apart) into xs and returns 1 / sqrt(mean(x^2) + eps). Each thread issues all its loads
 // before using one (one L2 round trip for d <= 4 * threads). Rows c0..c1 of x
 // are also added into `carry` and cleared in `zero` from the same loads, or,
 // with `stash`, kept there in fixed point for the caller to add later.
@@ -102,7 +102,7 @@ template <int NT>
 __device__ __forceinline__ float norm_load(float* xs, const float* src, const long long* srcf,
                                            int d, float eps, float* red, long long* carry,
                                            long long* zero, int c0, int c1,
-                                           long long* stash = nullptr) {
+                                           long long* stash = nullptr, int copies = 1) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float ss = 0.0f;
     for (int base = 0; base < d; base += kRowRegs * NT) {
@@ -114,8 +114,12 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
             fx[k] = 0;
             v[k] = 0.0f;
             if (i < d) {
-                if (srcf) fx[k] = __ldcg(srcf + i);
-                else v[k] = __ldg(src + i);
+                if (srcf) {
+                    fx[k] = __ldcg(srcf + i);
+                    for (int c = 1; c < copies; ++c) fx[k] += __ldcg(srcf + static_cast<size_t>(c) * d + i);
+                } else {
+                    v[k] = __ldg(src + i);
+                }
             }
         }
 #pragma unroll
@@ -276,7 +280,7 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
     // head 0's CTAs keep their rows of the residual, added into x_mid once the
     // cluster's exchanges are behind them
     const float inv = norm_load<kFAttnThreads>(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
-                                h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst);
+                                h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst, kFfnCopies);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(&st->err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -438,7 +442,8 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
     if (h == 0) {
         for (int r = r0 + tid; r < r1; r += kFAttnThreads) {
             add_fixed(a.x_mid + r, cst[r - r0]);
-            a.x_zero[r] = 0;
+#pragma unroll
+            for (int c = 0; c < kFfnCopies; ++c) a.x_zero[static_cast<size_t>(c) * d + r] = 0;
         }
     }
     if ((h % grp) == 0) {
@@ -567,7 +572,8 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
     // rows split over the CTAs
     const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
     const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
-    const float inv = norm_load<kFFfnThreads>(xs, nullptr, f.x_mid, d, f.eps, red, f.x_out, f.x_zero, q0, q1);
+    long long* x_out = f.x_out + static_cast<size_t>(c % kFfnCopies) * d;  // this CTA's copy
+    const float inv = norm_load<kFFfnThreads>(xs, nullptr, f.x_mid, d, f.eps, red, x_out, f.x_zero, q0, q1);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(f.err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -588,7 +594,7 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
     for (int i = tid; i < d; i += kFFfnThreads) {
         float acc = 0.0f;
         for (int u = 0; u < nu; ++u) acc = fmaf(w2t[static_cast<size_t>(u) * d + i], hb[u], acc);
-        add_fixed(f.x_out + i, to_fixed(acc));
+        add_fixed(x_out + i, to_fixed(acc));
     }
 }
 

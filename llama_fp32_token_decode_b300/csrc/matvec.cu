@@ -203,7 +203,10 @@ __global__ void __maxnreg__(88) matvec_kernel(const MatvecArgs a) {
         // the residual in fixed point (value * 2^32): converted once into xs
         float ss = 0.0f;
         for (int i = tid; i < K; i += kThreads) {
-            const float v = __ll2float_rn(__ldcg(a.src_fixed + i)) * (1.0f / 4294967296.0f);
+            long long f = 0;
+#pragma unroll
+            for (int c = 0; c < kFfnCopies; ++c) f += __ldcg(a.src_fixed + static_cast<size_t>(c) * K + i);
+            const float v = __ll2float_rn(f) * (1.0f / 4294967296.0f);
             xs[i] = v;
             ss += v * v;
         }
