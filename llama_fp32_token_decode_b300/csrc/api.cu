@@ -1739,9 +1739,10 @@ double l2_kernel_bytes(const l2_handle* h, int32_t kind, int32_t pos) {
         case 4: return 4.0 * (d * F + F + 2 * d);
         case 5: return 4.0 * (V * d + 2 * d + V);
         // the two-kernels-per-layer blocks: weights once, the KV rows once per
-        // kv head, the residual in and out in 8-byte fixed point
+        // kv head, the residual in and out in 8-byte fixed point (the FFN
+        // block's output row in kFfnCopies copies)
         case 14: return 4.0 * ((d + 2 * kvd) * d + d * d + 2.0 * (pos + 1) * kvd + 2 * kvd + d) +
-                        8.0 * 3 * d;
+                        8.0 * (2 * kFfnCopies + 1) * d;
         case 15: return 4.0 * (3 * F * d + d) + 8.0 * 3 * d;
         default: break;
     }
