@@ -73,7 +73,7 @@ __device__ __forceinline__ void add_fixed(long long* p, long long v) {
 // Shared-memory carve-up of the attention block (floats; every piece 16-byte aligned).
 struct FAttnLayout {
     int rows_qkv, rows_o;       // this CTA's Q/K/V rows and Wo block rows (maximum over ranks)
-    int off_wq, off_wo, off_x, off_qkv, off_part, off_red, off_g, off_c, off_rs, total;
+    int off_wq, off_wo, off_x, off_qkv, off_part, off_red, off_c, off_rs, total;
 };
 __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     FAttnLayout L;
@@ -85,15 +85,16 @@ __host__ __device__ inline FAttnLayout fattn_layout(int d, int hd) {
     L.off_qkv = L.off_x + ((d + 3) & ~3);
     L.off_part = L.off_qkv + ((3 * hd + 3) & ~3);
     L.off_red = L.off_part + G8 * ((hd + 2 + 3) & ~3);
-    L.off_g = L.off_red + kFAttnWarps * ((hd + 2 + 3) & ~3) + 64;
-    L.off_c = L.off_g + ((d + 3) & ~3);                         // carried rows, 8 bytes each
+    L.off_c = L.off_red + kFAttnWarps * ((hd + 2 + 3) & ~3) + 64;  // carried rows, 8 bytes each
     L.off_rs = L.off_c + 2 * ((d / G8 + 1 + 3) & ~3);           // RoPE pairs of the rows
     L.total = L.off_rs + 2 * ((L.rows_qkv / 2 + 3) & ~3);
     return L;
 }
 
-// First half of the RMS norm: loads x (float src, or fixed point srcf, the
-// sum of `copies` copies d apart) into xs and returns 1 / sqrt(mean(x^2) + eps). Each thread issues all its loads
+// RMS norm of a row: loads x (float src, or fixed point srcf, the sum of
+// `copies` copies d apart) and the gain g (the same round trip) into xs as
+// g x, and returns inv = 1 / sqrt(mean(x^2) + eps): the normalised row is
+// inv * xs, and the caller applies inv to the dot products it takes with xs. Each thread issues all its loads
 // before using one (one L2 round trip for d <= 4 * threads). Rows c0..c1 of x
 // are also added into `carry` and cleared in `zero` from the same loads, or,
 // with `stash`, kept there in fixed point for the caller to add later.
@@ -102,17 +103,20 @@ template <int NT>
 __device__ __forceinline__ float norm_load(float* xs, const float* src, const long long* srcf,
                                            int d, float eps, float* red, long long* carry,
                                            long long* zero, int c0, int c1,
-                                           long long* stash = nullptr, int copies = 1) {
+                                           long long* stash = nullptr, int copies = 1,
+                                           const float* gain = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float ss = 0.0f;
     for (int base = 0; base < d; base += kRowRegs * NT) {
         long long fx[kRowRegs];
         float v[kRowRegs];
+        float gk[kRowRegs];
 #pragma unroll
         for (int k = 0; k < kRowRegs; ++k) {
             const int i = base + k * NT + tid;
             fx[k] = 0;
             v[k] = 0.0f;
+            gk[k] = (gain != nullptr && i < d) ? __ldg(gain + i) : 1.0f;
             if (i < d) {
                 if (srcf) {
                     fx[k] = __ldcg(srcf + i);
@@ -127,7 +131,7 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
             const int i = base + k * NT + tid;
             if (i < d) {
                 if (srcf) v[k] = from_fixed(fx[k]);
-                xs[i] = v[k];
+                xs[i] = gk[k] * v[k];  // g x: the 1 / rms scale goes on the dot products
                 ss += v[k] * v[k];
                 if (i >= c0 && i < c1) {
                     const long long xf = srcf ? fx[k] : to_fixed(v[k]);
@@ -147,14 +151,6 @@ __device__ __forceinline__ float norm_load(float* xs, const float* src, const lo
     float t = lane < NT / 32 ? red[lane] : 0.0f;  // every warp forms the same total
     t = warp_sum(t);
     return 1.0f / sqrtf(t / static_cast<float>(d) + eps);
-}
-
-// Second half: xs = g * (inv * x), g in shared memory. Each thread scales the
-// elements it loaded, so only the barrier after it is needed.
-template <int NT>
-__device__ __forceinline__ void norm_scale(float* xs, const float* g, float inv, int d) {
-    for (int i = threadIdx.x; i < d; i += NT) xs[i] = g[i] * (inv * xs[i]);
-    __syncthreads();
 }
 
 // Dot products of two shared-memory rows with xs by one warp (16-byte
@@ -208,7 +204,6 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
     float* qkv = sm + L.off_qkv;
     float* part = sm + L.off_part;
     float* red = sm + L.off_red;
-    float* gs = sm + L.off_g;
     long long* cst = reinterpret_cast<long long*>(sm + L.off_c);
     float2* rs = reinterpret_cast<float2*>(sm + L.off_rs);
     const int pstride = (hd + 2 + 3) & ~3;
@@ -237,9 +232,8 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
         const uint64_t pol = (a.l2_policy == 0) ? make_policy_evict_first()
                                                 : make_policy_evict_last(__uint_as_float(
                                                       static_cast<uint32_t>(a.l2_policy)));
-        const uint32_t bytes = static_cast<uint32_t>(((t1 - t0) * d + (r1 - r0) * hd + d) * 4);
+        const uint32_t bytes = static_cast<uint32_t>(((t1 - t0) * d + (r1 - r0) * hd) * 4);
         mbar_arrive_expect_tx(&wbar, bytes);
-        bulk_g2s(gs, a.g_att, static_cast<uint32_t>(d * 4), &wbar, pol);
         // [q; k; v] rows t0..t1 as up to three runs of contiguous global rows
         int t = t0;
         while (t < t1) {
@@ -280,7 +274,7 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
     // head 0's CTAs keep their rows of the residual, added into x_mid once the
     // cluster's exchanges are behind them
     const float inv = norm_load<kFAttnThreads>(xs, emb_row, a.x_in, d, a.eps, red, a.x_mid, a.x_zero,
-                                h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst, kFfnCopies);
+                                h == 0 ? r0 : 0, h == 0 ? r1 : 0, cst, kFfnCopies, a.g_att);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(&st->err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -289,9 +283,6 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
     __syncthreads();
     const bool ok = s_fail == 0;  // on a timeout the exchanges still run (every CTA
                                   // sends its rows and partials), with zeros
-    if (!ok)
-        for (int i = tid; i < d; i += kFAttnThreads) gs[i] = 0.0f;
-    norm_scale<kFAttnThreads>(xs, gs, inv, d);
 
     // ---- Q/K/V rows of this CTA (pairs per warp: RoPE needs both)
     cluster_wait_all();  // every CTA of the cluster runs: remote writes allowed
@@ -301,8 +292,8 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
         if (ok) {
             const float2 r = warp_dot2(wq + static_cast<size_t>(tl) * d,
                                        wq + static_cast<size_t>(tl + 1) * d, xs, d, lane);
-            v0 = r.x;
-            v1 = r.y;
+            v0 = r.x * inv;
+            v1 = r.y * inv;
         }
         if (tg < 2 * hd) {  // q or k: rotate the pair
             const float2 cs = rs[p];
@@ -510,7 +501,7 @@ __global__ void __maxnreg__(80) fattn_kernel(const __grid_constant__ FAttnArgs a
 
 // Shared-memory carve-up of the FFN block for at most `units` hidden units.
 struct FFfnLayout {
-    int off_w13, off_w2, off_x, off_hb, off_red, off_g, total;
+    int off_w13, off_w2, off_x, off_hb, off_red, total;
 };
 __host__ __device__ inline FFfnLayout fffn_layout(int d, int units) {
     FFfnLayout L;
@@ -519,8 +510,7 @@ __host__ __device__ inline FFfnLayout fffn_layout(int d, int units) {
     L.off_x = L.off_w2 + units * d;
     L.off_hb = L.off_x + ((d + 3) & ~3);
     L.off_red = L.off_hb + ((units + 3) & ~3);
-    L.off_g = L.off_red + 64;
-    L.total = L.off_g + ((d + 3) & ~3);
+    L.total = L.off_red + 64;
     return L;
 }
 
@@ -539,7 +529,6 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
     float* xs = sm + L.off_x;
     float* hb = sm + L.off_hb;
     float* red = sm + L.off_red;
-    float* gs = sm + L.off_g;
     __shared__ __align__(8) uint64_t wbar;
     __shared__ int s_fail;
 
@@ -553,8 +542,7 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
         const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
                                                 : make_policy_evict_last(__uint_as_float(
                                                       static_cast<uint32_t>(f.l2_policy)));
-        mbar_arrive_expect_tx(&wbar, static_cast<uint32_t>((3 * nu * d + d) * 4));
-        bulk_g2s(gs, f.g_ffn, static_cast<uint32_t>(d * 4), &wbar, pol);
+        mbar_arrive_expect_tx(&wbar, static_cast<uint32_t>(3 * nu * d * 4));
     }
     if (tid == 0 && nu > 0) {
         const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
@@ -573,7 +561,8 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
     const int q0 = static_cast<int>(static_cast<long long>(d) * c / G);
     const int q1 = static_cast<int>(static_cast<long long>(d) * (c + 1) / G);
     long long* x_out = f.x_out + static_cast<size_t>(c % kFfnCopies) * d;  // this CTA's copy
-    const float inv = norm_load<kFFfnThreads>(xs, nullptr, f.x_mid, d, f.eps, red, x_out, f.x_zero, q0, q1);
+    const float inv = norm_load<kFFfnThreads>(xs, nullptr, f.x_mid, d, f.eps, red, x_out, f.x_zero,
+                                              q0, q1, nullptr, 1, f.g_ffn);
     if (!mbar_wait_bounded(&wbar, 0u) && tid == 0) {
         atomicOr(f.err, ERR_TIMEOUT_TMA);
         s_fail = 1;
@@ -581,13 +570,13 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
     }
     __syncthreads();
     if (s_fail || nu == 0) return;
-    norm_scale<kFFfnThreads>(xs, gs, inv, d);
 
     // SwiGLU of the CTA's hidden units (interleaved rows: 2u gate, 2u + 1 up)
     for (int u = warp; u < nu; u += kFFfnWarps) {
         const float2 gu = warp_dot2(w13 + static_cast<size_t>(2 * u) * d,
                                     w13 + static_cast<size_t>(2 * u + 1) * d, xs, d, lane);
-        if (lane == 0) hb[u] = (gu.x / (1.0f + expf(-gu.x))) * gu.y;
+        const float gt = gu.x * inv, up = gu.y * inv;
+        if (lane == 0) hb[u] = (gt / (1.0f + expf(-gt))) * up;
     }
     __syncthreads();
     // their contribution to every output: y[i] = sum_u W2[i][u0 + u] hb[u]
