@@ -561,7 +561,7 @@ def run_ours(args, world, rank, local):
     # every kernel kind of the forward, timed live at the same position
     kinds = {}
     for kind in range(6):
-        t = l2.l2_time_kernel(dec.h, kind, pos_mid, iters if kind < 5 else 8, stream)
+        t = median_time(l2, dec.h, kind, pos_mid, iters if kind < 5 else 8, stream)
         b = l2.l2_kernel_bytes(dec.h, kind, pos_mid)
         kinds[l2.KERNEL_KINDS[kind]] = {
             "launch_ms": t, "GB/s": b / (t / 1e3) / 1e9, "frac": b / (t / 1e3) / 1e9 / peak,
@@ -734,6 +734,12 @@ def batched_gemm_shape(cfg, kind):
     return {6: (d + 2 * kvd, d), 8: (d, d), 9: (2 * F, d), 10: (d, F), 11: (V, d)}.get(kind)
 
 
+def median_time(l2, h, kind, pos, iters, stream, reps=3):
+    """Per-launch time of one kernel kind: the median of `reps` timed loops of
+    `iters` launches (one loop can catch a clock or scheduling excursion)."""
+    return float(np.median([l2.l2_time_kernel(h, kind, pos, iters, stream) for _ in range(reps)]))
+
+
 def run_ours_batched(args, world, rank, local, compact=False):
     """Batch 256 on the 44M shape: one step = one l2_generate_batch_device of
     the whole workload (every sequence's prompt and generated positions,
@@ -807,7 +813,7 @@ def run_ours_batched(args, world, rank, local, compact=False):
     pos_mid = int(np.mean(lens)) - 1 + steps // 2
     per = {}
     for kind, name in BATCHED_KINDS.items():
-        t = l2.l2_time_kernel(dec.h, kind, pos_mid, 3 * L, stream)
+        t = median_time(l2, dec.h, kind, pos_mid, 3 * L, stream)
         launches = {11: 1, 12: 1}.get(kind, L)
         shp = batched_gemm_shape(cfg, kind)
         flops = 2.0 * B * shp[0] * shp[1] if shp else 0.0
