@@ -63,7 +63,7 @@ struct l2_handle {
     int a_rows = 128;                  // rows of the GEMMs' A tiles: 64 when rows <= 64
     // 64-row handles whose QKV / W1W3 / classifier launches are drained: the
     // *_hi copy holds W * g in fp32 (no lo copy), split in shared memory
-    bool conv_qkv = false, conv_w13 = false, conv_cls = false;
+    bool conv_qkv = false, conv_wo = false, conv_w13 = false, conv_w2 = false, conv_cls = false;
     float* bw = nullptr;
     float *qkv_hi = nullptr, *qkv_lo = nullptr, *wo_hi = nullptr, *wo_lo = nullptr;
     float *w13_hi = nullptr, *w13_lo = nullptr, *w2_hi = nullptr, *w2_lo = nullptr;
@@ -477,7 +477,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.x_lo = h->xn_lo;
             g.ss_out = h->ss_ffn;
             g.ss_stride = h->ss_stride;
-            g.conv = h->a_rows == 64 ? 1 : 0;  // fp32 Wo split in shared memory (no gain)
+            g.conv = h->conv_wo ? 1 : 0;  // fp32 Wo split in shared memory (no gain)
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_wo, g.N, g.K), h->m_wo, g, s, true);
         case BK_W13:
             g.N = 2 * F;
@@ -499,7 +499,7 @@ cudaError_t launch_bkind(l2_handle* h, int kind, int l, int row0, int M, int mod
             g.x_lo = h->xn_lo;
             g.ss_out = h->ss_att;
             g.ss_stride = h->ss_stride;
-            g.conv = h->a_rows == 64 ? 1 : 0;  // fp32 W2 split in shared memory (no gain)
+            g.conv = h->conv_w2 ? 1 : 0;  // fp32 W2 split in shared memory (no gain)
             return launch_gemm(GEPI_RESIDUAL, plan(h->gp_w2, g.N, g.K), h->m_w2, g, s, true);
         case BK_CLS:
             g.layer = 0;
@@ -655,15 +655,6 @@ int setup_batched(l2_handle* h) {
     };
     const size_t n_qkv = L * (d + 2 * kvd) * d, n_wo = L * d * d, n_w13 = L * 2 * F * d;
     const size_t n_w2 = L * d * F, n_cls = V * d;
-    const size_t o_qh = take(n_qkv), o_ql = take(n_qkv), o_oh = take(n_wo), o_ol = take(n_wo);
-    const size_t o_uh = take(n_w13), o_ul = take(n_w13), o_dh = take(n_w2), o_dl = take(n_w2);
-    const size_t o_ch = take(n_cls), o_cl = take(n_cls);
-    L2_CUDA(h, cudaMalloc(&h->bw, off * sizeof(float)));
-    h->qkv_hi = h->bw + o_qh; h->qkv_lo = h->bw + o_ql;
-    h->wo_hi = h->bw + o_oh; h->wo_lo = h->bw + o_ol;
-    h->w13_hi = h->bw + o_uh; h->w13_lo = h->bw + o_ul;
-    h->w2_hi = h->bw + o_dh; h->w2_lo = h->bw + o_dl;
-    h->cls_hi = h->bw + o_ch; h->cls_lo = h->bw + o_cl;
     cudaStream_t s = h->stream;
     L2_CUDA(h, prepare_gemm(&h->gocc));
     const int Mb = static_cast<int>(RW);
@@ -677,23 +668,44 @@ int setup_batched(l2_handle* h) {
     h->gp_w13 = plan_gemm(h->gocc, Mb, static_cast<int>(2 * F), static_cast<int>(d), 256, ar);
     h->gp_w2 = plan_gemm(h->gocc, Mb, static_cast<int>(d), static_cast<int>(F), 128, ar);
     h->gp_cls = plan_gemm(h->gocc, Mb, static_cast<int>(V), static_cast<int>(d), 256, ar);
+    // 64-row handles whose launches are drained split fp32 weights in shared
+    // memory: no tf32 pair copy for them (Wo, W2: the weights themselves;
+    // QKV, W1/W3, classifier: W * g in fp32 in the hi buffer)
     h->conv_qkv = ar == 64 && gemm_drained(h->gp_qkv, static_cast<int>(d));
+    h->conv_wo = ar == 64 && gemm_drained(h->gp_wo, static_cast<int>(d));
     h->conv_w13 = ar == 64 && gemm_drained(h->gp_w13, static_cast<int>(d));
+    h->conv_w2 = ar == 64 && gemm_drained(h->gp_w2, static_cast<int>(F));
     h->conv_cls = ar == 64 && gemm_drained(h->gp_cls, static_cast<int>(d));
+    const size_t o_qh = take(n_qkv), o_ql = h->conv_qkv ? 0 : take(n_qkv);
+    const size_t o_oh = h->conv_wo ? 0 : take(n_wo), o_ol = h->conv_wo ? 0 : take(n_wo);
+    const size_t o_uh = take(n_w13), o_ul = h->conv_w13 ? 0 : take(n_w13);
+    const size_t o_dh = h->conv_w2 ? 0 : take(n_w2), o_dl = h->conv_w2 ? 0 : take(n_w2);
+    const size_t o_ch = take(n_cls), o_cl = h->conv_cls ? 0 : take(n_cls);
+    L2_CUDA(h, cudaMalloc(&h->bw, off * sizeof(float)));
+    // buffers that are not allocated alias one of the same size that is, so
+    // that every tensor map stays valid; their launches never read them
+    h->qkv_hi = h->bw + o_qh;
+    h->qkv_lo = h->conv_qkv ? h->qkv_hi : h->bw + o_ql;
+    h->wo_hi = h->conv_wo ? h->wo : h->bw + o_oh;
+    h->wo_lo = h->conv_wo ? h->wo : h->bw + o_ol;
+    h->w13_hi = h->bw + o_uh;
+    h->w13_lo = h->conv_w13 ? h->w13_hi : h->bw + o_ul;
+    h->w2_hi = h->conv_w2 ? h->w2 : h->bw + o_dh;
+    h->w2_lo = h->conv_w2 ? h->w2 : h->bw + o_dl;
+    h->cls_hi = h->bw + o_ch;
+    h->cls_lo = h->conv_cls ? h->cls_hi : h->bw + o_cl;
     // the GEMMs that consume a normalised row carry the RMSNorm gain in their
-    // weights (W[n][k] * g[k]); the row scale is applied in their epilogue.
-    // Launches that split W in shared memory read W * g in fp32 from the hi
-    // copy (the lo copy is not read).
+    // weights (W[n][k] * g[k]); the row scale is applied in their epilogue
     if (h->conv_qkv)
         L2_CUDA(h, launch_scale_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, s));
     else
         L2_CUDA(h, launch_split_tf32_gain(h->wqkv, h->g_att, d, d + 2 * kvd, L, h->qkv_hi, h->qkv_lo, s));
-    L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
+    if (!h->conv_wo) L2_CUDA(h, launch_split_tf32(h->wo, h->wo_hi, h->wo_lo, n_wo, s));
     if (h->conv_w13)
         L2_CUDA(h, launch_scale_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, s));
     else
         L2_CUDA(h, launch_split_tf32_gain(h->w13, h->g_ffn, d, 2 * F, L, h->w13_hi, h->w13_lo, s));
-    L2_CUDA(h, launch_split_tf32(h->w2, h->w2_hi, h->w2_lo, n_w2, s));
+    if (!h->conv_w2) L2_CUDA(h, launch_split_tf32(h->w2, h->w2_hi, h->w2_lo, n_w2, s));
     if (h->conv_cls)
         L2_CUDA(h, launch_scale_gain(h->wcls, h->g_final, d, V, 1, h->cls_hi, s));
     else

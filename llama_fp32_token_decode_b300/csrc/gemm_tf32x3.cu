@@ -1027,6 +1027,8 @@ cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cud
         }
         return cudaErrorInvalidValue;
     }
+    // a handle that kept no tf32 pair for this GEMM plans only drained launches
+    if (g.conv) return cudaErrorInvalidValue;
     return launch_bd<BN, false>(epi, m, g, ks, s, pdl);
 }
 
