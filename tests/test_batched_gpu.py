@@ -52,6 +52,10 @@ BATCHED = {
                         vocab_size=3001, seq_len=20, max_batch=130), 130),
     "b256_hd48_tied": (config(dim=288, hidden_dim=768, n_layers=1, n_heads=6, vocab_size=517,
                               seq_len=12, max_batch=256, shared_classifier=1), 256),
+    # at most 64 rows with K of 4096: drained launches that split fp32
+    # weights in shared memory (M = 64 MMAs), head_dim 128, GQA
+    "b6_wide_drained": (config(dim=4096, hidden_dim=4096, n_layers=1, n_heads=32, n_kv_heads=8,
+                               vocab_size=600, seq_len=12, max_batch=6), 6),
 }
 
 
