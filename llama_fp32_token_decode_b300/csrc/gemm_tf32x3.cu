@@ -150,16 +150,18 @@ struct Cfg {
         return drain ? 2 * BN : BN;
     }
     static constexpr int PS = BN + 4;  // row stride (floats) of a staged partial tile
-    // split-K receive buffer: one slot per peer, ceil(128 / S) rows of PS floats
-    __host__ __device__ static constexpr size_t recv_bytes(int ksplit) {
-        return ksplit > 1 ? static_cast<size_t>(ksplit - 1) * ((128 + ksplit - 1) / ksplit) * PS * 4
-                          : 0;
+    // split-K receive buffer: one slot per peer, ceil(a_rows / S) rows of PS
+    // floats (each CTA of the cluster owns that share of the tile's rows)
+    __host__ __device__ static constexpr size_t recv_bytes(int ksplit, int a_rows = 128) {
+        return ksplit > 1
+                   ? static_cast<size_t>(ksplit - 1) * ((a_rows + ksplit - 1) / ksplit) * PS * 4
+                   : 0;
     }
     // dynamic shared memory of a launch: alignment slack, a ring of `stages`
     // slots (>= 2: the staged partial tile reuses the first two), the receive
     // buffer of a split launch, barriers
     __host__ __device__ static constexpr size_t smem_for(int stages, int ksplit, int a_rows = 128) {
-        return 1024 + static_cast<size_t>(stages) * stage_bytes(a_rows) + recv_bytes(ksplit) + 256;
+        return 1024 + static_cast<size_t>(stages) * stage_bytes(a_rows) + recv_bytes(ksplit, a_rows) + 256;
     }
     static_assert(128 * PS * 4 <= 2 * STAGE, "partial tile must fit in two slots");
     static_assert(128 * PS * 4 <= 2 * (2 * 64 * BK * 4 + 2 * B_BYTES),
@@ -408,18 +410,27 @@ __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
 // S == 1: the epilogue runs on the register sums (thread = row). S > 1: every
 // CTA stages its partial tile in its own shared memory and pushes each peer's
 // row slice into that peer's receive buffer (bulk copy, completion on the
-// peer's mbarrier); CTA s adds rows [128 s / S, 128 (s+1) / S) of the S
-// partials in rank order (a fixed order: the result does not depend on
+// peer's mbarrier); CTA s adds rows [TR s / S, TR (s+1) / S) of the S
+// partials (TR = 128, or 64 with 64-row A tiles) in rank order (a fixed order: the result does not depend on
 // timing) and applies the epilogue to them.
-// CONV (drained launches of 64-row handles for the GEMMs without a folded
-// gain: Wo, W2): the weight tiles arrive as fp32 (one copy, half the bytes of
-// the tf32 pair) and kConvWarps extra warps split each landed tile in shared
+// CONV (drained launches of 64-row handles): the weight tiles arrive as fp32
+// (one copy, W * g where the RMSNorm gain is folded in, half the bytes of the
+// tf32 pair) and kConvWarps extra warps split each landed tile in shared
 // memory: the tensor core reads an fp32 operand as tf32 by dropping its 13
 // low mantissa bits, so hi = w stays in place and lo = w - trunc(w), exact in
 // fp32, goes to the lo tile (the tensor core truncates lo in turn: a relative
 // error below 2^-20 of w, against 2^-23 for the rounded pair of the copies);
-// the MMA warp waits for the split tile. (A folded gain would add a product
-// and a second store per element: measured slower than the pair copies.)
+// the MMA warp waits for the split tile.
+// SWAP (CONV with 128-wide tiles): the operands trade places, D^T = W x^T,
+// the 128 weight rows being the M = 128 operand and the tile's 64 rows the
+// N = 64 one. An M = 64 MMA keeps the tensor core as long as an M = 128 one,
+// so the 64-row tile costs half the tensor time this way; TMEM lane i then
+// holds weight row n0 + i and column t tile row t, the drain leaves each
+// thread one weight row's 64 sums, and the epilogue always stages the
+// partial tile (row-major, as the unswapped path does) before it reads it
+// back by rows, split or not. (Measured on the 7B-shape prefill GEMMs: the
+// mainloop was bound by the M = 64 MMAs at 0.7 us per K-block, the weight
+// stream alone running at 0.4.)
 constexpr int kConvWarps = 2;  // 8 warps in all: a ninth would cap a thread at 168 registers
 constexpr int gemm_threads(bool drain, bool conv = false) {
     return drain ? (conv ? 192 + 32 * kConvWarps : 192) : 256;
@@ -450,7 +461,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     const int nsplit = gridDim.x, split = blockIdx.x;
     const uint32_t recv_base = base + static_cast<uint32_t>(S * stage_b);
     uint64_t* full = reinterpret_cast<uint64_t*>(gbase + static_cast<size_t>(S) * stage_b +
-                                                 C::recv_bytes(nsplit));
+                                                 C::recv_bytes(nsplit, g.a_rows == 64 ? 64 : 128));
     uint64_t* empty = full + S;
     uint64_t* accfull = empty + S;   // [2] chunk accumulated in TMEM buffer b
     uint64_t* accfree = accfull + 2; // [2] TMEM buffer b drained
@@ -458,6 +469,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     uint64_t* convb = recvb + 1;     // CONV: [S] the slot's weight tile is split
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(convb + (CONV ? S : 0));
     static_assert(!CONV || DRAIN, "the split warps come with the drained layout");
+    // SWAP (CONV with 128-wide tiles, whose launches hold at most 64 rows): the
+    // weight tile is the M = 128 operand and the 64 rows the N = 64 one
+    constexpr bool SWAP = CONV && BN == 128;
+    constexpr int RN = SWAP ? 64 : BN;  // TMEM columns of one accumulator
     __shared__ int s_err;
     // QKV epilogue: state of the tile's rows, loaded once during the mainloop
     __shared__ RowState s_rows[EPI == GEPI_QKV_ROPE ? 128 : 1];
@@ -512,9 +527,11 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     auto b_hi = [&](int s) { return a_hi(s) + static_cast<uint32_t>(2 * a_bytes); };
     auto b_lo = [&](int s) { return b_hi(s) + C::B_BYTES; };
 
-    float R[DRAIN ? BN : 1];  // DRAIN, warps 0-3: this thread's row, summed over chunks
+    // DRAIN, warps 0-3: this thread's row of the tile (SWAP: its weight row's
+    // column of 64 tile rows), summed over chunks
+    float R[DRAIN ? RN : 1];
 #pragma unroll
-    for (int j = 0; j < (DRAIN ? BN : 1); ++j) R[j] = 0.0f;
+    for (int j = 0; j < (DRAIN ? RN : 1); ++j) R[j] = 0.0f;
 
     constexpr int kProdWarp = DRAIN ? 4 : 0, kMmaWarp = DRAIN ? 5 : 1;
     // bytes a slot's copies bring: with CONV one fp32 weight tile, not the pair
@@ -558,7 +575,9 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
         if (lane == 0) {
             // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1; 64-row
             // A tiles take M = 64 MMAs (half the tensor work and A reads)
-            const uint32_t idesc = g.a_rows == 64 ? idesc_tf32(64, BN) : idesc_tf32(128, BN);
+            const uint32_t idesc = SWAP             ? idesc_tf32(128, 64)
+                                   : g.a_rows == 64 ? idesc_tf32(64, BN)
+                                                    : idesc_tf32(128, BN);
             for (int i = 0; i < NK; ++i) {
                 const int c = i / CH, w = i % CH, buf = c & 1;
                 if (w == 0 && c >= 2 &&
@@ -573,16 +592,22 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + static_cast<uint32_t>(buf * BN);
+                const uint32_t acc = tmem + static_cast<uint32_t>(buf * RN);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint64_t ah = sw128_desc(a_hi(s) + 32 * k);
                     const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
                     const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
                     const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
-                    mma_tf32(acc, al, bh, idesc, (w | k) != 0);
-                    mma_tf32(acc, ah, bl, idesc, 1u);
-                    mma_tf32(acc, ah, bh, idesc, 1u);
+                    if constexpr (SWAP) {  // D^T = W x^T: the same three products
+                        mma_tf32(acc, bh, al, idesc, (w | k) != 0);
+                        mma_tf32(acc, bl, ah, idesc, 1u);
+                        mma_tf32(acc, bh, ah, idesc, 1u);
+                    } else {
+                        mma_tf32(acc, al, bh, idesc, (w | k) != 0);
+                        mma_tf32(acc, ah, bl, idesc, 1u);
+                        mma_tf32(acc, ah, bh, idesc, 1u);
+                    }
                 }
                 mma_commit(&empty[s]);
                 if (w == CH - 1 || i == NK - 1) mma_commit(&accfull[buf]);
@@ -651,10 +676,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
             }
             tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < BN / 32; ++j) {
+            for (int j = 0; j < RN / 32; ++j) {
                 float v[32];
                 __syncwarp();  // tcgen05.ld is warp-collective
-                tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * BN + 32 * j), v);
+                tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * RN + 32 * j), v);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) R[32 * j + t] += v[t];
             }
@@ -692,7 +717,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     };
     const int ss_slot = 2 * (n0 / BN);  // this tile's sum-of-squares slots
 
-    if (nsplit == 1) {
+    if (nsplit == 1 && !SWAP) {
         if (s_err) {
             if (threadIdx.x == 0) atomicOr(g.err, ERR_TIMEOUT_TMA);
         } else if (reader) {
@@ -705,7 +730,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
             if constexpr (DRAIN) {
                 if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < BN; j += 4) {
+                    for (int j = 0; j < RN; j += 4) {  // RN == BN on this path
                         const int gc = n0 + j;
                         if (gc < g.N) {
                             const float a4[4] = {R[j] * sc, R[j + 1] * sc, R[j + 2] * sc,
@@ -751,7 +776,12 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
         // stage this CTA's partial tile (row-major, stride PS) in the ring
         float* P = reinterpret_cast<float*>(gbase);
         if (reader) {
-            if constexpr (DRAIN) {
+            if constexpr (SWAP) {
+                // this thread's weight row is column n of the row-major tile
+                const int n = 32 * (warp & 3) + lane;
+#pragma unroll
+                for (int t = 0; t < 64; ++t) P[t * PS + n] = R[t];
+            } else if constexpr (DRAIN) {
                 if (row >= 0) {
 #pragma unroll
                     for (int j = 0; j < BN; j += 4)
@@ -778,7 +808,7 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
             fence_proxy_async_smem();
         }
         __syncthreads();
-        cluster_wait_acquire();  // every peer's barriers are initialised
+        if (nsplit > 1) cluster_wait_acquire();  // every peer's barriers are initialised
         const int R_ = (TR + nsplit - 1) / nsplit;  // rows of a receive slot
         const int r0 = TR * split / nsplit, r1 = TR * (split + 1) / nsplit;
         const uint32_t pbase = smem_u32(P);
@@ -1022,6 +1052,7 @@ cudaError_t launch_bn(int epi, const GemmMaps& m, const GemmArgs& g, int ks, cud
     const int per_cta = (KB + ks - 1) / ks;
     if (per_cta > kDrainAbove) {
         if constexpr (has_drain<BN>()) {
+            if (g.conv && g.a_rows != 64) return cudaErrorInvalidValue;  // tiles of <= 64 rows
             if (g.conv) return launch_bd<BN, true, true>(epi, m, g, ks, s, pdl);
             return launch_bd<BN, true>(epi, m, g, ks, s, pdl);
         }
