@@ -423,14 +423,12 @@ __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
 // the MMA warp waits for the split tile.
 // SWAP (CONV with 128-wide tiles): the operands trade places, D^T = W x^T,
 // the 128 weight rows being the M = 128 operand and the tile's 64 rows the
-// N = 64 one. An M = 64 MMA keeps the tensor core as long as an M = 128 one,
-// so the 64-row tile costs half the tensor time this way; TMEM lane i then
-// holds weight row n0 + i and column t tile row t, the drain leaves each
-// thread one weight row's 64 sums, and the epilogue always stages the
-// partial tile (row-major, as the unswapped path does) before it reads it
-// back by rows, split or not. (Measured on the 7B-shape prefill GEMMs: the
-// mainloop was bound by the M = 64 MMAs at 0.7 us per K-block, the weight
-// stream alone running at 0.4.)
+// N = 64 one. A tf32 MMA (K = 8) takes max(51, N / 2) cycles whether M is 64
+// or 128 (measured on B300), so the same products cost 51 cycles each
+// instead of 64; TMEM lane i then holds weight row n0 + i and column t tile
+// row t, the drain leaves each thread one weight row's 64 sums, and the
+// epilogue always stages the partial tile (row-major, as the unswapped path
+// does) before it reads it back by rows, split or not.
 constexpr int kConvWarps = 2;  // 8 warps in all: a ninth would cap a thread at 168 registers
 constexpr int gemm_threads(bool drain, bool conv = false) {
     return drain ? (conv ? 192 + 32 * kConvWarps : 192) : 256;
@@ -452,7 +450,8 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     constexpr int PS = C::PS;     // row stride of the staged partial (floats)
     // A tiles of g.a_rows rows (128, or 64 with M = 64 MMAs: launches of at
     // most 64 rows)
-    const int a_bytes = (g.a_rows == 64 ? 64 : 128) * C::BK * 4;
+    // (CONV launches always hold 64-row tiles: compile-time sizes there)
+    const int a_bytes = CONV ? 64 * C::BK * 4 : (g.a_rows == 64 ? 64 : 128) * C::BK * 4;
     const int stage_b = 2 * a_bytes + 2 * C::B_BYTES;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -553,9 +552,11 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
                 tma_load_3d(a_lo(i), &mA_lo, kc, m0, 0, &full[i]);
             }
             int issued = pre;
+            int s = 0;        // slot of K-block i (i % S), counted
+            uint32_t ph = 0;  // parity of the empty phase it waits for ((i / S - 1) & 1)
             for (int i = pre; i < NK; ++i) {
-                const int s = i % S, kc = (kb0 + i) * 32;
-                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / S - 1) & 1u)) {
+                const int kc = (kb0 + i) * 32;
+                if (!mbar_wait_bounded(&empty[s], ph)) {
                     s_err = 1;
                     break;
                 }
@@ -565,6 +566,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
                 tma_load_3d(a_hi(s), &mA_hi, kc, m0, 0, &full[s]);
                 tma_load_3d(a_lo(s), &mA_lo, kc, m0, 0, &full[s]);
                 issued = i + 1;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (s_err) {  // let the copies in flight land before the CTA leaves
                 for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
@@ -574,10 +579,21 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     } else if (warp == kMmaWarp && (DRAIN || lane == 0)) {
         if (lane == 0) {
             // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1; 64-row
-            // A tiles take M = 64 MMAs (half the tensor work and A reads)
+            // A tiles take M = 64 MMAs (half the tensor work and A reads). The
+            // one issuing thread sets the pace (each MMA waits for its own
+            // issue), so the loop keeps its per-MMA work to additions: the
+            // slot's descriptors come from the first slot's by constant
+            // offsets, and slot and phase advance by counting.
             const uint32_t idesc = SWAP             ? idesc_tf32(128, 64)
                                    : g.a_rows == 64 ? idesc_tf32(64, BN)
                                                     : idesc_tf32(128, BN);
+            const uint64_t d_base = sw128_desc(base);  // Ahi of slot 0
+            const uint64_t d_slot = static_cast<uint64_t>(stage_b >> 4);
+            const uint64_t o_al = static_cast<uint64_t>(a_bytes >> 4);
+            const uint64_t o_bh = static_cast<uint64_t>((2 * a_bytes) >> 4);
+            const uint64_t o_bl = o_bh + static_cast<uint64_t>(C::B_BYTES >> 4);
+            int s = 0;
+            uint32_t ph = 0;  // phase parity of slot s's barriers
             for (int i = 0; i < NK; ++i) {
                 const int c = i / CH, w = i % CH, buf = c & 1;
                 if (w == 0 && c >= 2 &&
@@ -585,20 +601,23 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
                     s_err = 1;
                     break;
                 }
-                const int s = i % S;
                 uint64_t* ready = CONV ? &convb[s] : &full[s];
-                if (!mbar_wait_bounded(ready, static_cast<uint32_t>(i / S) & 1u)) {
+                if (!mbar_wait_bounded(ready, ph)) {
                     s_err = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t acc = tmem + static_cast<uint32_t>(buf * RN);
+                // descriptor start addresses are in 16-byte units: + 2 per
+                // 32-byte K step (the slots lie within shared memory, so the
+                // 14-bit field does not carry)
+                const uint64_t d_ah = d_base + static_cast<uint64_t>(s) * d_slot;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint64_t ah = sw128_desc(a_hi(s) + 32 * k);
-                    const uint64_t al = sw128_desc(a_lo(s) + 32 * k);
-                    const uint64_t bh = sw128_desc(b_hi(s) + 32 * k);
-                    const uint64_t bl = sw128_desc(b_lo(s) + 32 * k);
+                    const uint64_t ah = d_ah + 2 * k;
+                    const uint64_t al = ah + o_al;
+                    const uint64_t bh = ah + o_bh;
+                    const uint64_t bl = ah + o_bl;
                     if constexpr (SWAP) {  // D^T = W x^T: the same three products
                         mma_tf32(acc, bh, al, idesc, (w | k) != 0);
                         mma_tf32(acc, bl, ah, idesc, 1u);
@@ -611,6 +630,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
                 }
                 mma_commit(&empty[s]);
                 if (w == CH - 1 || i == NK - 1) mma_commit(&accfull[buf]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
     } else if (CONV && warp >= 6) {
@@ -620,9 +643,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
         constexpr int NCV = 32 * kConvWarps;
         constexpr int PER = BN * 8 / NCV;  // float4 per thread and tile
         static_assert(BN * 8 % NCV == 0, "whole float4 passes over a tile");
+        int s = 0;
+        uint32_t ph = 0;  // slot i % S and parity (i / S) & 1, counted
         for (int i = 0; i < NK; ++i) {
-            const int s = i % S;
-            if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / S) & 1u)) {
+            if (!mbar_wait_bounded(&full[s], ph)) {
                 s_err = 1;
                 break;
             }
@@ -638,6 +662,10 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
             fence_proxy_async_smem();  // the tensor core reads what was just written
             __syncwarp();
             if (lane == 0) mbar_arrive(&convb[s]);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
     } else if constexpr (!DRAIN) {
         // the other warps wait below for the single accumulator; warp 2 first
