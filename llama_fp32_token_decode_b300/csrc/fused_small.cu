@@ -538,12 +538,7 @@ __global__ void __launch_bounds__(kFFfnThreads) fffn_kernel(const __grid_constan
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
-                                                : make_policy_evict_last(__uint_as_float(
-                                                      static_cast<uint32_t>(f.l2_policy)));
-        mbar_arrive_expect_tx(&wbar, static_cast<uint32_t>(3 * nu * d * 4));
-    }
+    if (tid == 0) mbar_arrive_expect_tx(&wbar, static_cast<uint32_t>(3 * nu * d * 4));
     if (tid == 0 && nu > 0) {
         const uint64_t pol = (f.l2_policy == 0) ? make_policy_evict_first()
                                                 : make_policy_evict_last(__uint_as_float(
