@@ -411,8 +411,9 @@ __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
 // CTA stages its partial tile in its own shared memory and pushes each peer's
 // row slice into that peer's receive buffer (bulk copy, completion on the
 // peer's mbarrier); CTA s adds rows [TR s / S, TR (s+1) / S) of the S
-// partials (TR = 128, or 64 with 64-row A tiles) in rank order (a fixed order: the result does not depend on
-// timing) and applies the epilogue to them.
+// partials (TR = 128, or 64 with 64-row A tiles) in rank order (a fixed
+// order: the result does not depend on timing) and applies the epilogue to
+// them.
 // CONV (drained launches of 64-row handles): the weight tiles arrive as fp32
 // (one copy, W * g where the RMSNorm gain is folded in, half the bytes of the
 // tf32 pair) and kConvWarps extra warps split each landed tile in shared
@@ -579,11 +580,12 @@ __global__ void __launch_bounds__(gemm_threads(DRAIN, CONV), 1)
     } else if (warp == kMmaWarp && (DRAIN || lane == 0)) {
         if (lane == 0) {
             // ---- MMA issuer: chunk c accumulates in TMEM buffer c & 1; 64-row
-            // A tiles take M = 64 MMAs (half the tensor work and A reads). The
-            // one issuing thread sets the pace (each MMA waits for its own
-            // issue), so the loop keeps its per-MMA work to additions: the
-            // slot's descriptors come from the first slot's by constant
-            // offsets, and slot and phase advance by counting.
+            // A tiles take M = 64 MMAs (half the A reads), or with SWAP the
+            // weight tile is M and the rows N = 64. The one issuing thread
+            // sets the pace (each MMA waits for its own issue), so the loop
+            // keeps its per-MMA work to additions: the slot's descriptors come
+            // from the first slot's by constant offsets, and slot and phase
+            // advance by counting.
             const uint32_t idesc = SWAP             ? idesc_tf32(128, 64)
                                    : g.a_rows == 64 ? idesc_tf32(64, BN)
                                                     : idesc_tf32(128, BN);
