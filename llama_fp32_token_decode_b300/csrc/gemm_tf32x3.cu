@@ -405,7 +405,9 @@ __device__ __forceinline__ RowState load_row_state(const GemmArgs& g, int r) {
 // kChunk K-blocks go into one of two TMEM accumulators in turn, and warps 0-3
 // drain each finished chunk into registers with ordinary fp32 additions while
 // the next chunk accumulates in the other buffer (accfull / accfree
-// barriers): about 5e-7 at any K.
+// barriers): about 1e-6 at any K with 4-block chunks (2-block chunks halve
+// that and cost the MMA thread twice the commits and waits: the 7B-shape
+// prefill GEMMs 2-3 % slower).
 //
 // S == 1: the epilogue runs on the register sums (thread = row). S > 1: every
 // CTA stages its partial tile in its own shared memory and pushes each peer's
@@ -434,7 +436,7 @@ constexpr int kConvWarps = 2;  // 8 warps in all: a ninth would cap a thread at 
 constexpr int gemm_threads(bool drain, bool conv = false) {
     return drain ? (conv ? 192 + 32 * kConvWarps : 192) : 256;
 }
-constexpr int kChunk = 2;         // K-blocks per TMEM accumulation chunk (DRAIN)
+constexpr int kChunk = 4;         // K-blocks per TMEM accumulation chunk (DRAIN)
 constexpr int kDrainAbove = 16;   // a CTA with more K-blocks than this drains chunks
 
 // DRAIN == false (a CTA's K range is at most kDrainAbove K-blocks, error below
